@@ -1,0 +1,219 @@
+/*
+ * ds4g.h — C ABI of the B300 routed-MoE block (libds4g.so).
+ *
+ * What it computes: the routed mixture-of-experts feed-forward block of
+ * DeepSeek V4 Flash as the ds4 engine runs it with 2-bit experts:
+ *   router scores -> top-6 of 256 experts -> for each selected expert a
+ *   dequantise-inside-the-matmul SwiGLU MLP (gate/up IQ2_XXS, down Q2_K, or
+ *   Q4_K for the q4 layers) -> weighted sum -> plus an always-on bf16 shared
+ *   expert.
+ *
+ * Sources (web pages describing the ds4 engine):
+ *   [P1] chenxutan.com, "ds4 深度实战：当 Redis 之父用纯 C 重写本地推理引擎":
+ *        §2.1 (asymmetric 2-bit policy: gate/up IQ2_XXS, down Q2_K, shared
+ *        expert and router kept at high precision), §2.3 (router+expert fusion,
+ *        model-specific memory layout, chunked prefill), §3.2 (moe_forward:
+ *        router -> only the routed experts -> shared expert -> merge).
+ *   [P5] juejin.cn, "Redis 作者出手！ds4：用 C 语言从零打造 DeepSeek V4 Flash
+ *        本地推理引擎": §2.1 (model constants: 4096 embd, 256 experts, 6 used,
+ *        1 shared, 2048 expert FFN), §2.3 (block_q2_K 84 B and block_iq2_xxs
+ *        66 B per 256 weights), §2.4 (the IQ2 grid-row dot kernel: a grid row is
+ *        8 int8 values).
+ * Where the pages are silent (score function, bias use, tie rule, inner bit
+ * layout of the blocks, SwiGLU, RMS norm) the reading taken is stated at the
+ * entry point that depends on it.
+ *
+ * Conventions (all entry points):
+ *  - Dimensions are fixed: H = 4096 (hidden), F = 2048 (expert FFN),
+ *    E = 256 experts, K = 6 used per token.  Other shapes -> DS4G_EUNSUPPORTED.
+ *  - "dev" pointers are CUDA device pointers owned by the caller; "host"
+ *    pointers are ordinary host memory owned by the caller.  The library never
+ *    frees or retains a caller pointer beyond the call.
+ *  - Every dev pointer must be 16-byte aligned, else DS4G_EALIGN.
+ *  - All argument checks run on the host before any launch; a failed check
+ *    launches nothing.  A failed launch returns DS4G_ECUDA.
+ *  - GPU entry points are asynchronous on the given stream (0 = legacy
+ *    default stream).  Faults the kernels detect (an expert id outside
+ *    [0,256)) are recorded in a status word at the start of the workspace and
+ *    read back by ds4g_last_error(); no kernel traps or spins unboundedly.
+ *  - Hot entry points allocate nothing: scratch comes from the caller's
+ *    workspace, sized by the matching *_workspace() query.
+ *  - Row-major everywhere: hidden[T][4096]; a weight matrix [rows][cols] has
+ *    rows = output features, cols = input features.
+ */
+#ifndef DS4G_H
+#define DS4G_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *ds4g_stream_t; /* == cudaStream_t */
+
+#define DS4G_N_EMBD        4096
+#define DS4G_N_FF_EXP      2048
+#define DS4G_N_EXPERT      256
+#define DS4G_N_EXPERT_USED 6
+
+typedef enum {
+    DS4G_OK = 0,
+    DS4G_EINVAL = 1,       /* NULL pointer, T < 1, bad enum, inconsistent sizes */
+    DS4G_EALIGN = 2,       /* a device pointer is not 16-byte aligned          */
+    DS4G_ENOSPACE = 3,     /* workspace or output buffer too small             */
+    DS4G_ECUDA = 4,        /* a CUDA runtime call or launch failed             */
+    DS4G_EUNSUPPORTED = 5, /* shape or type combination not implemented        */
+    DS4G_ETIMEOUT = 6,     /* a bounded device wait gave up                    */
+    DS4G_EDEVICE = 7       /* a kernel flagged bad data (e.g. expert id >= 256)*/
+} ds4g_status;
+
+typedef enum {
+    DS4G_IQ2_XXS = 0, /* 66 B / 256 weights: fp16 d, 64 B of grid/sign codes  */
+    DS4G_Q2_K = 1,    /* 84 B / 256: scales[16], qs[64], fp16 d, fp16 dmin    */
+    DS4G_Q4_K = 2,    /* 144 B / 256: fp16 d, fp16 dmin, scales[12], qs[128]  */
+    DS4G_BF16 = 3     /* plain bf16, 2 B / weight                              */
+} ds4g_qtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *ds4g_status_str(ds4g_status s);
+
+/* ------------------------------------------------------------------------
+ * Block formats and the device layout ("model-specific memory layout",
+ * [P1] §2.3).  The GGUF-format blocks are the structs of [P5] §2.3 laid end to
+ * end, row by row (row r, block b at byte (r*cols/256 + b)*block_bytes).
+ * The device ("packed") layout is a pure byte/bit permutation of the same
+ * content into 16-row tiles so that each GPU lane reads exactly the codes it
+ * multiplies; it holds the same number of bytes.  No arithmetic is done.
+ * ------------------------------------------------------------------------ */
+
+/* Bytes of one 256-weight block in GGUF format (66, 84, 144; 512 for BF16). */
+size_t ds4g_block_bytes(ds4g_qtype t);
+
+/* Bytes of a packed [rows][cols] matrix (== GGUF bytes).  0 if the shape is
+ * invalid (rows % 16 != 0 or cols % 256 != 0) or t is DS4G_BF16. */
+size_t ds4g_packed_size(ds4g_qtype t, int rows, int cols);
+
+/* Host-only.  GGUF-format blocks (host, in_bytes) -> packed layout (host,
+ * out_bytes).  Layout only.  Errors: EINVAL (NULL, bad type), EUNSUPPORTED
+ * (shape), ENOSPACE (in_bytes or out_bytes below ds4g_packed_size). */
+ds4g_status ds4g_quantize_pack(ds4g_qtype t, int rows, int cols,
+                               const void *gguf_blocks, size_t in_bytes,
+                               void *packed, size_t out_bytes);
+
+/* Host-only inverse of ds4g_quantize_pack (used by tests: round trip). */
+ds4g_status ds4g_unpack(ds4g_qtype t, int rows, int cols,
+                        const void *packed, size_t in_bytes,
+                        void *gguf_blocks, size_t out_bytes);
+
+/* Device twin of ds4g_quantize_pack for resident model loading: gguf_dev and
+ * packed_dev are device buffers of ds4g_packed_size() bytes (must not
+ * overlap).  Asynchronous on stream s.  Same errors as the host version plus
+ * EALIGN / ECUDA. */
+ds4g_status ds4g_quantize_pack_device(ds4g_qtype t, int rows, int cols,
+                                      const void *gguf_dev, void *packed_dev,
+                                      ds4g_stream_t s);
+
+/* Dequantise a packed matrix to fp32 and/or bf16 (bf16 = round-to-nearest-
+ * even of the fp32 value).  Exposes the arithmetic the MoE kernels use so it
+ * can be checked bit for bit:
+ *   IQ2_XXS: w = ((d * (0.5 + ls)) * 0.25) * (+-grid[a][j])       ([P5] §2.3)
+ *   Q2_K/Q4_K: w = fma(d * sc, q, -(dmin * m))
+ * each step one IEEE fp32 rounding.  iq2_grid (dev, 256 x 8 int8 packed as
+ * uint64, little-endian bytes) is required for IQ2_XXS, ignored otherwise.
+ * out_f32 [rows][cols] and out_bf16 [rows][cols] (bf16 bits) are dev; either
+ * may be NULL but not both. */
+ds4g_status ds4g_dequantize(ds4g_qtype t, const void *packed, int rows, int cols,
+                            const uint64_t *iq2_grid, float *out_f32,
+                            uint16_t *out_bf16, ds4g_stream_t s);
+
+/* ------------------------------------------------------------------------
+ * Router ([P1] §3.2 "Router 计算专家选择"; [P5] §2.1 DS4_N_EXPERT_USED = 6).
+ * For each token t (reading for what the pages leave open: sigmoid scores,
+ * bias used only to select, ties to the lower expert id, weights = selected
+ * unbiased scores renormalised to sum 1, no extra scale factor):
+ *   logit_e = sum_j hidden[t][j] * router[e][j]       (fp32 accumulate)
+ *   s_e     = 1 / (1 + exp(-logit_e))
+ *   ids[t]  = the 6 experts with the largest s_e + bias[e], largest first,
+ *             equal keys -> lower e first
+ *   w[t][k] = s_{ids[t][k]} / sum_k' s_{ids[t][k']}
+ * hidden [T][4096] f32 dev, router [256][4096] f32 dev, bias [256] f32 dev,
+ * ids [T][6] int32 dev, w [T][6] f32 dev, workspace dev of at least
+ * ds4g_route_workspace(T) bytes (holds the status word and the logits).
+ * ------------------------------------------------------------------------ */
+size_t ds4g_route_workspace(int T);
+ds4g_status ds4g_moe_route(const float *hidden, int T, const float *router,
+                           const float *bias, int32_t *ids, float *w,
+                           void *workspace, size_t ws_bytes, ds4g_stream_t s);
+
+/* ------------------------------------------------------------------------
+ * Token -> expert bucketing (batched decode and chunked prefill, [P1] §2.3).
+ * For the 6T entries (t,k) in row-major order:
+ *   counts[e]   = number of entries with ids[t][k] == e          (e < 256)
+ *   offsets[e]  = sum_{e' < e} counts[e'];  offsets[256] = 6T
+ *   perm[offsets[e] + r] = t*6 + k of the r-th entry (in (t,k) order) of e
+ *   inv[t*6 + k] = its position in perm  (perm[inv[i]] == i)
+ * Integer work, bit-exact.  All arrays dev int32.  An id outside [0,256)
+ * sets DS4G_EDEVICE in the workspace status word and is counted nowhere.
+ * ------------------------------------------------------------------------ */
+size_t ds4g_bucket_workspace(int T);
+ds4g_status ds4g_moe_bucket(const int32_t *ids, int T, int32_t *counts,
+                            int32_t *offsets, int32_t *perm, int32_t *inv,
+                            void *workspace, size_t ws_bytes, ds4g_stream_t s);
+
+/* ------------------------------------------------------------------------
+ * One MoE layer's weights, all device memory owned by the caller.
+ * gate/up/down are device arrays of 256 device pointers, one packed matrix
+ * per expert: gate/up [2048][4096] of gate_up_type, down [4096][2048] of
+ * down_type.  Supported pairs: (IQ2_XXS, Q2_K) — the q2 layers — and
+ * (Q4_K, Q4_K) — the q4 layers of the q2-q4 model ([P1] §2.1).
+ * Shared expert: bf16 bits, row-major, sh_gate/sh_up [2048][4096],
+ * sh_down [4096][2048] (kept unquantised, [P1] §2.1).
+ * iq2_grid: 256 rows of 8 int8 grid values (IQ2_XXS codebook), dev.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+    ds4g_qtype gate_up_type;
+    ds4g_qtype down_type;
+    const void *const *gate;
+    const void *const *up;
+    const void *const *down;
+    const uint16_t *sh_gate;
+    const uint16_t *sh_up;
+    const uint16_t *sh_down;
+    const uint64_t *iq2_grid;
+} ds4g_layer;
+
+/* ------------------------------------------------------------------------
+ * The MoE block given the routing ([P1] §3.2 moe_forward).  For each token t:
+ *   for k in 0..5, e = ids[t][k]:
+ *     g = G_e x, u = U_e x  (weights dequantised inside the matmul)
+ *     h_k = silu(g) * u                        (SwiGLU, no clamp)
+ *     y_k = D_e h_k
+ *   s = Sd (silu(Sg x) * (Su x))                (bf16 shared expert)
+ *   out[t] = s + sum_{k=0..5} w[t][k] * y_k     (fixed k order, no atomics)
+ * hidden [T][4096] f32 dev, ids [T][6] int32 dev, w [T][6] f32 dev,
+ * out [T][4096] f32 dev.  A repeated id within a token is legal (both terms
+ * are summed).  Arithmetic: fp32 accumulation; activations enter the tensor
+ * cores as an fp16 hi+lo pair for small T (|x| < 65504 required) and as bf16
+ * for the bucketed prefill path (large T), where weights are bf16-rounded.
+ * workspace dev >= ds4g_forward_workspace(T) bytes.
+ * ------------------------------------------------------------------------ */
+size_t ds4g_forward_workspace(int T);
+ds4g_status ds4g_moe_forward(const float *hidden, int T, const ds4g_layer *L,
+                             const int32_t *ids, const float *w, float *out,
+                             void *workspace, size_t ws_bytes, ds4g_stream_t s);
+
+/* RMS norm between chained layers (pages silent; reading: eps = 1e-6, no
+ * learned gain): y[t] = x[t] / sqrt(mean_j x[t][j]^2 + 1e-6).  In place
+ * (x == y) is allowed.  x, y [T][4096] f32 dev. */
+ds4g_status ds4g_rmsnorm(const float *x, int T, float *y, ds4g_stream_t s);
+
+/* Synchronises stream s, reads the status word in workspace (dev) and
+ * returns it (DS4G_OK if no kernel flagged anything), then clears it. */
+ds4g_status ds4g_last_error(void *workspace, ds4g_stream_t s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DS4G_H */
