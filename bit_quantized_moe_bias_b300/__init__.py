@@ -1,0 +1,234 @@
+"""Python binding of libds4g.so — the B300 routed-MoE block of DeepSeek V4
+Flash with 2-bit experts (IQ2_XXS gate/up, Q2_K down; Q4_K for q4 layers).
+
+Argument marshalling only: every step of the block runs in the library's
+CUDA kernels.  Function names match the C ABI in include/ds4g.h; device
+buffers are torch tensors (``data_ptr()``), streams default to torch's current
+stream.  There is no fallback: if libds4g.so is missing or a call fails, an
+exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import re
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SO = os.path.join(_HERE, "libds4g.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "ds4g.h")
+
+DS4G_IQ2_XXS, DS4G_Q2_K, DS4G_Q4_K, DS4G_BF16 = 0, 1, 2, 3
+N_EMBD, N_FF_EXP, N_EXPERT, N_EXPERT_USED = 4096, 2048, 256, 6
+STATUS = {0: "DS4G_OK", 1: "DS4G_EINVAL", 2: "DS4G_EALIGN", 3: "DS4G_ENOSPACE", 4: "DS4G_ECUDA",
+          5: "DS4G_EUNSUPPORTED", 6: "DS4G_ETIMEOUT", 7: "DS4G_EDEVICE"}
+
+
+class DS4GError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {STATUS.get(code, code)}")
+        self.code = code
+
+
+class ds4g_layer(C.Structure):
+    _fields_ = [("gate_up_type", C.c_int), ("down_type", C.c_int), ("gate", C.c_void_p),
+                ("up", C.c_void_p), ("down", C.c_void_p), ("sh_gate", C.c_void_p),
+                ("sh_up", C.c_void_p), ("sh_down", C.c_void_p), ("iq2_grid", C.c_void_p)]
+
+
+_lib = None
+_FWD_SIG = None
+
+
+def lib():
+    """Load libds4g.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_SO):
+            raise RuntimeError(f"{_SO} is not built; run bit_quantized_moe_bias_b300/build.py")
+        L = C.CDLL(_SO)
+        vp, i, sz = C.c_void_p, C.c_int, C.c_size_t
+        fwd = [vp, i, C.POINTER(ds4g_layer), vp, vp, vp, vp, sz, vp]
+        sig = {
+            "ds4g_status_str": ([i], C.c_char_p),
+            "ds4g_block_bytes": ([i], sz),
+            "ds4g_packed_size": ([i, i, i], sz),
+            "ds4g_quantize_pack": ([i, i, i, vp, sz, vp, sz], i),
+            "ds4g_unpack": ([i, i, i, vp, sz, vp, sz], i),
+            "ds4g_quantize_pack_device": ([i, i, i, vp, vp, vp], i),
+            "ds4g_dequantize": ([i, vp, i, i, vp, vp, vp, vp], i),
+            "ds4g_route_workspace": ([i], sz),
+            "ds4g_moe_route": ([vp, i, vp, vp, vp, vp, vp, sz, vp], i),
+            "ds4g_bucket_workspace": ([i], sz),
+            "ds4g_moe_bucket": ([vp, i, vp, vp, vp, vp, vp, sz, vp], i),
+            "ds4g_forward_workspace": ([i], sz),
+            "ds4g_moe_forward": (fwd, i),
+            "ds4g_moe_gate_up": (fwd, i),
+            "ds4g_moe_down": (fwd, i),
+            "ds4g_rmsnorm": ([vp, i, vp, vp], i),
+            "ds4g_last_error": ([vp, vp], i),
+        }
+        for name, (args, res) in sig.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = L
+    return _lib
+
+
+def header_functions() -> list[str]:
+    """Names of the functions declared in include/ds4g.h."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"\b(ds4g_[a-z_0-9]+)\s*\(", text)))
+
+
+def _check(fn: str, rc: int):
+    if rc != 0:
+        raise DS4GError(fn, rc)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def ds4g_status_str(code: int) -> str:
+    return lib().ds4g_status_str(code).decode()
+
+
+def ds4g_block_bytes(qtype: int) -> int:
+    return lib().ds4g_block_bytes(qtype)
+
+
+def ds4g_packed_size(qtype: int, rows: int, cols: int) -> int:
+    return lib().ds4g_packed_size(qtype, rows, cols)
+
+
+def ds4g_quantize_pack(qtype: int, rows: int, cols: int, gguf: np.ndarray) -> np.ndarray:
+    """Host: GGUF-format bytes -> packed device-layout bytes (numpy uint8)."""
+    gguf = np.ascontiguousarray(gguf, np.uint8)
+    n = ds4g_packed_size(qtype, rows, cols)
+    out = np.empty(max(n, 1), np.uint8)
+    _check("ds4g_quantize_pack", lib().ds4g_quantize_pack(qtype, rows, cols, _ptr(gguf), gguf.nbytes,
+                                                          _ptr(out), out.nbytes))
+    return out[:n]
+
+
+def ds4g_unpack(qtype: int, rows: int, cols: int, packed: np.ndarray) -> np.ndarray:
+    packed = np.ascontiguousarray(packed, np.uint8)
+    n = ds4g_packed_size(qtype, rows, cols)
+    out = np.empty(max(n, 1), np.uint8)
+    _check("ds4g_unpack", lib().ds4g_unpack(qtype, rows, cols, _ptr(packed), packed.nbytes, _ptr(out),
+                                            out.nbytes))
+    return out[:n]
+
+
+def ds4g_quantize_pack_device(qtype, rows, cols, gguf_dev, packed_dev, stream=None):
+    _check("ds4g_quantize_pack_device",
+           lib().ds4g_quantize_pack_device(qtype, rows, cols, _ptr(gguf_dev), _ptr(packed_dev),
+                                           _stream(stream)))
+
+
+def ds4g_dequantize(qtype, packed_dev, rows, cols, grid_dev=None, out_f32=None, out_bf16=None, stream=None):
+    _check("ds4g_dequantize", lib().ds4g_dequantize(qtype, _ptr(packed_dev), rows, cols, _ptr(grid_dev),
+                                                    _ptr(out_f32), _ptr(out_bf16), _stream(stream)))
+
+
+def ds4g_route_workspace(T: int) -> int:
+    return lib().ds4g_route_workspace(T)
+
+
+def ds4g_moe_route(hidden, router, bias, ids, w, workspace, stream=None):
+    T = hidden.shape[0]
+    _check("ds4g_moe_route", lib().ds4g_moe_route(_ptr(hidden), T, _ptr(router), _ptr(bias), _ptr(ids),
+                                                  _ptr(w), _ptr(workspace), workspace.numel(),
+                                                  _stream(stream)))
+
+
+def ds4g_bucket_workspace(T: int) -> int:
+    return lib().ds4g_bucket_workspace(T)
+
+
+def ds4g_moe_bucket(ids, counts, offsets, perm, inv, workspace, stream=None):
+    T = ids.shape[0]
+    _check("ds4g_moe_bucket", lib().ds4g_moe_bucket(_ptr(ids), T, _ptr(counts), _ptr(offsets), _ptr(perm),
+                                                    _ptr(inv), _ptr(workspace), workspace.numel(),
+                                                    _stream(stream)))
+
+
+def ds4g_forward_workspace(T: int) -> int:
+    return lib().ds4g_forward_workspace(T)
+
+
+def _fwd(name, hidden, layer, ids, w, out, workspace, stream):
+    T = hidden.shape[0]
+    _check(name, getattr(lib(), name)(_ptr(hidden), T, C.byref(layer), _ptr(ids), _ptr(w), _ptr(out),
+                                      _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def ds4g_moe_forward(hidden, layer: ds4g_layer, ids, w, out, workspace, stream=None):
+    _fwd("ds4g_moe_forward", hidden, layer, ids, w, out, workspace, stream)
+
+
+def ds4g_moe_gate_up(hidden, layer: ds4g_layer, ids, w, out, workspace, stream=None):
+    _fwd("ds4g_moe_gate_up", hidden, layer, ids, w, out, workspace, stream)
+
+
+def ds4g_moe_down(hidden, layer: ds4g_layer, ids, w, out, workspace, stream=None):
+    _fwd("ds4g_moe_down", hidden, layer, ids, w, out, workspace, stream)
+
+
+def ds4g_rmsnorm(x, y, stream=None):
+    _check("ds4g_rmsnorm", lib().ds4g_rmsnorm(_ptr(x), x.shape[0], _ptr(y), _stream(stream)))
+
+
+def ds4g_last_error(workspace, stream=None) -> int:
+    return lib().ds4g_last_error(_ptr(workspace), _stream(stream))
+
+
+# --------------------------------------------------------------- conveniences
+def workspace(nbytes: int, device="cuda"):
+    """Zero-filled device workspace (the kernels keep their counters at zero
+    between calls, so a workspace needs zeroing only once)."""
+    import torch
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+class MoELayer:
+    """Device-resident weights of one MoE layer and its ds4g_layer struct.
+
+    gate/up/down: one uint8 tensor each of shape [n_experts, packed_bytes]
+    (packed layout); ``expert_ids`` maps row i of those tensors to an expert
+    id (experts absent from the list get NULL pointers, which the kernels
+    reject if selected).  sh_*: bf16-bits 16-bit tensors.  grid: 64-bit [256].
+    """
+
+    def __init__(self, gate, up, down, sh_gate, sh_up, sh_down, grid=None,
+                 gate_up_type=DS4G_IQ2_XXS, down_type=DS4G_Q2_K, expert_ids=None):
+        import torch
+        dev = gate.device
+        n = gate.shape[0]
+        ids = list(range(n)) if expert_ids is None else list(expert_ids)
+        self.tensors = (gate, up, down, sh_gate, sh_up, sh_down, grid)
+        ptrs = np.zeros((3, N_EXPERT), np.int64)
+        for row, e in enumerate(ids):
+            ptrs[0, e] = gate[row].data_ptr()
+            ptrs[1, e] = up[row].data_ptr()
+            ptrs[2, e] = down[row].data_ptr()
+        self.ptrs = torch.from_numpy(ptrs).to(dev)
+        self.struct = ds4g_layer(gate_up_type, down_type, self.ptrs[0].data_ptr(), self.ptrs[1].data_ptr(),
+                                 self.ptrs[2].data_ptr(), sh_gate.data_ptr(), sh_up.data_ptr(),
+                                 sh_down.data_ptr(), 0 if grid is None else grid.data_ptr())

@@ -1,0 +1,241 @@
+// route.cu — router scores and top-6 selection (chenxutan ds4 article §3.2
+// "Router 计算专家选择"; juejin ds4 article §2.1: 256 routed experts, 6 used).
+// Readings where the pages are silent: sigmoid score, bias only for
+// selection, ties to the lower expert id, weights = selected unbiased scores
+// renormalised to sum 1.
+//
+// One launch for any T:
+//   small T (<= 8): CTA (expert group of 8, k-quarter); each warp streams one
+//     router row quarter once and dots it with all T tokens;
+//   large T: 32-token x 64-expert fp32 SIMT tiles over the full K.
+// Partial logits go to the workspace; the last CTA to finish a token range
+// (atomic ticket, no waiting) sums them in a fixed order and runs the top-k,
+// one warp per token.
+#include <float.h>
+
+#include "ds4g_internal.cuh"
+
+namespace ds4g {
+
+constexpr int kRouteSmallT = 8;
+constexpr int kRouteKS = 4;   // k-splits on the small-T path
+constexpr int kTileT = 32, kTileE = 64, kTileK = 32;
+
+struct RouteArgs {
+    const float *x;
+    int T;
+    const float *R;
+    const float *bias;
+    int32_t *ids;
+    float *w;
+    float *part;      // small: [KS][T][256]; large: [T][256]
+    uint32_t *cnt;    // small: [1]; large: [ceil(T/32)]
+    uint32_t *status;
+};
+
+// Warp: top-6 for one token given its 256 logits (in shared memory).
+__device__ void topk_warp(const RouteArgs &a, int t, const float *logit) {
+    const int lane = threadIdx.x & 31;
+    float key[8], s[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int e = lane + 32 * i;
+        s[i] = 1.0f / (1.0f + expf(-logit[e]));
+        key[i] = s[i] + a.bias[e];
+    }
+    int sel_e[kK];
+    float sel_s[kK];
+#pragma unroll
+    for (int k = 0; k < kK; ++k) {
+        float bk = -FLT_MAX;
+        int be = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = lane + 32 * i;
+            if (key[i] > bk || (key[i] == bk && e < be)) {
+                bk = key[i];
+                be = e;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ok = __shfl_xor_sync(0xffffffffu, bk, off);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+            if (ok > bk || (ok == bk && oe < be)) {
+                bk = ok;
+                be = oe;
+            }
+        }
+        const int owner = be & 31, slot = be >> 5;
+        float sv = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (i == slot) sv = s[i];
+        sv = __shfl_sync(0xffffffffu, sv, owner);
+        if (lane == owner) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (i == slot) key[i] = -FLT_MAX;
+        }
+        sel_e[k] = be;
+        sel_s[k] = sv;
+    }
+    if (lane == 0) {
+        float sum = 0.f;
+#pragma unroll
+        for (int k = 0; k < kK; ++k) sum += sel_s[k];
+#pragma unroll
+        for (int k = 0; k < kK; ++k) {
+            a.ids[t * kK + k] = sel_e[k];
+            a.w[t * kK + k] = sel_s[k] / sum;
+        }
+    }
+}
+
+// grid (32, KS), block 256.
+__global__ void __launch_bounds__(256) route_small_kernel(RouteArgs a) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.x * 8 + warp, ks = blockIdx.y;
+    const int k0 = ks * (kH / kRouteKS);
+    float4 r[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        r[i] = __ldcs(reinterpret_cast<const float4 *>(a.R + (size_t)e * kH + k0 + 4 * lane + 128 * i));
+    for (int t = 0; t < a.T; ++t) {
+        const float *xr = a.x + (size_t)t * kH + k0;
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 xv = *reinterpret_cast<const float4 *>(xr + 4 * lane + 128 * i);
+            acc = fmaf(r[i].x, xv.x, acc);
+            acc = fmaf(r[i].y, xv.y, acc);
+            acc = fmaf(r[i].z, xv.z, acc);
+            acc = fmaf(r[i].w, xv.w, acc);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) a.part[((size_t)ks * a.T + t) * kE + e] = acc;
+    }
+    __threadfence();  // every writer publishes its partials before the ticket
+    __shared__ uint32_t last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const uint32_t ticket = atomicAdd(a.cnt, 1u);
+        last = (ticket == gridDim.x * gridDim.y - 1) ? 1u : 0u;
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    __shared__ float lg[kRouteSmallT][kE];
+    for (int i = threadIdx.x; i < a.T * kE; i += blockDim.x) {
+        const int t = i / kE, ee = i % kE;
+        float v = 0.f;
+        for (int s = 0; s < kRouteKS; ++s) v += __ldcg(a.part + ((size_t)s * a.T + t) * kE + ee);
+        lg[t][ee] = v;
+    }
+    __syncthreads();
+    if (warp < a.T) topk_warp(a, warp, lg[warp]);
+    if (threadIdx.x == 0) *a.cnt = 0u;
+}
+
+// grid (ceil(T/32), 4), block 256: fp32 tile 32 tokens x 64 experts.
+__global__ void __launch_bounds__(256) route_tiled_kernel(RouteArgs a) {
+    __shared__ float xs[kTileT][kTileK + 1];
+    __shared__ float rs[kTileE][kTileK + 1];
+    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+    const int t0 = blockIdx.x * kTileT, e0 = blockIdx.y * kTileE;
+    float acc[2][4] = {};
+    for (int k0 = 0; k0 < kH; k0 += kTileK) {
+        for (int i = tid; i < kTileT * kTileK; i += 256) {
+            const int tt = i / kTileK, kk = i % kTileK;
+            xs[tt][kk] = (t0 + tt < a.T) ? a.x[(size_t)(t0 + tt) * kH + k0 + kk] : 0.f;
+        }
+        for (int i = tid; i < kTileE * kTileK; i += 256) {
+            const int ee = i / kTileK, kk = i % kTileK;
+            rs[ee][kk] = a.R[(size_t)(e0 + ee) * kH + k0 + kk];
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int kk = 0; kk < kTileK; ++kk) {
+            const float x0 = xs[ty][kk], x1 = xs[ty + 16][kk];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float rv = rs[tx + 16 * j][kk];
+                acc[0][j] = fmaf(x0, rv, acc[0][j]);
+                acc[1][j] = fmaf(x1, rv, acc[1][j]);
+            }
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int t = t0 + ty + 16 * i;
+        if (t < a.T)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) a.part[(size_t)t * kE + e0 + tx + 16 * j] = acc[i][j];
+    }
+    __threadfence();
+    __shared__ uint32_t last;
+    __syncthreads();
+    if (tid == 0) {
+        const uint32_t ticket = atomicAdd(a.cnt + blockIdx.x, 1u);
+        last = (ticket == gridDim.y - 1) ? 1u : 0u;
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    __shared__ float lg[8][kE];
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int tt = warp; tt < kTileT; tt += 8) {
+        const int t = t0 + tt;
+        if (t >= a.T) break;
+        for (int i = lane; i < kE; i += 32) lg[warp][i] = __ldcg(a.part + (size_t)t * kE + i);
+        __syncwarp();
+        topk_warp(a, t, lg[warp]);
+        __syncwarp();
+    }
+    if (tid == 0) a.cnt[blockIdx.x] = 0u;
+}
+
+}  // namespace ds4g
+
+using namespace ds4g;
+
+static size_t route_part_bytes(int T) {
+    return T <= kRouteSmallT ? (size_t)kRouteKS * T * kE * 4 : (size_t)T * kE * 4;
+}
+
+extern "C" size_t ds4g_route_workspace(int T) {
+    if (T < 1) return 0;
+    const size_t ntile = (size_t)(T + kTileT - 1) / kTileT;
+    return kWsHeader + align_up(ntile * 4 + 4, 256) + align_up(route_part_bytes(T), 256);
+}
+
+extern "C" ds4g_status ds4g_moe_route(const float *hidden, int T, const float *router,
+                                      const float *bias, int32_t *ids, float *w, void *workspace,
+                                      size_t ws_bytes, ds4g_stream_t s) {
+    if (!hidden || !router || !bias || !ids || !w || !workspace || T < 1) return DS4G_EINVAL;
+    if (((uintptr_t)hidden | (uintptr_t)router | (uintptr_t)bias | (uintptr_t)ids | (uintptr_t)w |
+         (uintptr_t)workspace) & 15)
+        return DS4G_EALIGN;
+    if (ws_bytes < ds4g_route_workspace(T)) return DS4G_ENOSPACE;
+    RouteArgs a;
+    a.x = hidden;
+    a.T = T;
+    a.R = router;
+    a.bias = bias;
+    a.ids = ids;
+    a.w = w;
+    uint8_t *ws = (uint8_t *)workspace;
+    a.status = (uint32_t *)ws;
+    const size_t ntile = (size_t)(T + kTileT - 1) / kTileT;
+    a.cnt = (uint32_t *)(ws + kWsHeader);
+    a.part = (float *)(ws + kWsHeader + align_up(ntile * 4 + 4, 256));
+    cudaStream_t st = (cudaStream_t)s;
+    if (T <= kRouteSmallT) {
+        route_small_kernel<<<dim3(kE / 8, kRouteKS), 256, 0, st>>>(a);
+    } else {
+        route_tiled_kernel<<<dim3((unsigned)ntile, kE / kTileE), 256, 0, st>>>(a);
+    }
+    return cudaGetLastError() == cudaSuccess ? DS4G_OK : DS4G_ECUDA;
+}

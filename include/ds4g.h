@@ -204,6 +204,21 @@ ds4g_status ds4g_moe_forward(const float *hidden, int T, const ds4g_layer *L,
                              const int32_t *ids, const float *w, float *out,
                              void *workspace, size_t ws_bytes, ds4g_stream_t s);
 
+/* The two phases of ds4g_moe_forward, for callers that schedule them
+ * separately (e.g. to overlap other work between them, or to time them):
+ * ds4g_moe_gate_up computes h_k = silu(G_e x) * (U_e x) for every slot and
+ * the shared expert into the workspace; ds4g_moe_down reads them from the
+ * same workspace and writes out.  Same arguments and checks as
+ * ds4g_moe_forward; calling gate_up then down on the same workspace and
+ * stream equals one ds4g_moe_forward.  Only for T <= 3 (the per-slot decode
+ * path), else DS4G_EUNSUPPORTED. */
+ds4g_status ds4g_moe_gate_up(const float *hidden, int T, const ds4g_layer *L,
+                             const int32_t *ids, const float *w, float *out,
+                             void *workspace, size_t ws_bytes, ds4g_stream_t s);
+ds4g_status ds4g_moe_down(const float *hidden, int T, const ds4g_layer *L,
+                          const int32_t *ids, const float *w, float *out,
+                          void *workspace, size_t ws_bytes, ds4g_stream_t s);
+
 /* RMS norm between chained layers (pages silent; reading: eps = 1e-6, no
  * learned gain): y[t] = x[t] / sqrt(mean_j x[t][j]^2 + 1e-6).  In place
  * (x == y) is allowed.  x, y [T][4096] f32 dev. */

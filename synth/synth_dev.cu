@@ -13,34 +13,40 @@ static __host__ __device__ inline uint64_t splitmix64(uint64_t x) {
     return z ^ (z >> 31);
 }
 
-// One thread per 8-byte word of the raw stream.
-__global__ void fill_raw(uint8_t *out, uint64_t nbytes, uint64_t base) {
-    const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const uint64_t off = i * 8;
-    if (off >= nbytes) return;
-    const uint64_t v = splitmix64(base + i);
-    if (off + 8 <= nbytes && (((uintptr_t)(out + off)) & 7) == 0) {
-        *(uint64_t *)(out + off) = v;
-    } else {
-        for (int b = 0; b < 8 && off + b < nbytes; ++b) out[off + b] = (uint8_t)(v >> (8 * b));
-    }
-}
-
-// One thread per fp16 scale field: fp16(1e-3 + 3e-3 * (h >> 40) * 2^-24).
-__global__ void fill_fp16(uint8_t *out, uint64_t nblk, int bb, int nf, int off0, int off1,
-                          uint64_t base_d) {
-    const uint64_t n = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (n >= nblk * (uint64_t)nf) return;
-    const uint64_t blk = n / nf;
-    const int fi = (int)(n % nf);
-    const uint64_t u = splitmix64(base_d + n) >> 40;
-    float t = __fmul_rn((float)u, 5.9604644775390625e-08f);  // * 2^-24, exact
+// fp16 bits of 1e-3 + 3e-3 * u * 2^-24 for field number n (separate fp32
+// roundings, then fp16 round-to-nearest-even).
+static __device__ inline uint32_t scale_bits(uint64_t base_d, uint64_t n) {
+    const uint32_t u = (uint32_t)(splitmix64(base_d + n) >> 40);
+    float t = __fmul_rn(__uint2float_rn(u), 5.9604644775390625e-08f);
     t = __fmul_rn(3e-3f, t);
     const float d = __fadd_rn(1e-3f, t);
-    const uint16_t bits = __half_as_ushort(__float2half_rn(d));
-    uint8_t *p = out + blk * bb + (fi == 0 ? off0 : off1);
-    p[0] = (uint8_t)(bits & 0xff);
-    p[1] = (uint8_t)(bits >> 8);
+    return (uint32_t)__half_as_ushort(__float2half_rn(d));
+}
+
+// One thread per 8-byte word: the raw hash word, with every byte that belongs
+// to an fp16 scale field replaced by that field's byte.
+__global__ void fill_gguf(uint8_t *out, uint64_t nbytes, uint64_t base, uint64_t base_d, int bb,
+                          int nf, int off0, int off1) {
+    const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const uint64_t pos0 = i * 8;
+    if (pos0 >= nbytes) return;
+    const uint64_t v = splitmix64(base + i);
+    uint8_t bytes[8];
+    for (int b = 0; b < 8; ++b) {
+        const uint64_t pos = pos0 + b;
+        uint8_t val = (uint8_t)(v >> (8 * b));
+        const uint64_t blk = pos / (uint64_t)bb;
+        const int off = (int)(pos % (uint64_t)bb);
+        for (int f = 0; f < nf; ++f) {
+            const int fo = f == 0 ? off0 : off1;
+            if (off == fo || off == fo + 1) {
+                const uint32_t bits = scale_bits(base_d, blk * nf + f);
+                val = (uint8_t)(off == fo ? (bits & 0xffu) : (bits >> 8));
+            }
+        }
+        bytes[b] = val;
+    }
+    for (int b = 0; b < 8 && pos0 + b < nbytes; ++b) out[pos0 + b] = bytes[b];
 }
 
 extern "C" int synth_fill_gguf(int qtype, int rows, int cols, uint64_t seed, uint64_t stream,
@@ -53,15 +59,12 @@ extern "C" int synth_fill_gguf(int qtype, int rows, int cols, uint64_t seed, uin
     default: return -1;
     }
     if (!dev || rows <= 0 || cols <= 0 || cols % 256) return -1;
-    cudaStream_t s = (cudaStream_t)cuda_stream;
     const uint64_t nblk = (uint64_t)rows * (cols / 256);
     const uint64_t nbytes = nblk * bb;
     const uint64_t base = seed ^ splitmix64(stream);
     const uint64_t base_d = seed ^ splitmix64(stream | (1ull << 63));
     const uint64_t nw = (nbytes + 7) / 8;
-    fill_raw<<<(unsigned)((nw + 255) / 256), 256, 0, s>>>((uint8_t *)dev, nbytes, base);
-    const uint64_t nfld = nblk * nf;
-    fill_fp16<<<(unsigned)((nfld + 255) / 256), 256, 0, s>>>((uint8_t *)dev, nblk, bb, nf, off0,
-                                                             off1, base_d);
+    fill_gguf<<<(unsigned)((nw + 255) / 256), 256, 0, (cudaStream_t)cuda_stream>>>(
+        (uint8_t *)dev, nbytes, base, base_d, bb, nf, off0, off1);
     return cudaGetLastError() == cudaSuccess ? 0 : -2;
 }

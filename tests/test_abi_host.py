@@ -1,0 +1,149 @@
+"""CPU-side checks of the C-ABI library: it loads, exports every function the
+header declares, packs/unpacks losslessly into the documented layout, and
+rejects bad arguments before touching the GPU."""
+import ctypes as C
+
+import numpy as np
+import pytest
+
+import bit_quantized_moe_bias_b300 as B
+import synth
+
+
+def test_library_exports_every_header_function():
+    L = B.lib()
+    names = B.header_functions()
+    assert len(names) >= 17
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+
+
+@pytest.mark.parametrize("qt,bb", [(0, 66), (1, 84), (2, 144), (3, 512)])
+def test_block_bytes(qt, bb):
+    assert B.ds4g_block_bytes(qt) == bb
+
+
+def test_packed_size_rules():
+    assert B.ds4g_packed_size(0, 2048, 4096) == 2048 * 16 * 66
+    assert B.ds4g_packed_size(1, 4096, 2048) == 4096 * 8 * 84
+    assert B.ds4g_packed_size(2, 16, 256) == 144 * 16
+    assert B.ds4g_packed_size(0, 15, 256) == 0       # rows not a multiple of 16
+    assert B.ds4g_packed_size(0, 16, 300) == 0       # cols not a multiple of 256
+    assert B.ds4g_packed_size(3, 16, 256) == 0       # bf16 is not packed
+
+
+@pytest.mark.parametrize("qt", [0, 1, 2])
+@pytest.mark.parametrize("rows,cols", [(16, 256), (48, 768), (64, 4096)])
+def test_pack_unpack_round_trip(qt, rows, cols):
+    g = synth.gguf_matrix(qt, rows, cols, 11, 1000 + rows + qt)
+    p = B.ds4g_quantize_pack(qt, rows, cols, g)
+    assert p.nbytes == g.nbytes and not np.array_equal(p, g)
+    assert np.array_equal(B.ds4g_unpack(qt, rows, cols, p), g)
+
+
+def test_iq2_layout_matches_documentation():
+    """Packed IQ2_XXS: record of GGUF sub-block j of tile row rr sits at
+    512*hrow + 16*(4g + t) + 8*jj (g = rr&7, hrow = rr>>3, t = j&3, jj = j>>2);
+    d at 1024 + 4g + 2*hrow."""
+    g = synth.gguf_matrix(0, 16, 256, 3, 9).reshape(16, 66)
+    p = B.ds4g_quantize_pack(0, 16, 256, g.reshape(-1))
+    for rr in range(16):
+        gg, hrow = rr & 7, rr >> 3
+        for j in range(8):
+            off = 512 * hrow + 16 * (4 * gg + (j & 3)) + 8 * (j >> 2)
+            assert np.array_equal(p[off:off + 8], g[rr, 2 + 8 * j: 10 + 8 * j])
+        assert np.array_equal(p[1024 + 4 * gg + 2 * hrow: 1026 + 4 * gg + 2 * hrow], g[rr, 0:2])
+
+
+def test_q2k_layout_matches_documentation():
+    """Packed Q2_K: quant of weight n (sub-block sb = n//16, i = n%16 = 4c+p)
+    at bit 16*(p&1) + 2*(2c + (p>>1)) of the word at 512*hrow + 16*(4g+t) + 4G
+    (t = sb&3, G = sb>>2); GGUF field of n = 128h + 32jq + l is bits 2jq of
+    qs[32h + l]."""
+    g = synth.gguf_matrix(1, 16, 256, 4, 10).reshape(16, 84)
+    p = B.ds4g_quantize_pack(1, 16, 256, g.reshape(-1))
+    words = p.view("<u4")
+    for rr in (0, 5, 8, 15):
+        gg, hrow = rr & 7, rr >> 3
+        for n in range(256):
+            h, jq, l = n // 128, (n % 128) // 32, n % 32
+            q_ref = (int(g[rr, 16 + 32 * h + l]) >> (2 * jq)) & 3
+            sb, i = n // 16, n % 16
+            c, pp = i // 4, i % 4
+            wi = (512 * hrow + 16 * (4 * gg + (sb & 3)) + 4 * (sb >> 2)) // 4
+            q = (int(words[wi]) >> (16 * (pp & 1) + 2 * (2 * c + (pp >> 1)))) & 3
+            assert q == q_ref
+        for sb in range(16):
+            assert p[1024 + 128 * hrow + 4 * (4 * gg + (sb & 3)) + (sb >> 2)] == g[rr, sb]
+
+
+def test_q4k_layout_matches_documentation():
+    """Packed Q4_K: weight n (sub-block j = n//32, i = n%32 = 4c+p) at bit
+    16*(p&1) + 4*(2*(c&1) + (p>>1)) of the word at
+    1024*hrow + 32*(4g+t) + 4*(4jj + (c>>1)) (t = j&3, jj = j>>2); GGUF: weight
+    64c4 + l is the low nibble of qs[32c4 + l], 64c4 + 32 + l the high one."""
+    g = synth.gguf_matrix(2, 16, 256, 4, 12).reshape(16, 144)
+    p = B.ds4g_quantize_pack(2, 16, 256, g.reshape(-1))
+    words = p.view("<u4")
+    for rr in (1, 7, 9, 14):
+        gg, hrow = rr & 7, rr >> 3
+        for n in range(256):
+            c4, r = n // 64, n % 64
+            q_ref = (int(g[rr, 16 + 32 * c4 + (r % 32)]) >> (0 if r < 32 else 4)) & 15
+            j, i = n // 32, n % 32
+            c, pp = i // 4, i % 4
+            wi = (1024 * hrow + 32 * (4 * gg + (j & 3)) + 4 * (4 * (j >> 2) + (c >> 1))) // 4
+            q = (int(words[wi]) >> (16 * (pp & 1) + 4 * (2 * (c & 1) + (pp >> 1)))) & 15
+            assert q == q_ref
+        assert np.array_equal(p[2048 + 12 * rr: 2060 + 12 * rr], g[rr, 4:16])
+
+
+def test_pack_rejects_bad_arguments():
+    L = B.lib()
+    buf = np.zeros(1 << 16, np.uint8)
+    ptr = buf.ctypes.data
+    assert L.ds4g_quantize_pack(0, 16, 256, None, 0, ptr, buf.nbytes) == 1            # EINVAL
+    assert L.ds4g_quantize_pack(7, 16, 256, ptr, buf.nbytes, ptr, buf.nbytes) == 1    # bad type
+    assert L.ds4g_quantize_pack(0, 17, 256, ptr, buf.nbytes, ptr, buf.nbytes) == 5    # EUNSUPPORTED
+    assert L.ds4g_quantize_pack(0, 16, 256, ptr, 100, ptr, buf.nbytes) == 3           # ENOSPACE
+    assert L.ds4g_quantize_pack(0, 16, 256, ptr, buf.nbytes, ptr, 100) == 3
+
+
+def test_gpu_entry_points_validate_before_launch():
+    """Bad arguments come back as status codes without any CUDA call."""
+    L = B.lib()
+    fake = 0x10000000           # aligned fake device address (never dereferenced)
+    odd = fake + 4
+    big = 1 << 30
+    lay = B.ds4g_layer(0, 1, fake, fake, fake, fake, fake, fake, fake)
+    for f in (L.ds4g_moe_forward, L.ds4g_moe_gate_up, L.ds4g_moe_down):
+        assert f(None, 1, C.byref(lay), fake, fake, fake, fake, big, None) == 1        # NULL hidden
+        assert f(fake, 0, C.byref(lay), fake, fake, fake, fake, big, None) == 1        # T < 1
+        assert f(odd, 1, C.byref(lay), fake, fake, fake, fake, big, None) == 2         # misaligned
+        assert f(fake, 1, C.byref(lay), fake, fake, fake, fake, 16, None) == 3         # workspace
+        bad = B.ds4g_layer(0, 2, fake, fake, fake, fake, fake, fake, fake)             # IQ2 + Q4_K
+        assert f(fake, 1, C.byref(bad), fake, fake, fake, fake, big, None) == 5
+        nogrid = B.ds4g_layer(0, 1, fake, fake, fake, fake, fake, fake, None)
+        assert f(fake, 1, C.byref(nogrid), fake, fake, fake, fake, big, None) == 1
+    assert L.ds4g_moe_gate_up(fake, 4, C.byref(lay), fake, fake, fake, fake, big, None) == 5  # phases: T <= 3
+    r = L.ds4g_moe_route
+    assert r(fake, 1, fake, fake, fake, fake, fake, 8, None) == 3
+    assert r(fake, 1, fake, odd, fake, fake, fake, big, None) == 2
+    assert r(None, 1, fake, fake, fake, fake, fake, big, None) == 1
+    assert L.ds4g_moe_bucket(fake, 0, fake, fake, fake, fake, fake, big, None) == 1
+    assert L.ds4g_dequantize(0, fake, 16, 256, None, fake, None, None) == 1           # IQ2 needs grid
+    assert L.ds4g_dequantize(1, fake, 16, 300, None, fake, None, None) == 5
+    assert L.ds4g_rmsnorm(odd, 1, fake, None) == 2
+    assert L.ds4g_quantize_pack_device(1, 16, 256, odd, fake, None) == 2
+
+
+def test_workspace_sizes_grow_with_T():
+    assert B.ds4g_route_workspace(0) == 0
+    assert B.ds4g_route_workspace(1) < B.ds4g_route_workspace(2048)
+    assert 0 < B.ds4g_forward_workspace(1) <= B.ds4g_forward_workspace(3)
+    assert B.ds4g_bucket_workspace(1) >= 256
+
+
+def test_status_strings():
+    assert B.ds4g_status_str(0) == "ok"
+    assert "bad data" in B.ds4g_status_str(7)
