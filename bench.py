@@ -1,0 +1,366 @@
+#!/usr/bin/env python3
+"""Benchmark of the B300 routed-MoE block (libds4g) — one JSON line.
+
+Default workload (config 1): full-depth decode of DeepSeek-V4-Flash MoE
+layers — 43 stacked layers, each with 256 routed experts (IQ2_XXS gate/up,
+Q2_K down, 78 GB packed in HBM) plus a bf16 shared expert and an fp32 router;
+one step = 64 consecutive tokens, each a fresh N(0,1) hidden vector, passed
+through rmsnorm -> route -> MoE forward for all 43 layers.  The step is
+captured once as a CUDA graph and replayed.  Metric: tokens/s (whole job).
+
+--impl reference times the CPU oracle (plain C, fp64) on a bounded sample of
+the same workload on this host's cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+H, F, E, K = 4096, 2048, 256, 6
+NLAYER = 43
+SEED = 0
+CFG = 1
+# algorithmic bytes of one token through one layer: 6 selected experts'
+# packed gate/up/down + bf16 shared expert + fp32 router (+ activations)
+ROUTED_BYTES = 6 * (2 * 2162688 + 2752512)          # 42,467,328
+SHARED_BYTES = 3 * F * H * 2                        # 50,331,648
+ROUTER_BYTES = E * H * 4                            # 4,194,304
+ACT_BYTES = 2 * H * 4 + E * 4                       # x in, out, bias
+LAYER_BYTES = ROUTED_BYTES + SHARED_BYTES + ROUTER_BYTES + ACT_BYTES
+# gate/up launch (dominant kernel): routed gate+up + shared gate+up + x
+GATEUP_BYTES = 6 * 2 * 2162688 + 2 * F * H * 2 + H * 4
+METRIC = "routed-MoE tokens/s (decode, prefill) and achieved HBM GB/s vs B300 peak"
+WORKLOAD = ("config1 full-depth decode: 43 MoE layers x 256 experts (IQ2_XXS gate/up, Q2_K down, "
+            "bf16 shared, fp32 router), 1 token at a time, 64 tokens per step")
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6400.0, "fallback"
+
+
+def traffic_record(kernel):
+    """Per-launch DRAM traffic of `kernel` from the committed ncu summary, if
+    it was taken on the current source of that kernel (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel)
+    if not d:
+        return None
+    src = os.path.join(ROOT, d["source"])
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] if os.path.exists(src) else None
+    return d["bytes_per_launch"] if h == d["source_sha"] else None
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.samples = []
+        if self.proc is None:
+            return False
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        for line in out.strip().splitlines():
+            parts = [s.strip() for s in line.split(",")]
+            if len(parts) >= 7:
+                self.samples.append(parts)
+        return False
+
+    def summary(self):
+        if not getattr(self, "samples", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
+        mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in self.samples for i in range(4) if s[3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------------ our arm
+def build_model(dev, nlayer):
+    import torch
+    import bit_quantized_moe_bias_b300 as B
+    grid = torch.from_numpy(np.ascontiguousarray(synth.iq2_grid(SEED)).view(np.int64).reshape(256)).to(dev)
+    sizes = {0: B.ds4g_packed_size(0, F, H), 1: B.ds4g_packed_size(1, H, F)}
+    tmp = torch.empty(max(sizes.values()), dtype=torch.uint8, device=dev)
+    layers = []
+    for l in range(nlayer):
+        mats = {}
+        for kind, qt, rows, cols in ((synth.KIND_GATE, 0, F, H), (synth.KIND_UP, 0, F, H), (synth.KIND_DOWN, 1, H, F)):
+            t = torch.empty(E, sizes[qt], dtype=torch.uint8, device=dev)
+            for e in range(E):
+                synth.gguf_matrix_device(qt, rows, cols, SEED, synth.stream_id(CFG, l, kind, e), tmp.data_ptr(),
+                                         torch.cuda.current_stream().cuda_stream)
+                B.ds4g_quantize_pack_device(qt, rows, cols, tmp, t[e])
+            mats[kind] = t
+        shg, shu, shd = synth.shared(SEED, CFG, l)
+        sh = [torch.from_numpy(a.view(np.int16)).to(dev) for a in (shg, shu, shd)]
+        L = B.MoELayer(mats[synth.KIND_GATE], mats[synth.KIND_UP], mats[synth.KIND_DOWN], *sh, grid)
+        R = torch.from_numpy(synth.router(SEED, CFG, l)).to(dev)
+        b = torch.from_numpy(synth.bias_normal(SEED, CFG, l)).to(dev)
+        layers.append((L, R, b))
+    torch.cuda.synchronize()
+    return layers
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import bit_quantized_moe_bias_b300 as B
+    torch.cuda.set_device(local_rank)
+    dev = f"cuda:{local_rank}"
+    ntok = args.tokens
+    t_setup = time.time()
+    layers = build_model(dev, NLAYER)
+    setup_s = time.time() - t_setup
+    # per-step inputs: fresh N(0,1) hidden vectors, one per token
+    x_host = torch.from_numpy(synth.hidden(SEED + rank, CFG, ntok, layer=999, normalise=False)).pin_memory()
+    y_host = torch.empty(ntok, H, dtype=torch.float32).pin_memory()
+    x_dev = x_host.to(dev)
+    xn = torch.empty(1, H, device=dev)
+    act = [torch.empty(1, H, device=dev) for _ in range(2)]
+    out_all = torch.empty(ntok, H, device=dev)
+    ids = torch.empty(1, K, dtype=torch.int32, device=dev)
+    w = torch.empty(1, K, dtype=torch.float32, device=dev)
+    rws = B.workspace(B.ds4g_route_workspace(1), dev)
+    fws = B.workspace(B.ds4g_forward_workspace(1), dev)
+    launches_per_step = ntok * NLAYER * 4
+
+    def step(timing=None):
+        for i in range(ntok):
+            cur = x_dev[i:i + 1]
+            for l, (L, R, b) in enumerate(layers):
+                B.ds4g_rmsnorm(cur, xn)
+                B.ds4g_moe_route(xn, R, b, ids, w, rws)
+                dst = out_all[i:i + 1] if l == NLAYER - 1 else act[l & 1]
+                if timing is not None and i < timing[2]:
+                    timing[0][l + NLAYER * i].record()
+                    B.ds4g_moe_gate_up(xn, L.struct, ids, w, dst, fws)
+                    timing[1][l + NLAYER * i].record()
+                    B.ds4g_moe_down(xn, L.struct, ids, w, dst, fws)
+                else:
+                    B.ds4g_moe_forward(xn, L.struct, ids, w, dst, fws)
+                cur = dst
+
+    # eager warm-up (sets kernel attributes, checks status), then capture
+    step()
+    torch.cuda.synchronize()
+    st = B.ds4g_last_error(rws) or B.ds4g_last_error(fws)
+    if st:
+        raise RuntimeError(f"device status {st} during warm-up")
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---- timed region (device value): K graph replays, inputs resident
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    with ClockSampler(local_rank) as clk:
+        ev0.record()
+        for _ in range(args.steps):
+            graph.replay()
+        ev1.record()
+        torch.cuda.synchronize()
+    barrier()
+    dev_s = ev0.elapsed_time(ev1) / 1e3
+    # ---- end to end: host inputs copied in, result read back, every step
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        graph.replay()
+        y_host.copy_(out_all, non_blocking=True)
+        torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    barrier()
+    # ---- roofline of the dominant kernel (gate/up), CUDA events on its stream
+    ntime = min(ntok, 8)
+    evs = ([torch.cuda.Event(enable_timing=True) for _ in range(NLAYER * ntime)],
+           [torch.cuda.Event(enable_timing=True) for _ in range(NLAYER * ntime)], ntime)
+    step(timing=evs)
+    torch.cuda.synchronize()
+    gu_us = statistics.mean(a.elapsed_time(b) * 1e3 for a, b in zip(evs[0], evs[1]))
+    st = B.ds4g_last_error(rws) or B.ds4g_last_error(fws)
+    if st:
+        raise RuntimeError(f"device status {st} after the timed region")
+
+    times = [dev_s, e2e_s]
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor(times, device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        times = t.tolist()
+    dev_s, e2e_s = times
+    if rank != 0:
+        return None
+    tokens = ntok * args.steps * world
+    value = tokens / dev_s
+    hbm, kind = peaks()
+    achieved = GATEUP_BYTES / (gu_us * 1e-6) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dev_s / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "layers": NLAYER, "tokens_per_step": ntok, "global_batch": 1,
+                   "seq_len": 1, "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "no flush: 80 GB of weights streamed per step >> 126 MB L2",
+                   "weight_gb_per_token": round(NLAYER * LAYER_BYTES / 1e9, 4),
+                   "achieved_hbm_gbs_block": round(value / world * NLAYER * LAYER_BYTES / 1e9, 1),
+                   "setup_s": round(setup_s, 1)},
+        "e2e": {"value": round(tokens / e2e_s, 3), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(x_host.numel() * 4), "d2h_bytes_per_step": int(y_host.numel() * 4)},
+        "roofline": {"bound": "hbm", "kernel": "gateup_decode_kernel", "achieved": round(achieved, 1),
+                     "peak": hbm, "peak_kind": kind, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                     "bytes_per_launch": GATEUP_BYTES, "launch_us": round(gu_us, 3),
+                     "traffic": traffic_record("gateup_decode_kernel")},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_layers)
+    return line
+
+
+# ------------------------------------------------------------- CPU oracle
+_CACHE = {}
+
+
+def _cached(key, fn):
+    if key not in _CACHE:
+        _CACHE[key] = fn()
+    return _CACHE[key]
+
+
+def oracle_sample(nlayers):
+    """Oracle on 1 token through the first `nlayers` layers of the config-1
+    chain; returns (seconds of oracle compute, threads).  Generating the
+    synthetic weights is not timed (and is cached between samples)."""
+    import oracle
+    x = synth.hidden(SEED, CFG, 1, layer=999, normalise=False)
+    grid = synth.iq2_grid(SEED)
+    t = 0.0
+    for l in range(nlayers):
+        R, b, sh = _cached(("L", l), lambda: (synth.router(SEED, CFG, l), synth.bias_normal(SEED, CFG, l),
+                                              synth.shared(SEED, CFG, l)))
+        t0 = time.perf_counter()
+        xn = oracle.rmsnorm(x)
+        ids, w, _, _ = oracle.route(xn, R, b)
+        t += time.perf_counter() - t0
+        gate, up, down = [None] * E, [None] * E, [None] * E
+        for e in ids[0]:
+            gate[e], up[e], down[e] = _cached(("X", l, int(e)), lambda: synth.expert(SEED, CFG, l, int(e)))
+        t0 = time.perf_counter()
+        x = oracle.moe_forward(xn, ids, w, gate, up, down, *sh, grid)
+        t += time.perf_counter() - t0
+    return t, os.cpu_count()
+
+
+def cpu_baseline(nlayers):
+    t, cores = oracle_sample(nlayers)
+    per_token = t * NLAYER / nlayers
+    return {"value": round(1.0 / per_token, 5), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"1 token through the first {nlayers} of {NLAYER} layers (oracle rmsnorm + route + "
+                      f"forward, fp64, OpenMP over rows), extrapolated linearly to {NLAYER} layers"}
+
+
+def run_reference(args):
+    tokens, secs = 0, 0.0
+    for _ in range(args.warmup):
+        oracle_sample(1)
+    cores = os.cpu_count()
+    for _ in range(args.steps):
+        t, cores = oracle_sample(args.cpu_layers)
+        secs += t * NLAYER / args.cpu_layers
+        tokens += 1
+    value = tokens / secs
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "layers": NLAYER, "tokens_per_step": 1},
+        "cpu_baseline": {"value": round(value, 5), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"per step 1 token through {args.cpu_layers} of {NLAYER} layers, "
+                                   f"extrapolated to {NLAYER}"},
+        "e2e": {"value": round(value, 5), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--tokens", type=int, default=64)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-layers", type=int, default=43)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    line = run_ours(args, rank, world, local_rank)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
