@@ -143,8 +143,9 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = f"cuda:{local_rank}"
     ntok = args.tokens
+    nl = args.layers
     t_setup = time.time()
-    layers = build_model(dev, NLAYER)
+    layers = build_model(dev, nl)
     setup_s = time.time() - t_setup
     # per-step inputs: fresh N(0,1) hidden vectors, one per token
     x_host = torch.from_numpy(synth.hidden(SEED + rank, CFG, ntok, layer=999, normalise=False)).pin_memory()
@@ -157,7 +158,7 @@ def run_ours(args, rank, world, local_rank):
     w = torch.empty(1, K, dtype=torch.float32, device=dev)
     rws = B.workspace(B.ds4g_route_workspace(1), dev)
     fws = B.workspace(B.ds4g_forward_workspace(1), dev)
-    launches_per_step = ntok * NLAYER * 4
+    launches_per_step = ntok * nl * 4
 
     def step(timing=None):
         for i in range(ntok):
@@ -165,11 +166,11 @@ def run_ours(args, rank, world, local_rank):
             for l, (L, R, b) in enumerate(layers):
                 B.ds4g_rmsnorm(cur, xn)
                 B.ds4g_moe_route(xn, R, b, ids, w, rws)
-                dst = out_all[i:i + 1] if l == NLAYER - 1 else act[l & 1]
+                dst = out_all[i:i + 1] if l == nl - 1 else act[l & 1]
                 if timing is not None and i < timing[2]:
-                    timing[0][l + NLAYER * i].record()
+                    timing[0][l + nl * i].record()
                     B.ds4g_moe_gate_up(xn, L.struct, ids, w, dst, fws)
-                    timing[1][l + NLAYER * i].record()
+                    timing[1][l + nl * i].record()
                     B.ds4g_moe_down(xn, L.struct, ids, w, dst, fws)
                 else:
                     B.ds4g_moe_forward(xn, L.struct, ids, w, dst, fws)
@@ -222,8 +223,8 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     # ---- roofline of the dominant kernel (gate/up), CUDA events on its stream
     ntime = min(ntok, 8)
-    evs = ([torch.cuda.Event(enable_timing=True) for _ in range(NLAYER * ntime)],
-           [torch.cuda.Event(enable_timing=True) for _ in range(NLAYER * ntime)], ntime)
+    evs = ([torch.cuda.Event(enable_timing=True) for _ in range(nl * ntime)],
+           [torch.cuda.Event(enable_timing=True) for _ in range(nl * ntime)], ntime)
     step(timing=evs)
     torch.cuda.synchronize()
     gu_us = statistics.mean(a.elapsed_time(b) * 1e3 for a, b in zip(evs[0], evs[1]))
@@ -248,11 +249,11 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dev_s / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "layers": NLAYER, "tokens_per_step": ntok, "global_batch": 1,
+        "config": {"workload": WORKLOAD, "layers": nl, "tokens_per_step": ntok, "global_batch": 1,
                    "seq_len": 1, "parallelism": "replicas" if world > 1 else "single",
                    "l2": "no flush: 80 GB of weights streamed per step >> 126 MB L2",
-                   "weight_gb_per_token": round(NLAYER * LAYER_BYTES / 1e9, 4),
-                   "achieved_hbm_gbs_block": round(value / world * NLAYER * LAYER_BYTES / 1e9, 1),
+                   "weight_gb_per_token": round(nl * LAYER_BYTES / 1e9, 4),
+                   "achieved_hbm_gbs_block": round(value / world * nl * LAYER_BYTES / 1e9, 1),
                    "setup_s": round(setup_s, 1)},
         "e2e": {"value": round(tokens / e2e_s, 3), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(x_host.numel() * 4), "d2h_bytes_per_step": int(y_host.numel() * 4)},
@@ -338,6 +339,8 @@ def main():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--tokens", type=int, default=64)
+    ap.add_argument("--layers", type=int, default=NLAYER,
+                    help="stacked layers (43 = the full-depth workload; fewer only for profiling)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-layers", type=int, default=43)
     ap.add_argument("--no-cpu-baseline", action="store_true")
