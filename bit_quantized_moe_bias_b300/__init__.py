@@ -66,6 +66,7 @@ def lib():
             "ds4g_moe_forward": (fwd, i),
             "ds4g_moe_gate_up": (fwd, i),
             "ds4g_moe_down": (fwd, i),
+            "ds4g_moe_forward_noalloc": ([vp, i, C.POINTER(ds4g_layer), vp, vp, vp, vp], i),
             "ds4g_rmsnorm": ([vp, i, vp, vp], i),
             "ds4g_last_error": ([vp, vp], i),
         }
@@ -189,6 +190,14 @@ def ds4g_moe_gate_up(hidden, layer: ds4g_layer, ids, w, out, workspace, stream=N
 
 def ds4g_moe_down(hidden, layer: ds4g_layer, ids, w, out, workspace, stream=None):
     _fwd("ds4g_moe_down", hidden, layer, ids, w, out, workspace, stream)
+
+
+def ds4g_moe_forward_noalloc(hidden, layer: ds4g_layer, ids, w, out, stream=None):
+    """ds4g_moe_forward with the library's own static scratch (no workspace)."""
+    T = hidden.shape[0]
+    _check("ds4g_moe_forward_noalloc",
+           lib().ds4g_moe_forward_noalloc(_ptr(hidden), T, C.byref(layer), _ptr(ids), _ptr(w), _ptr(out),
+                                          _stream(stream)))
 
 
 def ds4g_rmsnorm(x, y, stream=None):

@@ -219,6 +219,38 @@ ds4g_status ds4g_moe_down(const float *hidden, int T, const ds4g_layer *L,
                           const int32_t *ids, const float *w, float *out,
                           void *workspace, size_t ws_bytes, ds4g_stream_t s);
 
+/* ------------------------------------------------------------------------
+ * ds4g_moe_forward without a workspace, for callers that cannot allocate
+ * device memory: code running inside an allocator or memory-pool callback
+ * (where calling cudaMalloc would re-enter the allocator), a real-time loop
+ * that must never stall on the driver's allocator, or a plugin whose host
+ * engine hands it fixed input/output buffers and owns all other memory.
+ * (The ds4 pages have no counterpart: their engine owns all its memory.)
+ *
+ * Same computation, arguments and checks as ds4g_moe_forward minus the
+ * workspace; the caller still passes hidden, ids, w and out.  Scratch is a
+ * library-owned device array of 5 MB (file scope, one per device that
+ * loads the library, held until the process exits).  Limits and behaviour:
+ *  - 1 <= T <= DS4G_NOALLOC_MAX_T, else DS4G_EINVAL (T < 1) or
+ *    DS4G_ENOSPACE (T too large), returned before any CUDA call.
+ *  - Allocates nothing: no cudaMalloc/cudaFree and no allocating library
+ *    call.  Every call clears the used part of the array with
+ *    cudaMemsetAsync on s, then runs the decode kernels on s.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - All calls share the one array: calls that overlap on the GPU (other
+ *    streams, other host threads) race and give wrong results.  Serialise
+ *    them, e.g. on one stream.
+ *  - Faults the kernels detect (a bad expert id) are recorded in the array's
+ *    status word, which no entry point reads back; callers that need that
+ *    check use ds4g_moe_forward with a workspace and ds4g_last_error.
+ * ------------------------------------------------------------------------ */
+#define DS4G_NOALLOC_MAX_T 64
+ds4g_status ds4g_moe_forward_noalloc(const float *hidden, int T, const ds4g_layer *L,
+                                     const int32_t *ids, const float *w, float *out,
+                                     ds4g_stream_t s);
+
 /* RMS norm between chained layers (pages silent; reading: eps = 1e-6, no
  * learned gain): y[t] = x[t] / sqrt(mean_j x[t][j]^2 + 1e-6).  In place
  * (x == y) is allowed.  x, y [T][4096] f32 dev. */
