@@ -111,7 +111,7 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ our arm
-def build_model(dev, nlayer):
+def build_model(dev, nlayer, cfg=CFG):
     import torch
     import bit_quantized_moe_bias_b300 as B
     grid = torch.from_numpy(np.ascontiguousarray(synth.iq2_grid(SEED)).view(np.int64).reshape(256)).to(dev)
@@ -123,15 +123,15 @@ def build_model(dev, nlayer):
         for kind, qt, rows, cols in ((synth.KIND_GATE, 0, F, H), (synth.KIND_UP, 0, F, H), (synth.KIND_DOWN, 1, H, F)):
             t = torch.empty(E, sizes[qt], dtype=torch.uint8, device=dev)
             for e in range(E):
-                synth.gguf_matrix_device(qt, rows, cols, SEED, synth.stream_id(CFG, l, kind, e), tmp.data_ptr(),
+                synth.gguf_matrix_device(qt, rows, cols, SEED, synth.stream_id(cfg, l, kind, e), tmp.data_ptr(),
                                          torch.cuda.current_stream().cuda_stream)
                 B.ds4g_quantize_pack_device(qt, rows, cols, tmp, t[e])
             mats[kind] = t
-        shg, shu, shd = synth.shared(SEED, CFG, l)
+        shg, shu, shd = synth.shared(SEED, cfg, l)
         sh = [torch.from_numpy(a.view(np.int16)).to(dev) for a in (shg, shu, shd)]
         L = B.MoELayer(mats[synth.KIND_GATE], mats[synth.KIND_UP], mats[synth.KIND_DOWN], *sh, grid)
-        R = torch.from_numpy(synth.router(SEED, CFG, l)).to(dev)
-        b = torch.from_numpy(synth.bias_normal(SEED, CFG, l)).to(dev)
+        R = torch.from_numpy(synth.router(SEED, cfg, l)).to(dev)
+        b = torch.from_numpy(synth.bias_normal(SEED, cfg, l)).to(dev)
         layers.append((L, R, b))
     torch.cuda.synchronize()
     return layers
@@ -269,6 +269,140 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
+# --------------------------------------------------------- prefill workload
+PF_T = 2048
+PF_CFG = 3
+# algorithmic FLOPs of the gate/up phase (routed 6T slots + shared T tokens)
+PF_GATEUP_FLOP = 2 * (6 * PF_T + PF_T) * 2 * F * H
+PF_FLOP = 2 * (6 * PF_T + PF_T) * 3 * F * H + 2 * PF_T * E * H   # + router
+PF_WORKLOAD = ("config3 chunked prefill: 1 MoE layer x 256 experts (IQ2_XXS gate/up, Q2_K down, bf16 shared, "
+               "fp32 router), T=2048 tokens per chunk, route + forward per step")
+
+
+def run_prefill(args, rank, world, local_rank):
+    import torch
+    import bit_quantized_moe_bias_b300 as B
+    torch.cuda.set_device(local_rank)
+    dev = f"cuda:{local_rank}"
+    T = PF_T
+    (L, R, b), = build_model(dev, 1, PF_CFG)
+    x_host = torch.from_numpy(synth.hidden(SEED + rank, PF_CFG, T)).pin_memory()
+    y_host = torch.empty(T, H, dtype=torch.float32).pin_memory()
+    x = x_host.to(dev)
+    ids = torch.empty(T, K, dtype=torch.int32, device=dev)
+    w = torch.empty(T, K, dtype=torch.float32, device=dev)
+    out = torch.empty(T, H, device=dev)
+    rws = B.workspace(B.ds4g_route_workspace(T), dev)
+    fws = B.workspace(B.ds4g_forward_workspace(T), dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)   # > 126 MB L2
+
+    def step(ev=None):
+        B.ds4g_moe_route(x, R, b, ids, w, rws)
+        if ev is not None:
+            ev[0].record()
+        B.ds4g_moe_gate_up(x, L.struct, ids, w, out, fws)
+        if ev is not None:
+            ev[1].record()
+        B.ds4g_moe_down(x, L.struct, ids, w, out, fws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = B.ds4g_last_error(rws) or B.ds4g_last_error(fws)
+    if st:
+        raise RuntimeError(f"device status {st} during warm-up")
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    evs = [(mk(), mk(), mk(), mk()) for _ in range(args.steps)]
+    barrier()
+    with ClockSampler(local_rank) as clk:
+        for e0, g0, g1, e1 in evs:
+            flush.zero_()
+            e0.record()
+            step((g0, g1))
+            e1.record()
+        torch.cuda.synchronize()
+    barrier()
+    dev_s = sum(e0.elapsed_time(e1) for e0, _, _, e1 in evs) / 1e3
+    gu_us = statistics.mean(g0.elapsed_time(g1) for _, g0, g1, _ in evs) * 1e3
+    # end to end through the same calls: host hidden in, host output back
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        x.copy_(x_host, non_blocking=True)
+        step()
+        y_host.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    barrier()
+    st = B.ds4g_last_error(rws) or B.ds4g_last_error(fws)
+    if st:
+        raise RuntimeError(f"device status {st} after the timed region")
+    times = [dev_s, e2e_s]
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor(times, device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        times = t.tolist()
+    dev_s, e2e_s = times
+    if rank != 0:
+        return None
+    tokens = T * args.steps * world
+    meas = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    peak, kind = (float(meas["bf16_tflops"]), "measured burst") if "bf16_tflops" in meas else (1800.0, "fallback")
+    achieved = PF_GATEUP_FLOP / (gu_us * 1e-6) / 1e12
+    line = {
+        "metric": METRIC, "value": round(tokens / dev_s, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dev_s / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16/bf16 x f16/bf16 -> f32",
+        "data": "synthetic",
+        "config": {"workload": PF_WORKLOAD, "tokens_per_step": T, "layers": 1,
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "flushed (512 MB write) before every timed step",
+                   "achieved_tflops_block": round(PF_FLOP / (dev_s / args.steps) / 1e12, 1)},
+        "e2e": {"value": round(tokens / e2e_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(x_host.numel() * 4),
+                "d2h_bytes_per_step": int(y_host.numel() * 4)},
+        "roofline": {"bound": "tensor", "kernel": "prefill_gemm_kernel (gate/up phase, incl. bucket + permute)",
+                     "achieved": round(achieved, 1), "peak": peak, "peak_kind": kind, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "flop_per_launch": PF_GATEUP_FLOP,
+                     "launch_us": round(gu_us, 2), "traffic": None},
+        "gpu_launches": 7 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_prefill(args.cpu_tokens)
+    return line
+
+
+def cpu_baseline_prefill(ntok):
+    """Oracle (route + forward) on the first `ntok` tokens of the prefill
+    chunk; tokens are independent given the routing, so tokens/s scales."""
+    import oracle
+    x = synth.hidden(SEED, PF_CFG, ntok)
+    R, b = synth.router(SEED, PF_CFG, 0), synth.bias_normal(SEED, PF_CFG, 0)
+    sh = synth.shared(SEED, PF_CFG, 0)
+    grid = synth.iq2_grid(SEED)
+    t0 = time.perf_counter()
+    ids, w, _, _ = oracle.route(x, R, b)
+    t_route = time.perf_counter() - t0
+    gate, up, down = [None] * E, [None] * E, [None] * E
+    for e in sorted(set(int(v) for v in ids.reshape(-1))):
+        gate[e], up[e], down[e] = synth.expert(SEED, PF_CFG, 0, e)
+    t0 = time.perf_counter()
+    oracle.moe_forward(x, ids, w, gate, up, down, *sh, grid)
+    t = t_route + time.perf_counter() - t0
+    return {"value": round(ntok / t, 4), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"first {ntok} of the {PF_T} tokens (oracle route + forward, fp64, OpenMP over rows); "
+                      "synthetic weight generation not timed"}
+
+
 # ------------------------------------------------------------- CPU oracle
 _CACHE = {}
 
@@ -344,6 +478,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-layers", type=int, default=43)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["decode", "prefill"], default="decode",
+                    help="decode = 43-layer full-depth decode (headline); prefill = T=2048 chunk, one layer")
+    ap.add_argument("--cpu-tokens", type=int, default=8, help="prefill CPU-baseline sample size")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -357,7 +494,8 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
-    line = run_ours(args, rank, world, local_rank)
+    run = run_prefill if args.workload == "prefill" else run_ours
+    line = run(args, rank, world, local_rank)
     if line is not None:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -7,6 +7,9 @@ namespace ds4g {
 size_t decode_workspace(int T);
 ds4g_status decode_forward(const float *hidden, int T, const ds4g_layer *L, const int32_t *ids,
                            const float *w, float *out, void *workspace, cudaStream_t st, int phases);
+size_t prefill_workspace(int T);
+ds4g_status prefill_forward(const float *hidden, int T, const ds4g_layer *L, const int32_t *ids, const float *w,
+                            float *out, void *workspace, cudaStream_t st, int phases);
 
 // y = x / sqrt(mean(x^2) + 1e-6); one CTA of 256 threads per row of 4096.
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const float *x, float *y) {
@@ -56,6 +59,7 @@ extern "C" const char *ds4g_status_str(ds4g_status s) {
 
 extern "C" size_t ds4g_forward_workspace(int T) {
     if (T < 1) return 0;
+    if (T >= kPrefillMinT) return prefill_workspace(T);
     return decode_workspace(T < kDecodeMaxT ? T : kDecodeMaxT);
 }
 
@@ -85,8 +89,12 @@ static ds4g_status run_forward(const float *hidden, int T, const ds4g_layer *L, 
                                ds4g_stream_t s, int phases) {
     const ds4g_status chk = check_forward_args(hidden, T, L, ids, w, out, workspace, ws_bytes);
     if (chk != DS4G_OK) return chk;
-    if (phases != 3 && T > kDecodeMaxT) return DS4G_EUNSUPPORTED;
+    if (phases != 3 && T > kDecodeMaxT && T < kPrefillMinT) return DS4G_EUNSUPPORTED;
     cudaStream_t st = (cudaStream_t)s;
+    if (T >= kPrefillMinT) {
+        if ((long long)T * (kK + 1) * kH * 4 > (1ll << 40)) return DS4G_EUNSUPPORTED;
+        return prefill_forward(hidden, T, L, ids, w, out, workspace, st, phases);
+    }
     for (int t0 = 0; t0 < T; t0 += kDecodeMaxT) {
         const int n = T - t0 < kDecodeMaxT ? T - t0 : kDecodeMaxT;
         const ds4g_status rc = decode_forward(hidden + (size_t)t0 * kH, n, L, ids + (size_t)t0 * kK,

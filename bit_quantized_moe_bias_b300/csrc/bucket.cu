@@ -97,3 +97,12 @@ extern "C" ds4g_status ds4g_moe_bucket(const int32_t *ids, int T, int32_t *count
                                                     (uint32_t *)workspace);
     return cudaGetLastError() == cudaSuccess ? DS4G_OK : DS4G_ECUDA;
 }
+
+namespace ds4g {
+// Launch helper for the prefill path (same kernel, status word given directly).
+ds4g_status bucket_launch(const int32_t *ids, int T, int32_t *counts, int32_t *offsets, int32_t *perm,
+                          int32_t *inv, uint32_t *status, cudaStream_t st) {
+    bucket_kernel<<<1, 1024, 0, st>>>(ids, T * kK, counts, offsets, perm, inv, status);
+    return cudaGetLastError() == cudaSuccess ? DS4G_OK : DS4G_ECUDA;
+}
+}  // namespace ds4g

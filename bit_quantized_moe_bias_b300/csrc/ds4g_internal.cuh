@@ -16,6 +16,7 @@ constexpr int kF = DS4G_N_FF_EXP;      // 2048
 constexpr int kE = DS4G_N_EXPERT;      // 256
 constexpr int kK = DS4G_N_EXPERT_USED; // 6
 constexpr int kDecodeMaxT = 3;         // per-slot GEMV path handles T <= 3 (smem)
+constexpr int kPrefillMinT = 64;       // from here on: bucketed tensor-core GEMM path
 
 // ---------------------------------------------------------------------------
 // Packed ("tile-block") layout.  A [rows][cols] matrix is cut into tiles of

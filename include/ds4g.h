@@ -194,10 +194,19 @@ typedef struct {
  *   out[t] = s + sum_{k=0..5} w[t][k] * y_k     (fixed k order, no atomics)
  * hidden [T][4096] f32 dev, ids [T][6] int32 dev, w [T][6] f32 dev,
  * out [T][4096] f32 dev.  A repeated id within a token is legal (both terms
- * are summed).  Arithmetic: fp32 accumulation; activations enter the tensor
- * cores as an fp16 hi+lo pair for small T (|x| < 65504 required) and as bf16
- * for the bucketed prefill path (large T), where weights are bf16-rounded.
- * workspace dev >= ds4g_forward_workspace(T) bytes.
+ * are summed).  Two paths, chosen by T:
+ *  - T < 64 (decode): per-slot dequant-in-register GEMV, processed in chunks
+ *    of 3 tokens.  Codes enter the tensor cores exactly; activations as an
+ *    fp16 hi+lo pair (|x| < 65504 required, else DS4G_EDEVICE); fp32
+ *    accumulation.  Expected error ~1e-5 relative.
+ *  - T >= 64 (chunked prefill, large batches): tokens bucketed by expert,
+ *    grouped tcgen05 GEMM.  Weights are the fp32 block formula rounded to
+ *    nearest even: fp16 with fp16 activations for the routed gate/up
+ *    (|x| < 65504 required, else DS4G_EDEVICE), bf16 with bf16 h for the
+ *    down projection, bf16 throughout for the shared expert; fp32
+ *    accumulation.  Expected error ~1e-3 relative L2 per token.
+ * workspace dev >= ds4g_forward_workspace(T) bytes (about 200 KB per token
+ * on the prefill path).
  * ------------------------------------------------------------------------ */
 size_t ds4g_forward_workspace(int T);
 ds4g_status ds4g_moe_forward(const float *hidden, int T, const ds4g_layer *L,
@@ -210,8 +219,9 @@ ds4g_status ds4g_moe_forward(const float *hidden, int T, const ds4g_layer *L,
  * the shared expert into the workspace; ds4g_moe_down reads them from the
  * same workspace and writes out.  Same arguments and checks as
  * ds4g_moe_forward; calling gate_up then down on the same workspace and
- * stream equals one ds4g_moe_forward.  Only for T <= 3 (the per-slot decode
- * path), else DS4G_EUNSUPPORTED. */
+ * stream equals one ds4g_moe_forward.  For T <= 3 (one decode chunk) or
+ * T >= 64 (prefill path: gate_up = bucketing, permute and the gate/up GEMM;
+ * down = the down GEMM and the combine); other T -> DS4G_EUNSUPPORTED. */
 ds4g_status ds4g_moe_gate_up(const float *hidden, int T, const ds4g_layer *L,
                              const int32_t *ids, const float *w, float *out,
                              void *workspace, size_t ws_bytes, ds4g_stream_t s);

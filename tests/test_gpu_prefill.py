@@ -1,0 +1,139 @@
+"""GPU parity of the bucketed tensor-core path (T >= 64: chunked prefill and
+large batches) against the CPU oracle, through the C ABI.
+
+The path rounds activations and dequantised weights to bf16 and accumulates
+in fp32 on the tensor cores, so the statement's prefill bound applies:
+relative L2 error <= 1e-2 per token.  Tokens are independent given the
+routing, so at full size the oracle recomputes a seeded sample of tokens."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import E, F, H, K, grid_u64
+
+torch = pytest.importorskip("torch")
+import bit_quantized_moe_bias_b300 as B  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+REL_L2 = 1e-2
+
+
+class FullLayer:
+    """All 256 experts of one layer, generated and packed on the device with
+    the seeded generator's CUDA twin (host bytes regenerated on demand)."""
+
+    def __init__(self, seed, cfg, layer, gut=synth.IQ2_XXS, dt=synth.Q2_K):
+        self.seed, self.cfg, self.lay, self.gut, self.dt = seed, cfg, layer, gut, dt
+        sizes = {gut: B.ds4g_packed_size(gut, F, H), dt: B.ds4g_packed_size(dt, H, F)}
+        tmp = torch.empty(max(sizes.values()), dtype=torch.uint8, device=DEV)
+        mats = {}
+        st = torch.cuda.current_stream().cuda_stream
+        for kind, qt, rows, cols in ((synth.KIND_GATE, gut, F, H), (synth.KIND_UP, gut, F, H),
+                                     (synth.KIND_DOWN, dt, H, F)):
+            t = torch.empty(E, sizes[qt], dtype=torch.uint8, device=DEV)
+            for e in range(E):
+                synth.gguf_matrix_device(qt, rows, cols, seed, synth.stream_id(cfg, layer, kind, e), tmp.data_ptr(), st)
+                B.ds4g_quantize_pack_device(qt, rows, cols, tmp, t[e])
+            mats[kind] = t
+        self.shared = synth.shared(seed, cfg, layer)
+        sh = [torch.from_numpy(a.view(np.int16)).to(DEV) for a in self.shared]
+        self.grid, g64 = grid_u64(seed)
+        gridt = torch.from_numpy(g64.view(np.int64)).to(DEV)
+        self.L = B.MoELayer(mats[synth.KIND_GATE], mats[synth.KIND_UP], mats[synth.KIND_DOWN], *sh, gridt, gut, dt)
+        torch.cuda.synchronize()
+
+    def oracle(self, x, ids, w):
+        gate, up, down = [None] * E, [None] * E, [None] * E
+        for e in sorted(set(int(v) for v in ids.reshape(-1))):
+            gate[e], up[e], down[e] = synth.expert(self.seed, self.cfg, self.lay, e, self.gut, self.dt)
+        return oracle.moe_forward(x, ids, w, gate, up, down, *self.shared, self.grid, self.gut, self.dt)
+
+
+@pytest.fixture(scope="module")
+def layer_q2():
+    return FullLayer(0, 3, 0)
+
+
+def _t(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def _forward(L, x, ids, w):
+    T = x.shape[0]
+    out = torch.full((T, H), float("nan"), dtype=torch.float32, device=DEV)
+    ws = B.workspace(B.ds4g_forward_workspace(T))
+    B.ds4g_moe_forward(_t(x), L.L.struct, _t(ids), _t(w), out, ws)
+    st = B.ds4g_last_error(ws)
+    return out.cpu().numpy(), st
+
+
+def _check_rows(got, ref):
+    assert np.all(np.isfinite(got))
+    for i in range(ref.shape[0]):
+        num = np.linalg.norm(got[i].astype(np.float64) - ref[i])
+        den = np.linalg.norm(ref[i].astype(np.float64))
+        assert num <= REL_L2 * den, f"row {i}: rel L2 {num / den:.3e}"
+
+
+def _sample(T, n, seed):
+    rng = np.random.default_rng(seed)
+    idx = set(rng.choice(T, size=min(n, T), replace=False).tolist()) | {0, T - 1}
+    return np.array(sorted(idx))
+
+
+@pytest.mark.parametrize("T", [64, 300, 2048])
+def test_prefill_matches_oracle(layer_q2, T):
+    x = synth.hidden(0, 3, T)
+    ids, w, _, _ = oracle.route(x, synth.router(0, 3), synth.bias_normal(0, 3))
+    got, st = _forward(layer_q2, x, ids, w)
+    assert st == 0
+    s = _sample(T, 10, T)
+    _check_rows(got[s], layer_q2.oracle(x[s], ids[s], w[s]))
+
+
+def test_prefill_big_buckets_and_duplicates(layer_q2):
+    """Few experts take all slots: buckets of 64..192 rows span several
+    128-row chunks; repeated ids inside a token are summed twice."""
+    T = 64
+    x = synth.hidden(5, 3, T)
+    ids = np.tile(np.array([[5, 5, 5, 9, 9, 200]], np.int32), (T, 1))
+    ids[::7, 3] = 17
+    w = np.tile(np.array([[0.3, 0.2, 0.1, 0.15, 0.15, 0.1]], np.float32), (T, 1))
+    got, st = _forward(layer_q2, x, ids, w)
+    assert st == 0
+    s = _sample(T, 6, 1)
+    _check_rows(got[s], layer_q2.oracle(x[s], ids[s], w[s]))
+
+
+def test_prefill_deterministic(layer_q2):
+    T = 128
+    x = synth.hidden(7, 3, T)
+    ids, w, _, _ = oracle.route(x, synth.router(0, 3), synth.bias_normal(0, 3))
+    a, _ = _forward(layer_q2, x, ids, w)
+    b, _ = _forward(layer_q2, x, ids, w)
+    assert np.array_equal(a, b)
+
+
+def test_prefill_bad_id_is_flagged(layer_q2):
+    T = 64
+    x = synth.hidden(8, 3, T)
+    ids, w, _, _ = oracle.route(x, synth.router(0, 3), synth.bias_normal(0, 3))
+    ids[3, 2] = 300
+    got, st = _forward(layer_q2, x, ids, w)
+    assert st == 7
+    ok = np.array([t for t in range(T) if t != 3])
+    assert np.all(np.isfinite(got[ok]))
+
+
+def test_prefill_q4k_layer():
+    L = FullLayer(4, 4, 3, synth.Q4_K, synth.Q4_K)
+    T = 96
+    x = synth.hidden(4, 4, T)
+    ids, w, _, _ = oracle.route(x, synth.router(4, 4), synth.bias_zipf(4, 4))
+    got, st = _forward(L, x, ids, w)
+    assert st == 0
+    s = _sample(T, 8, 2)
+    _check_rows(got[s], L.oracle(x[s], ids[s], w[s]))
+    assert K == ids.shape[1]
