@@ -158,15 +158,26 @@ def run_ours(args, rank, world, local_rank):
     w = torch.empty(1, K, dtype=torch.float32, device=dev)
     rws = B.workspace(B.ds4g_route_workspace(1), dev)
     fws = B.workspace(B.ds4g_forward_workspace(1), dev)
-    launches_per_step = ntok * nl * 4
+    lws = B.workspace(B.ds4g_layer_decode_workspace(), dev)
+    fused = args.decode_path == "fused"
+    launches_per_step = ntok * nl * (1 if fused else 4)
 
     def step(timing=None):
         for i in range(ntok):
             cur = x_dev[i:i + 1]
             for l, (L, R, b) in enumerate(layers):
+                dst = out_all[i:i + 1] if l == nl - 1 else act[l & 1]
+                if fused:
+                    # one launch: rmsnorm + router + top-6 + routed and shared experts
+                    if timing is not None and i < timing[2]:
+                        timing[0][l + nl * i].record()
+                    B.ds4g_moe_layer_decode(cur, R, b, L.struct, ids, w, dst, lws)
+                    if timing is not None and i < timing[2]:
+                        timing[1][l + nl * i].record()
+                    cur = dst
+                    continue
                 B.ds4g_rmsnorm(cur, xn)
                 B.ds4g_moe_route(xn, R, b, ids, w, rws)
-                dst = out_all[i:i + 1] if l == nl - 1 else act[l & 1]
                 if timing is not None and i < timing[2]:
                     timing[0][l + nl * i].record()
                     B.ds4g_moe_gate_up(xn, L.struct, ids, w, dst, fws)
@@ -179,7 +190,7 @@ def run_ours(args, rank, world, local_rank):
     # eager warm-up (sets kernel attributes, checks status), then capture
     step()
     torch.cuda.synchronize()
-    st = B.ds4g_last_error(rws) or B.ds4g_last_error(fws)
+    st = B.ds4g_last_error(rws) or B.ds4g_last_error(fws) or B.ds4g_last_error(lws)
     if st:
         raise RuntimeError(f"device status {st} during warm-up")
     graph = torch.cuda.CUDAGraph()
@@ -228,7 +239,7 @@ def run_ours(args, rank, world, local_rank):
     step(timing=evs)
     torch.cuda.synchronize()
     gu_us = statistics.mean(a.elapsed_time(b) * 1e3 for a, b in zip(evs[0], evs[1]))
-    st = B.ds4g_last_error(rws) or B.ds4g_last_error(fws)
+    st = B.ds4g_last_error(rws) or B.ds4g_last_error(fws) or B.ds4g_last_error(lws)
     if st:
         raise RuntimeError(f"device status {st} after the timed region")
 
@@ -244,7 +255,9 @@ def run_ours(args, rank, world, local_rank):
     tokens = ntok * args.steps * world
     value = tokens / dev_s
     hbm, kind = peaks()
-    achieved = GATEUP_BYTES / (gu_us * 1e-6) / 1e9
+    kbytes = LAYER_BYTES if fused else GATEUP_BYTES
+    kname = "decode_t1_kernel (whole layer)" if fused else "gateup_decode_kernel"
+    achieved = kbytes / (gu_us * 1e-6) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dev_s / args.steps * 1e3, 3), "higher_is_better": True,
@@ -257,10 +270,10 @@ def run_ours(args, rank, world, local_rank):
                    "setup_s": round(setup_s, 1)},
         "e2e": {"value": round(tokens / e2e_s, 3), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(x_host.numel() * 4), "d2h_bytes_per_step": int(y_host.numel() * 4)},
-        "roofline": {"bound": "hbm", "kernel": "gateup_decode_kernel", "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1),
                      "peak": hbm, "peak_kind": kind, "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                     "bytes_per_launch": GATEUP_BYTES, "launch_us": round(gu_us, 3),
-                     "traffic": traffic_record("gateup_decode_kernel")},
+                     "bytes_per_launch": kbytes, "launch_us": round(gu_us, 3),
+                     "traffic": traffic_record("decode_t1_kernel" if fused else "gateup_decode_kernel")},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
@@ -481,6 +494,8 @@ def main():
     ap.add_argument("--workload", choices=["decode", "prefill"], default="decode",
                     help="decode = 43-layer full-depth decode (headline); prefill = T=2048 chunk, one layer")
     ap.add_argument("--cpu-tokens", type=int, default=8, help="prefill CPU-baseline sample size")
+    ap.add_argument("--decode-path", choices=["fused", "split"], default="fused",
+                    help="fused = one launch per layer; split = rmsnorm, route, gate/up, down launches")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

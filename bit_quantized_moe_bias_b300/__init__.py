@@ -66,6 +66,8 @@ def lib():
             "ds4g_moe_forward": (fwd, i),
             "ds4g_moe_gate_up": (fwd, i),
             "ds4g_moe_down": (fwd, i),
+            "ds4g_layer_decode_workspace": ([], sz),
+            "ds4g_moe_layer_decode": ([vp, i, vp, vp, C.POINTER(ds4g_layer), vp, vp, vp, vp, sz, vp], i),
             "ds4g_moe_forward_noalloc": ([vp, i, C.POINTER(ds4g_layer), vp, vp, vp, vp], i),
             "ds4g_rmsnorm": ([vp, i, vp, vp], i),
             "ds4g_last_error": ([vp, vp], i),
@@ -190,6 +192,19 @@ def ds4g_moe_gate_up(hidden, layer: ds4g_layer, ids, w, out, workspace, stream=N
 
 def ds4g_moe_down(hidden, layer: ds4g_layer, ids, w, out, workspace, stream=None):
     _fwd("ds4g_moe_down", hidden, layer, ids, w, out, workspace, stream)
+
+
+def ds4g_layer_decode_workspace() -> int:
+    return lib().ds4g_layer_decode_workspace()
+
+
+def ds4g_moe_layer_decode(hidden, router, bias, layer: ds4g_layer, ids, w, out, workspace, normalize=True,
+                          stream=None):
+    """rmsnorm (optional) + route + forward of one token in one launch."""
+    _check("ds4g_moe_layer_decode",
+           lib().ds4g_moe_layer_decode(_ptr(hidden), 1 if normalize else 0, _ptr(router), _ptr(bias), C.byref(layer),
+                                       _ptr(ids), _ptr(w), _ptr(out), _ptr(workspace), workspace.numel(),
+                                       _stream(stream)))
 
 
 def ds4g_moe_forward_noalloc(hidden, layer: ds4g_layer, ids, w, out, stream=None):

@@ -230,6 +230,29 @@ ds4g_status ds4g_moe_down(const float *hidden, int T, const ds4g_layer *L,
                           void *workspace, size_t ws_bytes, ds4g_stream_t s);
 
 /* ------------------------------------------------------------------------
+ * One decode token through one whole MoE layer in a single launch ([P1]
+ * §2.3: router logic and expert compute fused into one GPU dispatch; §3.2
+ * moe_forward).  With xn = hidden / sqrt(mean(hidden^2) + 1e-6) if normalize
+ * is non-zero, else xn = hidden:
+ *   ids, w = the router of ds4g_moe_route applied to xn
+ *   out    = ds4g_moe_forward(xn, ids, w)
+ * hidden [4096] f32 dev (T = 1), router [256][4096] f32 dev, bias [256] f32
+ * dev, ids [6] int32 dev (out), w [6] f32 dev (out), out [4096] f32 dev.
+ * Only IQ2_XXS/Q2_K layers (else DS4G_EUNSUPPORTED; use route + forward).
+ * Arithmetic as the decode path of ds4g_moe_forward, except that the shared
+ * expert is summed in fp32 FMA.  workspace dev >= ds4g_layer_decode_workspace()
+ * bytes, zeroed once before first use (the kernel leaves its counters at
+ * zero); one call at a time per workspace.  Kernel-detected faults (bad
+ * expert id, |xn| >= 65504, a bounded wait that expired) are read back with
+ * ds4g_last_error(workspace).
+ * ------------------------------------------------------------------------ */
+size_t ds4g_layer_decode_workspace(void);
+ds4g_status ds4g_moe_layer_decode(const float *hidden, int normalize, const float *router,
+                                  const float *bias, const ds4g_layer *L, int32_t *ids,
+                                  float *w, float *out, void *workspace, size_t ws_bytes,
+                                  ds4g_stream_t s);
+
+/* ------------------------------------------------------------------------
  * ds4g_moe_forward without a workspace, for callers that cannot allocate
  * device memory: code running inside an allocator or memory-pool callback
  * (where calling cudaMalloc would re-enter the allocator), a real-time loop
