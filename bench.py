@@ -233,12 +233,18 @@ def run_ours(args, rank, world, local_rank):
     e2e_s = time.perf_counter() - t0
     barrier()
     # ---- roofline of the dominant kernel (gate/up), CUDA events on its stream
-    ntime = min(ntok, 8)
-    evs = ([torch.cuda.Event(enable_timing=True) for _ in range(nl * ntime)],
-           [torch.cuda.Event(enable_timing=True) for _ in range(nl * ntime)], ntime)
-    step(timing=evs)
-    torch.cuda.synchronize()
-    gu_us = statistics.mean(a.elapsed_time(b) * 1e3 for a, b in zip(evs[0], evs[1]))
+    if fused:
+        # one kernel per layer: its average duration over the timed graph
+        # replays (CUDA events on the replay stream) is the step time divided
+        # by the launches; eager per-launch events would include host gaps
+        gu_us = dev_s / args.steps / (ntok * nl) * 1e6
+    else:
+        ntime = min(ntok, 8)
+        evs = ([torch.cuda.Event(enable_timing=True) for _ in range(nl * ntime)],
+               [torch.cuda.Event(enable_timing=True) for _ in range(nl * ntime)], ntime)
+        step(timing=evs)
+        torch.cuda.synchronize()
+        gu_us = statistics.mean(a.elapsed_time(b) * 1e3 for a, b in zip(evs[0], evs[1]))
     st = B.ds4g_last_error(rws) or B.ds4g_last_error(fws) or B.ds4g_last_error(lws)
     if st:
         raise RuntimeError(f"device status {st} after the timed region")

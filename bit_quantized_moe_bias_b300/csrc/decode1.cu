@@ -41,21 +41,24 @@ constexpr int kNGrp = 4;                         // consumer groups
 constexpr int kGW = 4;                           // warps per group
 constexpr int kD1Cons = kNGrp * kGW;             // 16 consumer warps
 constexpr int kD1Threads = (2 + kD1Cons) * 32;   // producer + router + consumers
-constexpr int kD1Slot = 8448;                    // 8 x 1056: half an IQ2 row tile, the largest piece
-constexpr int kSlotsPerGrp = 4;                  // three pieces in flight per group
+constexpr int kD1Slot = 16896;                   // 16 x 1056: an IQ2 row tile, the largest piece
+constexpr int kSlotsPerGrp = 2;                  // one piece in flight while one is computed
 constexpr int kD1Slots = kNGrp * kSlotsPerGrp;   // 16
 
-// jobs and pieces per phase, in order: router rows (2 halves), shared
-// gate/up rows (gate row, up row), shared down row pairs (1 piece), routed
-// gate/up (slot, 16-row tile: gate/up x 2 halves), routed down (slot, 16-row
-// tile: 2 halves of 4 tile-blocks)
+// Jobs per phase, in order, and their pieces (each one contiguous copy of
+// about 16 KB: a bulk copy has a fixed cost, so pieces are kept large):
+//   router rows                       1 piece (16 KB)
+//   shared gate/up row pairs          2 pieces (gate rows, up rows: 16 KB each)
+//   shared down 4-row groups          1 piece (16 KB)
+//   routed gate/up (slot, 16-row tile) 2 pieces (gate, up: 16 tile-blocks each)
+//   routed down (slot, 16-row tile)   1 piece (8 Q2_K tile-blocks, 10.5 KB)
 constexpr int kNPhase = 5;
 constexpr int kJR = kE;
-constexpr int kJSG = kF;
-constexpr int kJSD = kH / 2;
+constexpr int kJSG = kF / 2;
+constexpr int kJSD = kH / 4;
 constexpr int kJRG = kK * (kF / 16);
 constexpr int kJRD = kK * (kH / 16);
-constexpr int kTileParts = 8 + kK;      // jobs contributing to one 16-row output tile
+constexpr int kTileParts = 4 + kK;      // jobs contributing to one 16-row output tile
 
 enum : int { PK_END = 0, PK_ROUTER, PK_SGU, PK_RGU, PK_SDN, PK_RDN };
 
@@ -101,13 +104,14 @@ struct D1Args {
 constexpr uint32_t kOffRing = 0;
 constexpr uint32_t kOffDesc = kOffRing + kD1Slots * kD1Slot;
 constexpr uint32_t kOffU = kOffDesc + kD1Slots * 16;
-constexpr uint32_t kUnion = 256 * 16 * 8 + 128 * 16 * 8 + kH * 4 + 2 * kH * 2;  // 80 KB (phase B uses 52 KB)
+constexpr uint32_t kUnion = 256 * 16 * 8 + 128 * 8 * 8 + kH * 4 + 2 * kH * 2;  // 72 KB (phase B uses 52 KB)
 constexpr uint32_t kOffHs = kOffU + kUnion;      // shared h (fp32), outside the union
 constexpr uint32_t kOffRed = kOffHs + kF * 4;
 constexpr uint32_t kOffZero = kOffRed + kNGrp * 2 * 128 * 4;
 constexpr uint32_t kOffWk = kOffZero + 512;
 constexpr uint32_t kOffIds = kOffWk + 32;
-constexpr uint32_t kOffCred = kOffIds + 32;
+constexpr uint32_t kOffEptr = kOffIds + 32;      // 18 expert matrix pointers (gate, up, down x 6)
+constexpr uint32_t kOffCred = kOffEptr + 18 * 8;
 constexpr uint32_t kOffBar = kOffCred + 64;
 constexpr uint32_t kOffFlags = kOffBar + 2 * kD1Slots * 8;
 constexpr size_t kD1SmemBytes = kOffFlags + 16;
@@ -116,7 +120,7 @@ struct D1Smem {
     uint8_t *ring;
     D1Desc *desc;
     uint2 *gtab;           // [256][16]   (phase A)
-    uint2 *stab;           // [128][16]
+    uint2 *stab;           // [128][8]
     float *xn;             // [4096]
     __half *xq;            // [2][4096] hi, lo
     __half *hq;            // [6][2][2048] (phase B, aliases phase A)
@@ -126,6 +130,7 @@ struct D1Smem {
     __half *zero;          // [256] zeros: operand of the inactive mma lanes
     float *wk;             // [6]
     int *ids_s;            // [6]
+    const uint8_t **eptr;  // [18] gate[6], up[6], down[6] of the selected experts (NULL if unusable)
     float *cta_red;        // [16]
     uint64_t *full, *empty;
     int *flags;            // [0] abort, [1] ids ready, [2] shared h: 0 absent, 1 loading, 2 present
@@ -139,7 +144,7 @@ __device__ __forceinline__ D1Smem d1_smem() {
     s.desc = reinterpret_cast<D1Desc *>(d1_raw + kOffDesc);
     s.gtab = reinterpret_cast<uint2 *>(d1_raw + kOffU);
     s.stab = s.gtab + 256 * 16;
-    s.xn = reinterpret_cast<float *>(s.stab + 128 * 16);
+    s.xn = reinterpret_cast<float *>(s.stab + 128 * 8);
     s.xq = reinterpret_cast<__half *>(s.xn + kH);
     s.hq = reinterpret_cast<__half *>(d1_raw + kOffU);
     s.xs16 = reinterpret_cast<float *>(s.hq + kK * 2 * kF);
@@ -148,6 +153,7 @@ __device__ __forceinline__ D1Smem d1_smem() {
     s.zero = reinterpret_cast<__half *>(d1_raw + kOffZero);
     s.wk = reinterpret_cast<float *>(d1_raw + kOffWk);
     s.ids_s = reinterpret_cast<int *>(d1_raw + kOffIds);
+    s.eptr = reinterpret_cast<const uint8_t **>(d1_raw + kOffEptr);
     s.cta_red = reinterpret_cast<float *>(d1_raw + kOffCred);
     s.full = reinterpret_cast<uint64_t *>(d1_raw + kOffBar);
     s.empty = s.full + kD1Slots;
@@ -230,21 +236,22 @@ __device__ __forceinline__ float dot8_bf16(uint4 wv, const float *xv, float acc)
 }
 
 // ------------------------------------------------------ piece consumers
-// Half a router row (2048 fp32, columns [2048 hf, +2048)) against xn: warp
-// wq takes columns [512 wq, +512) of the half; returns this lane's partial.
-__device__ __forceinline__ float router_half(const D1Smem &sm, const uint8_t *slot, int hf, int wq, int lane) {
-    const float4 *r = reinterpret_cast<const float4 *>(slot) + 128 * wq + lane;
-    const float4 *x = reinterpret_cast<const float4 *>(sm.xn + 2048 * hf) + 128 * wq + lane;
-    float acc = 0.f;
+// A router row (4096 fp32) against xn: warp wq takes columns [1024 wq, +1024);
+// returns this lane's partial.
+__device__ __forceinline__ float router_row(const D1Smem &sm, const uint8_t *slot, int wq, int lane) {
+    const float4 *r = reinterpret_cast<const float4 *>(slot) + 256 * wq + lane;
+    const float4 *x = reinterpret_cast<const float4 *>(sm.xn) + 256 * wq + lane;
+    float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 8; ++i) {
         const float4 rv = r[32 * i], xv = x[32 * i];
+        float &acc = (i & 1) ? acc1 : acc0;
         acc = fmaf(rv.x, xv.x, acc);
         acc = fmaf(rv.y, xv.y, acc);
         acc = fmaf(rv.z, xv.z, acc);
         acc = fmaf(rv.w, xv.w, acc);
     }
-    return acc;
+    return acc0 + acc1;
 }
 
 // 1024 bf16 weights at w (smem) dotted with 1024 fp32 values at v (smem),
@@ -285,7 +292,7 @@ __device__ __forceinline__ void iq2_tileblock(const D1Smem &sm, const uint8_t *t
     const float d4g = __half2float(__ushort_as_half((unsigned short)(dd & 0xffffu))) * 4194304.0f;
     const float d4h = __half2float(__ushort_as_half((unsigned short)(dd >> 16))) * 4194304.0f;
     const __half *xb = ((g >> 1) == t) ? sm.xq + (g & 1) * kH + 256 * b + 32 * t : sm.zero;
-    const uint2 *gt = sm.gtab + p, *st = sm.stab + p;   // entry i at gt[16 i]
+    const uint2 *gt = sm.gtab + p, *st = sm.stab + (lane & 7);   // entry i at gt[16 i], st[8 i]
     float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
     for (int jj = 0; jj < 2; ++jj) {
@@ -307,8 +314,8 @@ __device__ __forceinline__ void iq2_tileblock(const D1Smem &sm, const uint8_t *t
         for (int l = 0; l < 4; ++l) {
             const uint2 ga = gt[16 * __byte_perm(ia, 0, 0x4440 + l)];
             const uint2 gb = gt[16 * __byte_perm(ib, 0, 0x4440 + l)];
-            const uint2 sa = st[16 * bfe7(va, 7 * l)];
-            const uint2 sbv = st[16 * bfe7(vb, 7 * l)];
+            const uint2 sa = st[8 * bfe7(va, 7 * l)];
+            const uint2 sbv = st[8 * bfe7(vb, 7 * l)];
             mma_f16(c0, prmt(ga.x, sa.x, 0x5140), prmt(gb.x, sbv.x, 0x5140), prmt(ga.x, sa.x, 0x7362),
                     prmt(gb.x, sbv.x, 0x7362), B[4 * l], B[4 * l + 1]);
             mma_f16(c1, prmt(ga.y, sa.y, 0x5140), prmt(gb.y, sbv.y, 0x5140), prmt(ga.y, sa.y, 0x7362),
@@ -316,6 +323,68 @@ __device__ __forceinline__ void iq2_tileblock(const D1Smem &sm, const uint8_t *t
         }
         acc0 = fmaf(d4g * half_plus(va >> 28), (c0[0] + c0[1]) + (c1[0] + c1[1]), acc0);
         acc1 = fmaf(d4h * half_plus(vb >> 28), (c0[2] + c0[3]) + (c1[2] + c1[3]), acc1);
+    }
+    acc0 += __shfl_xor_sync(0xffffffffu, acc0, 1);
+    acc0 += __shfl_xor_sync(0xffffffffu, acc0, 2);
+    acc1 += __shfl_xor_sync(0xffffffffu, acc1, 1);
+    acc1 += __shfl_xor_sync(0xffffffffu, acc1, 2);
+    r0 = acc0;
+    r1 = acc1;
+}
+
+// Two adjacent IQ2_XXS tile-blocks (block columns b0, b0 + 1; 16 rows x 512
+// cols) processed interleaved for instruction-level parallelism; returns the
+// sum of both (in lanes t == 0) for rows g and g+8.  Same arithmetic as
+// iq2_tileblock.
+__device__ __forceinline__ void iq2_tileblock2(const D1Smem &sm, const uint8_t *tb, int b0, int lane, float &r0,
+                                               float &r1) {
+    const int g = lane >> 2, t = lane & 3, p = lane & 15;
+    uint4 qa[2], qb[2];
+    float d4g[2], d4h[2];
+    const __half *xb[2];
+    const bool act = (g >> 1) == t;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const uint8_t *tbu = tb + u * kTB_IQ2;
+        qa[u] = *reinterpret_cast<const uint4 *>(tbu + 16 * lane);
+        qb[u] = *reinterpret_cast<const uint4 *>(tbu + 512 + 16 * lane);
+        const uint32_t dd = *reinterpret_cast<const uint32_t *>(tbu + 1024 + 4 * g);
+        d4g[u] = __half2float(__ushort_as_half((unsigned short)(dd & 0xffffu))) * 4194304.0f;
+        d4h[u] = __half2float(__ushort_as_half((unsigned short)(dd >> 16))) * 4194304.0f;
+        xb[u] = act ? sm.xq + (g & 1) * kH + 256 * (b0 + u) + 32 * t : sm.zero;
+    }
+    const uint2 *gt = sm.gtab + p, *st = sm.stab + (lane & 7);   // entry i at gt[16 i], st[8 i]
+    float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+        float c0[2][4], c1[2][4];
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) c0[u][i] = c1[u][i] = 0.f;
+#pragma unroll
+        for (int l = 0; l < 4; ++l) {
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const uint4 B4 = *reinterpret_cast<const uint4 *>(xb[u] + 128 * jj + 8 * l);
+                const uint32_t ia = jj ? qa[u].z : qa[u].x, va = jj ? qa[u].w : qa[u].y;
+                const uint32_t ib = jj ? qb[u].z : qb[u].x, vb = jj ? qb[u].w : qb[u].y;
+                const uint2 ga = gt[16 * __byte_perm(ia, 0, 0x4440 + l)];
+                const uint2 gb = gt[16 * __byte_perm(ib, 0, 0x4440 + l)];
+                const uint2 sa = st[8 * bfe7(va, 7 * l)];
+                const uint2 sbv = st[8 * bfe7(vb, 7 * l)];
+                mma_f16(c0[u], prmt(ga.x, sa.x, 0x5140), prmt(gb.x, sbv.x, 0x5140), prmt(ga.x, sa.x, 0x7362),
+                        prmt(gb.x, sbv.x, 0x7362), B4.x, B4.y);
+                mma_f16(c1[u], prmt(ga.y, sa.y, 0x5140), prmt(gb.y, sbv.y, 0x5140), prmt(ga.y, sa.y, 0x7362),
+                        prmt(gb.y, sbv.y, 0x7362), B4.z, B4.w);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const uint32_t va = jj ? qa[u].w : qa[u].y, vb = jj ? qb[u].w : qb[u].y;
+            acc0 = fmaf(d4g[u] * half_plus(va >> 28), (c0[u][0] + c0[u][1]) + (c1[u][0] + c1[u][1]), acc0);
+            acc1 = fmaf(d4h[u] * half_plus(vb >> 28), (c0[u][2] + c0[u][3]) + (c1[u][2] + c1[u][3]), acc1);
+        }
     }
     acc0 += __shfl_xor_sync(0xffffffffu, acc0, 1);
     acc0 += __shfl_xor_sync(0xffffffffu, acc0, 2);
@@ -416,6 +485,19 @@ __device__ void d1_topk(const D1Args &a, const D1Smem &sm, const float (&bias_r)
         sel_e[k] = be;
         sel_s[k] = sv;
     }
+    // the producer streams the selected experts' matrices: cache their
+    // pointers here (one global load per pointer, once per CTA)
+    if (lane < 3 * kK) {
+        const int k = lane % kK, m = lane / kK;
+        int e = 0;
+#pragma unroll
+        for (int kk = 0; kk < kK; ++kk)
+            if (kk == k) e = sel_e[kk];
+        const uint8_t *const *tab = m == 0 ? a.gate : m == 1 ? a.up : a.down;
+        const uint8_t *ptr = tab[e];
+        sm.eptr[lane] = (ptr && !((uintptr_t)ptr & 15)) ? ptr : nullptr;
+    }
+    __syncwarp();
     if (lane == 0) {
         float sum = 0.f;
 #pragma unroll
@@ -440,7 +522,7 @@ __device__ __forceinline__ int phase_jobs(int p) {
     return p == 0 ? kJR : p == 1 ? kJSG : p == 2 ? kJSD : p == 3 ? kJRG : kJRD;
 }
 __device__ __forceinline__ int phase_off(int p, int c, int G) { return (p & 1) ? (G - 1 - c) : c; }
-__device__ __forceinline__ int phase_pieces(int p) { return p == 3 ? 4 : p == 2 ? 1 : 2; }
+__device__ __forceinline__ int phase_pieces(int p) { return (p == 1 || p == 3) ? 2 : 1; }
 
 // The CTA's i-th job -> (phase, job index); false past the end.
 __device__ __forceinline__ bool cta_job(int i, int c, int G, const int (&cnt)[kNPhase], int &p, int &j) {
@@ -454,6 +536,23 @@ __device__ __forceinline__ bool cta_job(int i, int c, int G, const int (&cnt)[kN
         i -= cnt[q];
     }
     return false;
+}
+
+// If this warp's counted job was the last of its 16-row output tile (the
+// counter returned kTileParts - 1), sum the tile's partials in a fixed order:
+// shared expert, then routed experts k = 0..5.
+__device__ __forceinline__ void finish_tile(const D1Args &a, int tile, uint32_t old_lane0, int lane) {
+    if (tile < 0) return;
+    const uint32_t old = __shfl_sync(0xffffffffu, old_lane0, 0);
+    if (old != kTileParts - 1) return;
+    if (lane < 16) {
+        const int row = 16 * tile + lane;
+        float v = __ldcg(a.p_s + row);
+#pragma unroll
+        for (int k = 0; k < kK; ++k) v += __ldcg(a.p_r + (size_t)k * kH + row);
+        a.out[row] = v;
+    }
+    if (lane == 0) a.sync->tile_cnt[tile] = 0u;
 }
 
 __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
@@ -480,106 +579,99 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
     }
 
     if (warp == 0) {
-        // ================================================== producer
-        if (lane == 0) {
-            int gi[kNGrp], pcq[kNGrp];
-            uint32_t itq[kNGrp];
-            bool fin[kNGrp];
-#pragma unroll
-            for (int q = 0; q < kNGrp; ++q) {
-                gi[q] = q;
-                pcq[q] = 0;
-                itq[q] = 0;
-                fin[q] = false;
-            }
+        // ================================================== producers
+        // Lane q feeds group q's ring, so the four rings fill in parallel.
+        if (lane < kNGrp) {
+            const int q = lane;
+            int gi = q, pcq = 0;
+            uint32_t itq = 0;
             bool ids_known = false;
-            int nfin = 0;
             long long t_idle = clock64();
-            while (nfin < kNGrp) {
+            while (true) {
                 if (*abort_flag) break;   // consumers leave on abort; nothing more to feed
-                bool prog = false;
-#pragma unroll
-                for (int q = 0; q < kNGrp; ++q) {
-                    if (fin[q]) continue;
-                    const int s = kSlotsPerGrp * q + (int)(itq[q] % kSlotsPerGrp);
-                    if (!tc::mbar_test_wait(&sm.empty[s], ((itq[q] / kSlotsPerGrp) & 1u) ^ 1u)) continue;
-                    int p, j;
-                    if (!cta_job(gi[q], c, G, cnt, p, j)) {
-                        sm.desc[s].kind = PK_END;
-                        tc::mbar_arrive(&sm.full[s]);
-                        fin[q] = true;
-                        ++nfin;
-                        prog = true;
+                const int s = kSlotsPerGrp * q + (int)(itq % kSlotsPerGrp);
+                if (!tc::mbar_test_wait(&sm.empty[s], ((itq / kSlotsPerGrp) & 1u) ^ 1u)) {
+                    if (clock64() - t_idle > (2ll << 30)) {
+                        // no slot freed for ~1 s: give up, let the groups finish
+                        d1_abort(a, sm.flags, 0x11u);
+                        break;
+                    }
+                    continue;
+                }
+                int p, j;
+                if (!cta_job(gi, c, G, cnt, p, j)) {
+                    sm.desc[s].kind = PK_END;
+                    tc::mbar_arrive(&sm.full[s]);
+                    break;
+                }
+                if ((p == 3 || p == 4) && !ids_known) {
+                    if (*reinterpret_cast<volatile int *>(&sm.flags[1]) == 0) {   // later
+                        if (clock64() - t_idle > (2ll << 30)) {
+                            d1_abort(a, sm.flags, 0x12u);
+                            break;
+                        }
                         continue;
                     }
-                    if ((p == 3 || p == 4) && !ids_known) {
-                        if (*reinterpret_cast<volatile int *>(&sm.flags[1]) == 0) continue;   // later
-                        ids_known = true;
-                    }
-                    const int pc = pcq[q];
-                    uint8_t *dst = sm.ring + (size_t)s * kD1Slot;
-                    D1Desc d;
-                    d.job = j;
-                    d.piece = pc;
-                    d.e = 0;
-                    const void *src = nullptr;
-                    uint32_t bytes = 0;
-                    if (p == 0) {
-                        d.kind = PK_ROUTER;
-                        src = a.router + (size_t)j * kH + 2048 * pc;
-                        bytes = 2048 * 4;
-                    } else if (p == 1) {
-                        d.kind = PK_SGU;
-                        src = (pc ? a.sh_up : a.sh_gate) + (size_t)j * kH;
-                        bytes = kH * 2;
-                    } else if (p == 2) {
-                        d.kind = PK_SDN;
-                        src = a.sh_down + (size_t)(2 * j) * kF;
-                        bytes = 2 * kF * 2;
-                    } else if (p == 3) {
-                        d.kind = PK_RGU;
-                        const int k = j / (kF / 16), tile = j % (kF / 16), e = sm.ids_s[k];
-                        d.e = k;
-                        if (expert_ok(e, (const void *const *)a.gate, (const void *const *)a.up, nullptr)) {
-                            src = ((pc >> 1) ? a.up[e] : a.gate[e]) + ((size_t)tile * 16 + 8 * (pc & 1)) * kTB_IQ2;
-                            bytes = 8 * kTB_IQ2;
-                        } else {
-                            d.e = -1;
-                            flag_status(a.status, DS4G_EDEVICE, (uint32_t)e);
-                        }
-                    } else {
-                        d.kind = PK_RDN;
-                        const int k = j / (kH / 16), tile = j % (kH / 16), e = sm.ids_s[k];
-                        d.e = k;
-                        if (expert_ok(e, (const void *const *)a.down, nullptr, nullptr)) {
-                            src = a.down[e] + ((size_t)tile * 8 + 4 * pc) * kTB_Q2K;
-                            bytes = 4 * kTB_Q2K;
-                        } else {
-                            d.e = -1;
-                            flag_status(a.status, DS4G_EDEVICE, (uint32_t)e);
-                        }
-                    }
-                    sm.desc[s] = d;
-                    if (bytes) {
-                        tc::mbar_arrive_expect_tx(&sm.full[s], bytes);
-                        bulk_load(dst, src, bytes, &sm.full[s]);
-                    } else {
-                        tc::mbar_arrive(&sm.full[s]);
-                    }
-                    ++itq[q];
-                    if (++pcq[q] == phase_pieces(p)) {
-                        pcq[q] = 0;
-                        gi[q] += kNGrp;
-                    }
-                    prog = true;
+                    ids_known = true;
                 }
-                if (prog) {
-                    t_idle = clock64();
-                } else if (clock64() - t_idle > (2ll << 30)) {
-                    // no slot freed and no ids for ~1 s: give up, let the groups finish
-                    d1_abort(a, sm.flags, 0x11u);
-                    t_idle = clock64();
+                const int pc = pcq;
+                uint8_t *dst = sm.ring + (size_t)s * kD1Slot;
+                D1Desc d;
+                d.job = j;
+                d.piece = pc;
+                d.e = 0;
+                const void *src = nullptr;
+                uint32_t bytes = 0;
+                if (p == 0) {
+                    d.kind = PK_ROUTER;
+                    src = a.router + (size_t)j * kH;
+                    bytes = kH * 4;
+                } else if (p == 1) {
+                    d.kind = PK_SGU;
+                    src = (pc ? a.sh_up : a.sh_gate) + (size_t)(2 * j) * kH;
+                    bytes = 2 * kH * 2;
+                } else if (p == 2) {
+                    d.kind = PK_SDN;
+                    src = a.sh_down + (size_t)(4 * j) * kF;
+                    bytes = 4 * kF * 2;
+                } else if (p == 3) {
+                    d.kind = PK_RGU;
+                    const int k = j / (kF / 16), tile = j % (kF / 16);
+                    const uint8_t *mat = sm.eptr[(pc ? kK : 0) + k];
+                    d.e = k;
+                    if (mat && sm.eptr[k] && sm.eptr[kK + k]) {
+                        src = mat + (size_t)tile * 16 * kTB_IQ2;
+                        bytes = 16 * kTB_IQ2;
+                    } else {
+                        d.e = -1;
+                        flag_status(a.status, DS4G_EDEVICE, (uint32_t)sm.ids_s[k]);
+                    }
+                } else {
+                    d.kind = PK_RDN;
+                    const int k = j / (kH / 16), tile = j % (kH / 16);
+                    const uint8_t *mat = sm.eptr[2 * kK + k];
+                    d.e = k;
+                    if (mat) {
+                        src = mat + (size_t)tile * 8 * kTB_Q2K;
+                        bytes = 8 * kTB_Q2K;
+                    } else {
+                        d.e = -1;
+                        flag_status(a.status, DS4G_EDEVICE, (uint32_t)sm.ids_s[k]);
+                    }
                 }
+                sm.desc[s] = d;
+                if (bytes) {
+                    tc::mbar_arrive_expect_tx(&sm.full[s], bytes);
+                    bulk_load(dst, src, bytes, &sm.full[s]);
+                } else {
+                    tc::mbar_arrive(&sm.full[s]);
+                }
+                ++itq;
+                if (++pcq == phase_pieces(p)) {
+                    pcq = 0;
+                    gi += kNGrp;
+                }
+                t_idle = clock64();
             }
         }
     } else if (warp == 1) {
@@ -605,8 +697,8 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) xv[i] = __ldg(a.x + ct + 512 * i);
         const uint64_t grow = ct < 256 ? __ldg(reinterpret_cast<const unsigned long long *>(a.grid) + ct) : 0ull;
-        for (int i = ct; i < 128 * 16; i += kD1Cons * 32) {
-            const uint32_t s7 = (uint32_t)(i >> 4);
+        for (int i = ct; i < 128 * 8; i += kD1Cons * 32) {
+            const uint32_t s7 = (uint32_t)(i >> 3);
             const uint32_t sg = s7 | ((uint32_t)(__popc(s7) & 1) << 7);
             uint32_t lo = 0, hi = 0;
 #pragma unroll
@@ -643,9 +735,9 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
         }
         asm volatile("bar.sync 1, %0;" ::"n"(kD1Cons * 32));
 
-        float pr = 0.f;                                   // router partial
         float rg0 = 0.f, rg1 = 0.f, ru0 = 0.f, ru1 = 0.f; // routed gate/up partials, rows g, g+8
-        float rdn0 = 0.f, rdn1 = 0.f;                     // routed down partials, rows g, g+8
+        int pend_tile = -1;                               // tile counted by this warp, not yet examined
+        uint32_t pend_old = 0u;
         bool in_down = false;
         int gpar = 0;
         for (uint32_t it = 0;; ++it) {
@@ -757,37 +849,32 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
             float *red = sm.red + (q * 2 + gpar) * 128;
             bool last = false;
             if (d.kind == PK_ROUTER) {
-                if (d.piece == 0) pr = 0.f;
-                pr += router_half(sm, slot, d.piece, wq, lane);
-                if (d.piece == 1) {
-                    const float v = warp_sum(pr);
-                    if (lane == 0) red[wq] = v;
-                    last = true;
-                }
+                // router row: warp wq takes columns [1024 wq, +1024)
+                const float v = warp_sum(router_row(sm, slot, wq, lane));
+                if (lane == 0) red[wq] = v;
+                last = true;
             } else if (d.kind == PK_SGU) {
-                // piece 0: gate row j, piece 1: up row j; warp wq: columns [1024 wq, +1024)
-                const float v = bf16_dot1024(reinterpret_cast<const __nv_bfloat16 *>(slot) + 1024 * wq,
-                                             sm.xn + 1024 * wq, lane);
+                // piece 0: gate rows 2j, 2j+1; piece 1: up rows; warp wq: row wq>>1, half wq&1
+                const __nv_bfloat16 *w = reinterpret_cast<const __nv_bfloat16 *>(slot) + (wq >> 1) * kH + 2048 * (wq & 1);
+                const float *xv = sm.xn + 2048 * (wq & 1);
+                const float v = bf16_dot1024(w, xv, lane) + bf16_dot1024(w + 1024, xv + 1024, lane);
                 if (lane == 0) red[4 * d.piece + wq] = v;
                 last = d.piece == 1;
             } else if (d.kind == PK_RGU) {
                 if (d.piece == 0) rg0 = rg1 = ru0 = ru1 = 0.f;
                 if (d.e >= 0) {
-#pragma unroll 1
-                    for (int i = 0; i < 2; ++i) {
-                        float t0, t1;
-                        iq2_tileblock(sm, slot + (size_t)(2 * wq + i) * kTB_IQ2, 8 * (d.piece & 1) + 2 * wq + i, lane,
-                                      t0, t1);
-                        if (d.piece >> 1) {
-                            ru0 += t0;
-                            ru1 += t1;
-                        } else {
-                            rg0 += t0;
-                            rg1 += t1;
-                        }
+                    float t0, t1, t2, t3;
+                    iq2_tileblock2(sm, slot + (size_t)(4 * wq) * kTB_IQ2, 4 * wq, lane, t0, t1);
+                    iq2_tileblock2(sm, slot + (size_t)(4 * wq + 2) * kTB_IQ2, 4 * wq + 2, lane, t2, t3);
+                    if (d.piece) {
+                        ru0 += t0 + t2;
+                        ru1 += t1 + t3;
+                    } else {
+                        rg0 += t0 + t2;
+                        rg1 += t1 + t3;
                     }
                 }
-                if (d.piece == 3) {
+                if (d.piece == 1) {
                     if ((lane & 3) == 0) {
                         red[wq * 16 + (lane >> 2)] = rg0;
                         red[wq * 16 + (lane >> 2) + 8] = rg1;
@@ -797,31 +884,29 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
                     last = true;
                 }
             } else if (d.kind == PK_SDN) {
-                // shared down rows 2j, 2j+1; warp wq: row wq>>1, half wq&1
-                const float v = bf16_dot1024(reinterpret_cast<const __nv_bfloat16 *>(slot) + (wq >> 1) * kF +
-                                                 1024 * (wq & 1),
-                                             sm.hs + 1024 * (wq & 1), lane);
+                // shared down rows 4j .. 4j+3; warp wq: row wq, all 2048 columns
+                const __nv_bfloat16 *w = reinterpret_cast<const __nv_bfloat16 *>(slot) + (size_t)wq * kF;
+                const float v = bf16_dot1024(w, sm.hs, lane) + bf16_dot1024(w + 1024, sm.hs + 1024, lane);
                 if (lane == 0) red[wq] = v;
                 last = true;
-            } else {  // PK_RDN: four Q2_K tile-blocks of one expert; warp wq: tile-block wq
-                if (d.piece == 0) rdn0 = rdn1 = 0.f;
+            } else {  // PK_RDN: eight Q2_K tile-blocks of one expert; warp wq: tile-blocks 2wq, 2wq+1
+                float s0 = 0.f, s1 = 0.f;
                 if (d.e >= 0) {
-                    float s0, s1;
-                    q2k_tileblock(sm, slot + (size_t)wq * kTB_Q2K, d.e, 4 * d.piece + wq, lane, s0, s1);
-                    rdn0 += s0;
-                    rdn1 += s1;
+                    float a0, a1, b0, b1;
+                    q2k_tileblock(sm, slot + (size_t)(2 * wq) * kTB_Q2K, d.e, 2 * wq, lane, a0, a1);
+                    q2k_tileblock(sm, slot + (size_t)(2 * wq + 1) * kTB_Q2K, d.e, 2 * wq + 1, lane, b0, b1);
+                    s0 = a0 + b0;
+                    s1 = a1 + b1;
                 }
-                if (d.piece == 1) {
-                    rdn0 += __shfl_xor_sync(0xffffffffu, rdn0, 1);
-                    rdn0 += __shfl_xor_sync(0xffffffffu, rdn0, 2);
-                    rdn1 += __shfl_xor_sync(0xffffffffu, rdn1, 1);
-                    rdn1 += __shfl_xor_sync(0xffffffffu, rdn1, 2);
-                    if ((lane & 3) == 0) {
-                        red[wq * 16 + (lane >> 2)] = rdn0;
-                        red[wq * 16 + (lane >> 2) + 8] = rdn1;
-                    }
-                    last = true;
+                s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+                s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+                s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+                s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+                if ((lane & 3) == 0) {
+                    red[wq * 16 + (lane >> 2)] = s0;
+                    red[wq * 16 + (lane >> 2) + 8] = s1;
                 }
+                last = true;
             }
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&sm.empty[s]);
@@ -836,11 +921,12 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
                         red_add_release(&a.sync->router_done, 1u);
                     }
                 } else if (d.kind == PK_SGU) {
-                    if (lane == 0) {
-                        a.h_s[d.job] =
-                            silu_f((red[0] + red[1]) + (red[2] + red[3])) * ((red[4] + red[5]) + (red[6] + red[7]));
-                        red_add_release(&a.sync->sgu_done, 1u);
+                    if (lane < 2) {
+                        a.h_s[2 * d.job + lane] = silu_f(red[2 * lane] + red[2 * lane + 1]) *
+                                                  (red[4 + 2 * lane] + red[4 + 2 * lane + 1]);
                     }
+                    __syncwarp();
+                    if (lane == 0) red_add_release(&a.sync->sgu_done, 1u);
                 } else if (d.kind == PK_RGU) {
                     if (lane < 16) {
                         const float gs = (red[lane] + red[16 + lane]) + (red[32 + lane] + red[48 + lane]);
@@ -849,8 +935,8 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
                         a.h_r[(size_t)k * kF + 16 * tl + lane] = silu_f(gs) * us;
                     }
                 } else if (d.kind == PK_SDN) {
-                    if (lane < 2) a.p_s[2 * d.job + lane] = red[2 * lane] + red[2 * lane + 1];
-                    tile = (2 * d.job) / 16;
+                    if (lane < 4) a.p_s[4 * d.job + lane] = red[lane];
+                    tile = (4 * d.job) / 16;
                 } else {  // routed down partial of one expert, weighted
                     const int k = d.job / (kH / 16), tl = d.job % (kH / 16);
                     if (lane < 16) {
@@ -860,25 +946,19 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
                     tile = tl;
                 }
                 if (tile >= 0) {
-                    // the last of the tile's 14 jobs sums its partials in a fixed order
+                    // Count this job into its output tile; the last of the tile's 14
+                    // jobs sums the partials.  The counter's old value is examined
+                    // only at this warp's next job end, so its latency is hidden.
+                    finish_tile(a, pend_tile, pend_old, lane);
                     __syncwarp();
-                    uint32_t old = 0;
-                    if (lane == 0) old = atom_add_acq_rel(&a.sync->tile_cnt[tile], 1u);
-                    old = __shfl_sync(0xffffffffu, old, 0);
-                    if (old == kTileParts - 1) {
-                        if (lane < 16) {
-                            const int row = 16 * tile + lane;
-                            float v = __ldcg(a.p_s + row);
-#pragma unroll
-                            for (int k = 0; k < kK; ++k) v += __ldcg(a.p_r + (size_t)k * kH + row);
-                            a.out[row] = v;
-                        }
-                        if (lane == 0) a.sync->tile_cnt[tile] = 0u;
-                    }
+                    pend_old = 0u;
+                    if (lane == 0) pend_old = atom_add_acq_rel(&a.sync->tile_cnt[tile], 1u);
+                    pend_tile = tile;
                 }
             }
             gpar ^= 1;
         }
+        if (wq == 0) finish_tile(a, pend_tile, pend_old, lane);
     }
 
     // ================================================== exit protocol
