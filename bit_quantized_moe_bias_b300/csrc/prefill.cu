@@ -75,16 +75,16 @@ struct PFArgs {
 // ------------------------------------------------------------ shared memory
 struct PFSmem {
     uint8_t *stage;        // kStages x {A0, A1, B}
-    uint4 *sel;            // [256] IQ2 grid row -> 4 prmt selectors
-    uint4 *sgn;            // [128] IQ2 sign index -> 4 sign masks
-    uint2 *q2lut;          // [256] byte of four 2-bit codes -> 2 selectors
+    uint4 *sel;            // [256][8] IQ2 grid row -> 4 prmt selectors (8 replicas: no bank conflicts)
+    uint4 *sgn;            // [128][8] IQ2 sign index -> 4 sign masks
+    uint2 *q2lut;          // [256][16] byte of four 2-bit codes -> 2 selectors (phase 2; aliases sel)
     int *tp;               // [258] task prefix over groups
     uint64_t *full_a, *full_b, *empty, *acc_full, *acc_empty;
     uint32_t *tmem_base;
     int *abort_flag;
 };
 
-constexpr size_t kSmemTables = 256 * 16 + 128 * 16 + 256 * 8 + 1040;
+constexpr size_t kSmemTables = 256 * 8 * 16 + 128 * 8 * 16 + 1040;   // 48 KB of tables + task prefix
 constexpr size_t kSmemBars = (3 * kStages + 4) * 8 + 16;
 constexpr size_t kPFSmemBytes = 1024 + (size_t)kStages * kStageBytes + kSmemTables + kSmemBars;
 
@@ -94,11 +94,10 @@ __device__ __forceinline__ PFSmem carve(uint8_t *raw) {
     s.stage = p;
     p += (size_t)kStages * kStageBytes;
     s.sel = (uint4 *)p;
-    p += 256 * 16;
-    s.sgn = (uint4 *)p;
-    p += 128 * 16;
     s.q2lut = (uint2 *)p;
-    p += 256 * 8;
+    p += 256 * 8 * 16;
+    s.sgn = (uint4 *)p;
+    p += 128 * 8 * 16;
     s.tp = (int *)p;
     p += 1040;
     uint64_t *b = (uint64_t *)p;
@@ -254,6 +253,19 @@ __device__ __forceinline__ void load_block(const PFArgs &a, const uint8_t *mat, 
     }
 }
 
+// Ask L2 to fetch the packed row segment this thread will need two block
+// columns from now (hides HBM latency behind the register double buffer).
+__device__ __forceinline__ void prefetch_block(const PFArgs &a, const uint8_t *mat, int r, int kb, int kh) {
+    const int nbc = a.Kdim / 256;
+    if (kb >= nbc) return;
+    const int rr = r & 15, g8 = rr & 7, hrow = rr >> 3;
+    const uint8_t *p;
+    if (a.qt == DS4G_IQ2_XXS) p = mat + ((size_t)(r >> 4) * nbc + kb) * kTB_IQ2 + 512 * hrow + 64 * g8;
+    else if (a.qt == DS4G_Q2_K) p = mat + ((size_t)(r >> 4) * nbc + kb) * kTB_Q2K + 512 * hrow + 64 * g8 + 32 * kh;
+    else p = mat + ((size_t)(r >> 4) * nbc + kb) * kTB_Q4K + 1024 * hrow + 128 * g8;
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ uint32_t word_of(const BlockRegs &R, int i) {
     const uint4 v = R.q[i >> 2];
     const int k = i & 3;
@@ -262,7 +274,7 @@ __device__ __forceinline__ uint32_t word_of(const BlockRegs &R, int i) {
 
 // IQ2_XXS: 32 weights of sub-block j (record of the row's 64 bytes) -> 4 chunks.
 __device__ __forceinline__ void dq_iq2_record(const PFSmem &sm, const BlockRegs &R, int j, uint8_t *tile, int m,
-                                              int chunk0) {
+                                              int chunk0, int rep8) {
     const int wi = 4 * (j & 3) + 2 * (j >> 2);
     const uint32_t ia = word_of(R, wi), v = word_of(R, wi + 1);
     const float d = f16lo(R.dd);
@@ -271,8 +283,8 @@ __device__ __forceinline__ void dq_iq2_record(const PFSmem &sm, const BlockRegs 
     split4(true, __fmul_rn(db, 8.0f), __fmul_rn(db, 25.0f), __fmul_rn(db, 43.0f), 0.0f, rlo, rhi);
 #pragma unroll
     for (int l = 0; l < 4; ++l) {
-        const uint4 sel = sm.sel[(ia >> (8 * l)) & 255u];
-        const uint4 sg = sm.sgn[(v >> (7 * l)) & 127u];
+        const uint4 sel = sm.sel[8 * ((ia >> (8 * l)) & 255u) + rep8];
+        const uint4 sg = sm.sgn[8 * ((v >> (7 * l)) & 127u) + rep8];
         uint4 o;
         o.x = prmt(rlo, rhi, sel.x) ^ sg.x;
         o.y = prmt(rlo, rhi, sel.y) ^ sg.y;
@@ -285,14 +297,14 @@ __device__ __forceinline__ void dq_iq2_record(const PFSmem &sm, const BlockRegs 
 // Q2_K: 16 weights of one sub-block (word W, scale byte scb) -> 2 chunks in
 // the K-order (0,2,4,...,14,1,3,...,15).
 __device__ __forceinline__ void dq_q2k_sub(const PFSmem &sm, uint32_t W, uint32_t scb, float d, float dmin,
-                                           uint8_t *tile, int m, int chunk0) {
+                                           uint8_t *tile, int m, int chunk0, int rep16) {
     const float dsc = __fmul_rn(d, (float)(scb & 15u));
     const float dm = __fmul_rn(dmin, (float)(scb >> 4));
     uint32_t rlo, rhi;
     split4(false, __fmaf_rn(dsc, 0.0f, -dm), __fmaf_rn(dsc, 1.0f, -dm), __fmaf_rn(dsc, 2.0f, -dm),
            __fmaf_rn(dsc, 3.0f, -dm), rlo, rhi);
-    const uint2 s0 = sm.q2lut[W & 255u], s1 = sm.q2lut[(W >> 8) & 255u];
-    const uint2 s2 = sm.q2lut[(W >> 16) & 255u], s3 = sm.q2lut[W >> 24];
+    const uint2 s0 = sm.q2lut[16 * (W & 255u) + rep16], s1 = sm.q2lut[16 * ((W >> 8) & 255u) + rep16];
+    const uint2 s2 = sm.q2lut[16 * ((W >> 16) & 255u) + rep16], s3 = sm.q2lut[16 * (W >> 24) + rep16];
     sts128(tile, m, chunk0,
            make_uint4(prmt(rlo, rhi, s0.x), prmt(rlo, rhi, s0.y), prmt(rlo, rhi, s1.x), prmt(rlo, rhi, s1.y)));
     sts128(tile, m, chunk0 + 1,
@@ -331,8 +343,9 @@ __device__ __forceinline__ void dq_q4k_sub(bool f16, const BlockRegs &R, int j, 
 
 // ------------------------------------------------------------------ kernel
 __global__ void __launch_bounds__(kPFThreads, 1)
-    prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA0,
-                        const __grid_constant__ CUtensorMap tmA1, PFArgs a) {
+    prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmB16, const __grid_constant__ CUtensorMap tmB32,
+                        const __grid_constant__ CUtensorMap tmB64, const __grid_constant__ CUtensorMap tmB128,
+                        const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1, PFArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const PFSmem sm = carve(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -353,7 +366,10 @@ __global__ void __launch_bounds__(kPFThreads, 1)
         }
         *sm.abort_flag = 0;
         tc::fence_mbar_init();
-        tc::prefetch_tmap(&tmB);
+        tc::prefetch_tmap(&tmB16);
+        tc::prefetch_tmap(&tmB32);
+        tc::prefetch_tmap(&tmB64);
+        tc::prefetch_tmap(&tmB128);
         tc::prefetch_tmap(&tmA0);
         tc::prefetch_tmap(&tmA1);
     }
@@ -379,7 +395,9 @@ __global__ void __launch_bounds__(kPFThreads, 1)
                 sel[wv] = lv[0] | ((lv[0] + 4) << 4) | (lv[1] << 8) | ((lv[1] + 4) << 12);
             }
             if (bad) flag_status(a.status, DS4G_EUNSUPPORTED, 0x6D1Du);
-            sm.sel[i] = make_uint4(sel[0], sel[1], sel[2], sel[3]);
+            const uint4 v4 = make_uint4(sel[0], sel[1], sel[2], sel[3]);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) sm.sel[8 * i + r] = v4;
         }
         for (int i = tid; i < 128; i += kPFThreads) {
             const uint32_t s = (uint32_t)i | ((uint32_t)(__popc(i) & 1) << 7);
@@ -387,7 +405,9 @@ __global__ void __launch_bounds__(kPFThreads, 1)
 #pragma unroll
             for (int wv = 0; wv < 4; ++wv)
                 mk[wv] = (((s >> (2 * wv)) & 1u) << 15) | (((s >> (2 * wv + 1)) & 1u) << 31);
-            sm.sgn[i] = make_uint4(mk[0], mk[1], mk[2], mk[3]);
+            const uint4 v4 = make_uint4(mk[0], mk[1], mk[2], mk[3]);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) sm.sgn[8 * i + r] = v4;
         }
     }
     if (a.phase == 2 && a.qt == DS4G_Q2_K) {
@@ -398,7 +418,9 @@ __global__ void __launch_bounds__(kPFThreads, 1)
                 const uint32_t c0 = (x >> (4 * h)) & 3u, c1 = (x >> (4 * h + 2)) & 3u;
                 sel[h] = c0 | ((c0 + 4) << 4) | (c1 << 8) | ((c1 + 4) << 12);
             }
-            sm.q2lut[x] = make_uint2(sel[0], sel[1]);
+            const uint2 v2 = make_uint2(sel[0], sel[1]);
+#pragma unroll
+            for (int r = 0; r < 16; ++r) sm.q2lut[16 * x + r] = v2;
         }
     }
     // task prefix over the groups (warp 2; 9 groups per lane)
@@ -440,8 +462,10 @@ __global__ void __launch_bounds__(kPFThreads, 1)
             uint32_t it = 0;
             for (int tau = blockIdx.x; tau < ntask && !*abort_flag; tau += gridDim.x) {
                 const PFTask t = decode_task(a, sm.tp, tau);
-                const int nbox = t.npad >> 4;
-                const uint32_t bytes = nbox * 2048u + (t.shared ? (uint32_t)nmat * kTile : 0u);
+                // one box per stage: the smallest of 16/32/64/128 rows covering the chunk
+                const int brows = t.npad <= 16 ? 16 : t.npad <= 32 ? 32 : t.npad <= 64 ? 64 : 128;
+                const CUtensorMap *tmB = brows == 16 ? &tmB16 : brows == 32 ? &tmB32 : brows == 64 ? &tmB64 : &tmB128;
+                const uint32_t bytes = (uint32_t)brows * 128u + (t.shared ? (uint32_t)nmat * kTile : 0u);
                 for (int ks = 0; ks < nkb; ++ks, ++it) {
                     const int s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1u;
@@ -451,8 +475,7 @@ __global__ void __launch_bounds__(kPFThreads, 1)
                     }
                     uint8_t *st = sm.stage + (size_t)s * kStageBytes;
                     tc::mbar_arrive_expect_tx(&sm.full_b[s], bytes);
-                    for (int i = 0; i < nbox; ++i)
-                        tc::tma_load_2d(st + 2 * kTile + i * 2048, &tmB, ks * kBK, t.row0 + 16 * i, &sm.full_b[s]);
+                    tc::tma_load_2d(st + 2 * kTile, tmB, ks * kBK, t.row0, &sm.full_b[s]);
                     if (t.shared) {
                         tc::tma_load_2d(st, &tmA0, ks * kBK, t.mt * kBM, &sm.full_b[s]);
                         if (nmat == 2) tc::tma_load_2d(st + kTile, &tmA1, ks * kBK, t.mt * kBM, &sm.full_b[s]);
@@ -584,7 +607,10 @@ __global__ void __launch_bounds__(kPFThreads, 1)
             for (int kb = 0; kb < nblk && ok; ++kb) {
                 // prefetch the next block column (possibly of the next task)
                 if (kb + 1 < nblk) {
-                    if (!t.shared) load_block(a, mat, r, kb + 1, half, nxt);
+                    if (!t.shared) {
+                        load_block(a, mat, r, kb + 1, half, nxt);
+                        prefetch_block(a, mat, r, kb + 2, half);
+                    }
                 } else if (taun < ntask && !tn.shared) {
                     const uint8_t *matn = (a.phase == 1 && half) ? a.A1[tn.g] : a.A0[tn.g];
                     load_block(a, matn, tn.mt * kBM + m, 0, half, nxt);
@@ -604,8 +630,8 @@ __global__ void __launch_bounds__(kPFThreads, 1)
                         if (a.phase == 1) {
                             uint8_t *tile = st + half * kTile;
                             if (a.qt == DS4G_IQ2_XXS) {
-                                dq_iq2_record(sm, cur, 2 * ks, tile, m, 0);
-                                dq_iq2_record(sm, cur, 2 * ks + 1, tile, m, 4);
+                                dq_iq2_record(sm, cur, 2 * ks, tile, m, 0, lane & 7);
+                                dq_iq2_record(sm, cur, 2 * ks + 1, tile, m, 4, lane & 7);
                             } else {
                                 dq_q4k_sub(true, cur, 2 * ks, cur.q[2 * ((2 * ks) & 3) + ((2 * ks) >> 2)], tile, m, 0);
                                 dq_q4k_sub(true, cur, 2 * ks + 1, cur.q[2 * ((2 * ks + 1) & 3) + ((2 * ks + 1) >> 2)],
@@ -615,8 +641,9 @@ __global__ void __launch_bounds__(kPFThreads, 1)
                             if (a.qt == DS4G_Q2_K) {
                                 const float d = f16lo(cur.dd), dmin = f16hi(cur.dd);
                                 const uint32_t sc0 = cur.s[0] >> (8 * ks), sc1 = cur.s[1] >> (8 * ks);
-                                dq_q2k_sub(sm, word_of(cur, ks), sc0 & 255u, d, dmin, st, m, 4 * half);
-                                dq_q2k_sub(sm, word_of(cur, 4 + ks), sc1 & 255u, d, dmin, st, m, 4 * half + 2);
+                                dq_q2k_sub(sm, word_of(cur, ks), sc0 & 255u, d, dmin, st, m, 4 * half, lane & 15);
+                                dq_q2k_sub(sm, word_of(cur, 4 + ks), sc1 & 255u, d, dmin, st, m, 4 * half + 2,
+                                           lane & 15);
                             } else {
                                 const int j0 = 2 * ks, j1 = 2 * ks + 1;
                                 const uint4 q0 = cur.q[2 * (j0 & 3) + (j0 >> 2)], q1 = cur.q[2 * (j1 & 3) + (j1 >> 2)];
@@ -809,10 +836,10 @@ ds4g_status prefill_forward(const float *hidden, int T, const ds4g_layer *L, con
         if (rc != DS4G_OK) return rc;
         permute_cast_kernel<<<nrow, 256, 0, st>>>(hidden, perm, offsets, T, xb, status);
         if (cudaGetLastError() != cudaSuccess) return DS4G_ECUDA;
-        CUtensorMap mB1, mG, mU;
-        if (!map_bf16(&mB1, xb, nrow, kH, 16) || !map_bf16(&mG, L->sh_gate, kF, kH, kBM) ||
-            !map_bf16(&mU, L->sh_up, kF, kH, kBM))
-            return DS4G_ECUDA;
+        CUtensorMap mB[4], mG, mU;
+        for (int i = 0; i < 4; ++i)
+            if (!map_bf16(&mB[i], xb, nrow, kH, 16u << i)) return DS4G_ECUDA;
+        if (!map_bf16(&mG, L->sh_gate, kF, kH, kBM) || !map_bf16(&mU, L->sh_up, kF, kH, kBM)) return DS4G_ECUDA;
         a.phase = 1;
         a.qt = L->gate_up_type;
         a.hb_q2perm = L->down_type == DS4G_Q2_K ? 1 : 0;
@@ -820,12 +847,14 @@ ds4g_status prefill_forward(const float *hidden, int T, const ds4g_layer *L, con
         a.Kdim = kH;
         a.A0 = reinterpret_cast<const uint8_t *const *>(L->gate);
         a.A1 = reinterpret_cast<const uint8_t *const *>(L->up);
-        prefill_gemm_kernel<<<g_pf_sms, kPFThreads, kPFSmemBytes, st>>>(mB1, mG, mU, a);
+        prefill_gemm_kernel<<<g_pf_sms, kPFThreads, kPFSmemBytes, st>>>(mB[0], mB[1], mB[2], mB[3], mG, mU, a);
         if (cudaGetLastError() != cudaSuccess) return DS4G_ECUDA;
     }
     if (!(phases & 2)) return DS4G_OK;
-    CUtensorMap mB2, mD;
-    if (!map_bf16(&mB2, hb, nrow, kF, 16) || !map_bf16(&mD, L->sh_down, kH, kF, kBM)) return DS4G_ECUDA;
+    CUtensorMap mB2[4], mD;
+    for (int i = 0; i < 4; ++i)
+        if (!map_bf16(&mB2[i], hb, nrow, kF, 16u << i)) return DS4G_ECUDA;
+    if (!map_bf16(&mD, L->sh_down, kH, kF, kBM)) return DS4G_ECUDA;
     a.phase = 2;
     a.qt = L->down_type;
     a.hb_q2perm = 0;
@@ -833,7 +862,7 @@ ds4g_status prefill_forward(const float *hidden, int T, const ds4g_layer *L, con
     a.Kdim = kF;
     a.A0 = reinterpret_cast<const uint8_t *const *>(L->down);
     a.A1 = nullptr;
-    prefill_gemm_kernel<<<g_pf_sms, kPFThreads, kPFSmemBytes, st>>>(mB2, mD, mD, a);
+    prefill_gemm_kernel<<<g_pf_sms, kPFThreads, kPFSmemBytes, st>>>(mB2[0], mB2[1], mB2[2], mB2[3], mD, mD, a);
     if (cudaGetLastError() != cudaSuccess) return DS4G_ECUDA;
     combine_kernel<<<T, 256, 0, st>>>(y, inv, T, out);
     if (cudaGetLastError() != cudaSuccess) return DS4G_ECUDA;
