@@ -3,35 +3,45 @@
 // GPU dispatch, hard-coded graph; §3.2: router -> only the routed experts'
 // weights -> shared expert -> merge).  For T = 1 with IQ2_XXS/Q2_K experts.
 //
-// One persistent CTA per SM, 18 warps: a producer warp, a router warp and
-// four consumer groups of four warps.  Each CTA owns a static list of jobs in
-// five phases — router rows, shared gate/up rows, routed gate/up 16-row tiles,
-// shared down row pairs, routed down (expert, 16-row tile) — phase p's jobs
-// dealt round-robin over the CTAs in alternating direction so per-CTA totals
-// balance, and the CTA's jobs dealt round-robin to its groups.  The producer
-// streams every weight piece (<= 8.5 KB, contiguous) of a group's jobs into
-// the group's four-slot shared-memory ring with cp.async.bulk, so each SM
-// keeps up to twelve pieces (~100 KB) in flight.  A group splits each piece
-// over its four warps, keeps partials in registers until the job's last
-// piece and reduces them in a fixed order behind a four-warp barrier.
+// One persistent CTA per SM, 18 warps: a producer warp, a control warp and
+// four consumer groups of four warps.  The work is cut into jobs of five
+// kinds — router rows, shared gate/up row pairs, shared down 4-row groups,
+// routed gate/up (slot, 16-row tile), routed down (slot, 16-row tile) — each
+// kind dealt round-robin over the CTAs (alternating direction per kind, so
+// per-CTA bytes balance) and over a CTA's four groups.  Producer lane q feeds
+// group q's two-slot shared-memory ring with contiguous bulk copies of about
+// 16 KB (a bulk copy has a fixed cost, so pieces are kept large), choosing
+// the group's next job by readiness: router rows first; routed gate/up as
+// soon as the expert ids are known, alternating with shared gate/up; then
+// routed down of the slots whose h is complete; then shared down once the
+// shared h is complete.  A group splits each piece over its four warps,
+// keeps partials in registers until the job's last piece and reduces them in
+// a fixed order behind a four-warp barrier.
 //
-// Dependencies are exactly those of the method:
-//  - expert ids: every CTA's router warp waits until all 256 router logits
-//    are stored, then computes the top-6 itself (all CTAs get the same ids);
-//    the producer streams routed pieces only after that;
-//  - h: a CTA enters the down phase once every CTA has stored its gate/up h
-//    (one release per CTA); down weights keep streaming meanwhile;
-//  - out: the shared-row jobs and the six routed jobs of a 16-row output tile
-//    store partials; the last of the 14 to finish (a per-tile counter) sums
-//    them in a fixed order.
-// Each CTA waits only for work that running CTAs own, and every wait is
-// bounded (~1 s); a timeout records DS4G_ETIMEOUT.
+// Dependencies are exactly those of the method, tracked by counters in the
+// workspace (release on store, acquire on read):
+//  - expert ids: the control warp of every CTA waits until all 256 router
+//    logits are stored and computes the top-6 itself (the pointer tables of
+//    its 8 experts per lane are already in registers);
+//  - routed h of slot k: complete when its 128 gate/up tiles are stored; each
+//    routed-down piece carries a copy of that h (fp16 hi/lo + 16-column
+//    sums, written by the gate/up jobs) next to its weights, so no CTA-wide
+//    transition is needed;
+//  - shared h: complete when its 1024 row pairs are stored; the control warp
+//    then copies it once into the CTA (over the activation, which every job
+//    that reads it has finished by then);
+//  - out: the four shared-down and six routed-down jobs of a 16-row output
+//    tile store partials; the last of the ten (a per-tile counter) sums them
+//    in a fixed order.
+// Every wait is bounded (~1 s); a timeout records DS4G_ETIMEOUT.
 //
 // Arithmetic: router and shared expert in fp32 FMA (bf16 weights widen
 // exactly); routed experts on mma.sync with exact codes (IQ2 grid value or
 // Q2_K quant as an fp16 subnormal, sign from the sign table) against the
 // activation as an fp16 hi + lo pair; block and sub-block scales applied in
-// fp32 to each 32- or 16-column partial.
+// fp32 to each 32- or 16-column partial.  The IQ2_XXS grid values must lie in
+// {8, 25, 43} (the format's magnitudes): the grid table holds, per row, 8
+// nibble codes that select the value bytes with one byte permute.
 #include "ds4g_internal.cuh"
 #include "tc.cuh"
 
@@ -40,18 +50,22 @@ namespace ds4g {
 constexpr int kNGrp = 4;                         // consumer groups
 constexpr int kGW = 4;                           // warps per group
 constexpr int kD1Cons = kNGrp * kGW;             // 16 consumer warps
-constexpr int kD1Threads = (2 + kD1Cons) * 32;   // producer + router + consumers
-constexpr int kD1Slot = 16896;                   // 16 x 1056: an IQ2 row tile, the largest piece
+constexpr int kD1Threads = (2 + kD1Cons) * 32;   // producer + control + consumers
+constexpr int kRdnW = 8 * kTB_Q2K;               // routed down piece: 16 rows x 2048 (10.5 KB)
+constexpr int kHSlot = 2 * kF * 2 + 128 * 4;     // routed h of one slot: fp16 hi, lo, 16-col sums
+constexpr int kD1Slot = kRdnW + kHSlot;          // 19456 B: the largest piece
+static_assert(kD1Slot >= 16 * kTB_IQ2 && kD1Slot >= 4 * kH && (kD1Slot % 128) == 0, "slot size");
 constexpr int kSlotsPerGrp = 2;                  // one piece in flight while one is computed
-constexpr int kD1Slots = kNGrp * kSlotsPerGrp;   // 16
+constexpr int kD1Slots = kNGrp * kSlotsPerGrp;   // 8
+constexpr int kRep = 16;                         // table replicas: one per lane of a half-warp
+constexpr int kMix = 1;                          // routed gate/up jobs between two shared gate/up jobs
 
-// Jobs per phase, in order, and their pieces (each one contiguous copy of
-// about 16 KB: a bulk copy has a fixed cost, so pieces are kept large):
-//   router rows                       1 piece (16 KB)
-//   shared gate/up row pairs          2 pieces (gate rows, up rows: 16 KB each)
-//   shared down 4-row groups          1 piece (16 KB)
-//   routed gate/up (slot, 16-row tile) 2 pieces (gate, up: 16 tile-blocks each)
-//   routed down (slot, 16-row tile)   1 piece (8 Q2_K tile-blocks, 10.5 KB)
+// Jobs per kind and their pieces:
+//   router rows                         1 piece (16 KB fp32)
+//   shared gate/up row pairs            2 pieces (gate rows, up rows: 16 KB each)
+//   shared down 4-row groups            1 piece (16 KB)
+//   routed gate/up (slot, 16-row tile)  2 pieces (gate, up: 16 tile-blocks each)
+//   routed down (slot, 16-row tile)     1 piece (8 Q2_K tile-blocks + that slot's h)
 constexpr int kNPhase = 5;
 constexpr int kJR = kE;
 constexpr int kJSG = kF / 2;
@@ -69,11 +83,11 @@ struct D1Desc {
 // Global coordination block (in the workspace; zero before the first launch;
 // the last CTA of every launch resets it).
 struct D1Sync {
-    uint32_t router_done;
-    uint32_t sgu_done;     // shared gate/up rows stored
-    uint32_t gu_cta;       // CTAs whose routed gate/up jobs are all stored
+    uint32_t router_done;  // router logits stored
+    uint32_t sgu_done;     // shared gate/up row pairs stored
     uint32_t exit_count;
-    uint32_t pad[12];
+    uint32_t pad0[5];
+    uint32_t rgu_done[8];  // per routed slot: gate/up 16-row tiles stored
     uint32_t tile_cnt[kH / 16];
 };
 
@@ -93,7 +107,7 @@ struct D1Args {
     uint32_t *status;
     D1Sync *sync;
     float *logits;         // [256]
-    float *h_r;            // [6][2048]
+    uint8_t *hr;           // [6][kHSlot]: fp16 h hi [2048], lo [2048], 16-col sums [128] (fp32)
     float *h_s;            // [2048]
     float *p_s;            // [4096] shared-expert output
     float *p_r;            // [6][4096] weighted routed outputs
@@ -103,37 +117,36 @@ struct D1Args {
 // Compile-time offsets from the start of dynamic shared memory.
 constexpr uint32_t kOffRing = 0;
 constexpr uint32_t kOffDesc = kOffRing + kD1Slots * kD1Slot;
-constexpr uint32_t kOffU = kOffDesc + kD1Slots * 16;
-constexpr uint32_t kUnion = 256 * 16 * 8 + 128 * 8 * 8 + kH * 4 + 2 * kH * 2;  // 72 KB (phase B uses 52 KB)
-constexpr uint32_t kOffHs = kOffU + kUnion;      // shared h (fp32), outside the union
-constexpr uint32_t kOffRed = kOffHs + kF * 4;
-constexpr uint32_t kOffZero = kOffRed + kNGrp * 2 * 128 * 4;
-constexpr uint32_t kOffWk = kOffZero + 512;
+constexpr uint32_t kOffGtab = kOffDesc + kD1Slots * 16;
+constexpr uint32_t kOffStab = kOffGtab + 256 * kRep * 4;
+constexpr uint32_t kOffXn = kOffStab + 128 * kRep * 8;   // x fp32; later the shared h (fp32)
+constexpr uint32_t kOffXq = kOffXn + kH * 4;
+constexpr uint32_t kOffRed = kOffXq + 2 * kH * 2;
+constexpr uint32_t kOffWk = kOffRed + kNGrp * 2 * 128 * 4;
 constexpr uint32_t kOffIds = kOffWk + 32;
 constexpr uint32_t kOffEptr = kOffIds + 32;      // 18 expert matrix pointers (gate, up, down x 6)
-constexpr uint32_t kOffCred = kOffEptr + 18 * 8;
+constexpr uint32_t kOffCred = kOffEptr + 160;
 constexpr uint32_t kOffBar = kOffCred + 64;
-constexpr uint32_t kOffFlags = kOffBar + 2 * kD1Slots * 8;
-constexpr size_t kD1SmemBytes = kOffFlags + 16;
+constexpr uint32_t kOffFlags = kOffBar + (2 * kD1Slots + 2) * 8;
+constexpr size_t kD1SmemBytes = kOffFlags + 32;
+static_assert(kD1SmemBytes <= 232448, "shared memory");
+static_assert((kOffXn % 128) == 0 && (kOffEptr % 8) == 0 && (kOffBar % 8) == 0, "alignment");
 
 struct D1Smem {
     uint8_t *ring;
     D1Desc *desc;
-    uint2 *gtab;           // [256][16]   (phase A)
-    uint2 *stab;           // [128][8]
-    float *xn;             // [4096]
-    __half *xq;            // [2][4096] hi, lo
-    __half *hq;            // [6][2][2048] (phase B, aliases phase A)
-    float *xs16;           // [6][128]
-    float *hs;             // [2048] shared h (its own region)
+    uint32_t *gtab;        // [256][kRep] nibble codes of the grid row's 8 values
+    uint2 *stab;           // [128][kRep] sign bytes (bit 7 of each byte) of the 8 values
+    float *xn;             // [4096] normalised activation (router, shared gate/up)
+    float *hs;             // [2048] shared h (same memory as xn, once xn is dead)
+    __half *xq;            // [2][4096] activation hi, lo
     float *red;            // [4 groups][2][128]
-    __half *zero;          // [256] zeros: operand of the inactive mma lanes
     float *wk;             // [6]
     int *ids_s;            // [6]
     const uint8_t **eptr;  // [18] gate[6], up[6], down[6] of the selected experts (NULL if unusable)
     float *cta_red;        // [16]
-    uint64_t *full, *empty;
-    int *flags;            // [0] abort, [1] ids ready, [2] shared h: 0 absent, 1 loading, 2 present
+    uint64_t *full, *empty, *xbar, *hsbar;
+    int *flags;            // [0] abort, [1] ids known, [2] shared h requested, [3] routed slots ready (mask)
 };
 
 extern __shared__ __align__(1024) uint8_t d1_raw[];
@@ -142,21 +155,20 @@ __device__ __forceinline__ D1Smem d1_smem() {
     D1Smem s;
     s.ring = d1_raw + kOffRing;
     s.desc = reinterpret_cast<D1Desc *>(d1_raw + kOffDesc);
-    s.gtab = reinterpret_cast<uint2 *>(d1_raw + kOffU);
-    s.stab = s.gtab + 256 * 16;
-    s.xn = reinterpret_cast<float *>(s.stab + 128 * 8);
-    s.xq = reinterpret_cast<__half *>(s.xn + kH);
-    s.hq = reinterpret_cast<__half *>(d1_raw + kOffU);
-    s.xs16 = reinterpret_cast<float *>(s.hq + kK * 2 * kF);
-    s.hs = reinterpret_cast<float *>(d1_raw + kOffHs);
+    s.gtab = reinterpret_cast<uint32_t *>(d1_raw + kOffGtab);
+    s.stab = reinterpret_cast<uint2 *>(d1_raw + kOffStab);
+    s.xn = reinterpret_cast<float *>(d1_raw + kOffXn);
+    s.hs = s.xn;
+    s.xq = reinterpret_cast<__half *>(d1_raw + kOffXq);
     s.red = reinterpret_cast<float *>(d1_raw + kOffRed);
-    s.zero = reinterpret_cast<__half *>(d1_raw + kOffZero);
     s.wk = reinterpret_cast<float *>(d1_raw + kOffWk);
     s.ids_s = reinterpret_cast<int *>(d1_raw + kOffIds);
     s.eptr = reinterpret_cast<const uint8_t **>(d1_raw + kOffEptr);
     s.cta_red = reinterpret_cast<float *>(d1_raw + kOffCred);
     s.full = reinterpret_cast<uint64_t *>(d1_raw + kOffBar);
     s.empty = s.full + kD1Slots;
+    s.xbar = s.empty + kD1Slots;
+    s.hsbar = s.xbar + 1;
     s.flags = reinterpret_cast<int *>(d1_raw + kOffFlags);
     return s;
 }
@@ -167,6 +179,12 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
                      tc::smem_u32(dst)),
                  "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
                  : "memory");
+}
+
+// Orders this thread's earlier (acquired) view of global memory before its
+// later bulk copies, which read through the async proxy.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
@@ -185,9 +203,6 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v) {
 }
 __device__ __forceinline__ void red_add_release(uint32_t *p, uint32_t v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ void st_release(uint32_t *p, uint32_t v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // Bounded spin until *p >= target.  Returns false on timeout or abort.
@@ -224,6 +239,29 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Warp totals of two per-lane values: lanes 0-15 end with the total of a0,
+// lanes 16-31 with the total of a1.
+__device__ __forceinline__ float warp_sum2(float a0, float a1, int lane) {
+    const bool up = lane & 16;
+    float m = up ? a1 : a0;
+    m += __shfl_xor_sync(0xffffffffu, up ? a0 : a1, 16);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) m += __shfl_xor_sync(0xffffffffu, m, o);
+    return m;
+}
+// Warp totals of four per-lane values: lanes 8r .. 8r+7 end with the total of a_r.
+__device__ __forceinline__ float warp_sum4(float a0, float a1, float a2, float a3, int lane) {
+    const bool up = lane & 16, mid = lane & 8;
+    float k0 = up ? a2 : a0, k1 = up ? a3 : a1;
+    k0 += __shfl_xor_sync(0xffffffffu, up ? a0 : a2, 16);
+    k1 += __shfl_xor_sync(0xffffffffu, up ? a1 : a3, 16);
+    float m = mid ? k1 : k0;
+    m += __shfl_xor_sync(0xffffffffu, mid ? k0 : k1, 8);
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) m += __shfl_xor_sync(0xffffffffu, m, o);
+    return m;
+}
+
 // bf16 x 8 (one uint4) dotted with 8 fp32 values
 __device__ __forceinline__ float dot8_bf16(uint4 wv, const float *xv, float acc) {
     const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
@@ -233,6 +271,27 @@ __device__ __forceinline__ float dot8_bf16(uint4 wv, const float *xv, float acc)
         acc = fmaf(__uint_as_float(wd[i] & 0xffff0000u), xv[2 * i + 1], acc);
     }
     return acc;
+}
+
+// 16-byte shared-memory load by the lanes where `pred` holds; zeros elsewhere
+// (the others issue no access).
+__device__ __forceinline__ uint4 lds128_if(const void *p, bool pred) {
+    uint4 v;
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %5, 0;\n\t"
+        "mov.b32 %0, 0;\n\tmov.b32 %1, 0;\n\tmov.b32 %2, 0;\n\tmov.b32 %3, 0;\n\t"
+        "@q ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n\t}"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "r"(tc::smem_u32(p)), "r"((int)pred)
+        : "memory");
+    return v;
+}
+
+// Order-preserving map of a float key to uint32 (larger key -> larger value).
+__device__ __forceinline__ uint32_t order_key(float f) {
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
 // ------------------------------------------------------ piece consumers
@@ -254,21 +313,25 @@ __device__ __forceinline__ float router_row(const D1Smem &sm, const uint8_t *slo
     return acc0 + acc1;
 }
 
-// 1024 bf16 weights at w (smem) dotted with 1024 fp32 values at v (smem),
-// summed over the warp.
-__device__ __forceinline__ float bf16_dot1024(const __nv_bfloat16 *w, const float *v, int lane) {
-    float acc0 = 0.f, acc1 = 0.f;
+// Rows w and w + ld (bf16, smem) against v (fp32, smem), 8 columns per step
+// at 8 * (lane + 32 i): this lane's partials.  Each v load serves both rows.
+template <int kSteps>
+__device__ __forceinline__ void bf16_rows2(const __nv_bfloat16 *w, int ld, const float *v, int lane, float &s0,
+                                           float &s1) {
+    float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < kSteps; ++i) {
         const int c = 8 * (lane + 32 * i);
-        const uint4 wv = *reinterpret_cast<const uint4 *>(w + c);
+        const uint4 w0 = *reinterpret_cast<const uint4 *>(w + c);
+        const uint4 w1 = *reinterpret_cast<const uint4 *>(w + ld + c);
         float xv[8];
         *reinterpret_cast<float4 *>(xv) = *reinterpret_cast<const float4 *>(v + c);
         *reinterpret_cast<float4 *>(xv + 4) = *reinterpret_cast<const float4 *>(v + c + 4);
-        if (i & 1) acc1 = dot8_bf16(wv, xv, acc1);
-        else acc0 = dot8_bf16(wv, xv, acc0);
+        a0 = dot8_bf16(w0, xv, a0);
+        a1 = dot8_bf16(w1, xv, a1);
     }
-    return warp_sum(acc0 + acc1);
+    s0 = a0;
+    s1 = a1;
 }
 
 __device__ __forceinline__ uint32_t bfe7(uint32_t v, uint32_t pos) {
@@ -277,72 +340,23 @@ __device__ __forceinline__ uint32_t bfe7(uint32_t v, uint32_t pos) {
     return r;
 }
 
-// One IQ2_XXS tile-block (16 rows x 256 cols) at tb, block column b, against
-// the fp16 hi/lo activation: returns (in lanes t == 0) rows g and g+8.
-// Lane (g, t) owns sub-blocks t and t+4 of rows g and g+8; the mma's B
-// operand is block-diagonal (only lanes with g/2 == t feed x, the others read
-// zeros), so each lane receives the sums of its own sub-blocks and applies
-// its own scales.
-__device__ __forceinline__ void iq2_tileblock(const D1Smem &sm, const uint8_t *tb, int b, int lane, float &r0,
-                                              float &r1) {
-    const int g = lane >> 2, t = lane & 3, p = lane & 15;
-    const uint4 qa = *reinterpret_cast<const uint4 *>(tb + 16 * lane);
-    const uint4 qb = *reinterpret_cast<const uint4 *>(tb + 512 + 16 * lane);
-    const uint32_t dd = *reinterpret_cast<const uint32_t *>(tb + 1024 + 4 * g);
-    const float d4g = __half2float(__ushort_as_half((unsigned short)(dd & 0xffffu))) * 4194304.0f;
-    const float d4h = __half2float(__ushort_as_half((unsigned short)(dd >> 16))) * 4194304.0f;
-    const __half *xb = ((g >> 1) == t) ? sm.xq + (g & 1) * kH + 256 * b + 32 * t : sm.zero;
-    const uint2 *gt = sm.gtab + p, *st = sm.stab + (lane & 7);   // entry i at gt[16 i], st[8 i]
-    float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-    for (int jj = 0; jj < 2; ++jj) {
-        uint32_t B[16];
-        const uint4 *src = reinterpret_cast<const uint4 *>(xb + 128 * jj);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const uint4 v = src[q];
-            B[4 * q + 0] = v.x;
-            B[4 * q + 1] = v.y;
-            B[4 * q + 2] = v.z;
-            B[4 * q + 3] = v.w;
-        }
-        const uint32_t ia = jj ? qa.z : qa.x, va = jj ? qa.w : qa.y;
-        const uint32_t ib = jj ? qb.z : qb.x, vb = jj ? qb.w : qb.y;
-        // two independent accumulators so consecutive mma do not wait on each other
-        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int l = 0; l < 4; ++l) {
-            const uint2 ga = gt[16 * __byte_perm(ia, 0, 0x4440 + l)];
-            const uint2 gb = gt[16 * __byte_perm(ib, 0, 0x4440 + l)];
-            const uint2 sa = st[8 * bfe7(va, 7 * l)];
-            const uint2 sbv = st[8 * bfe7(vb, 7 * l)];
-            mma_f16(c0, prmt(ga.x, sa.x, 0x5140), prmt(gb.x, sbv.x, 0x5140), prmt(ga.x, sa.x, 0x7362),
-                    prmt(gb.x, sbv.x, 0x7362), B[4 * l], B[4 * l + 1]);
-            mma_f16(c1, prmt(ga.y, sa.y, 0x5140), prmt(gb.y, sbv.y, 0x5140), prmt(ga.y, sa.y, 0x7362),
-                    prmt(gb.y, sbv.y, 0x7362), B[4 * l + 2], B[4 * l + 3]);
-        }
-        acc0 = fmaf(d4g * half_plus(va >> 28), (c0[0] + c0[1]) + (c1[0] + c1[1]), acc0);
-        acc1 = fmaf(d4h * half_plus(vb >> 28), (c0[2] + c0[3]) + (c1[2] + c1[3]), acc1);
-    }
-    acc0 += __shfl_xor_sync(0xffffffffu, acc0, 1);
-    acc0 += __shfl_xor_sync(0xffffffffu, acc0, 2);
-    acc1 += __shfl_xor_sync(0xffffffffu, acc1, 1);
-    acc1 += __shfl_xor_sync(0xffffffffu, acc1, 2);
-    r0 = acc0;
-    r1 = acc1;
-}
+// Value bytes 8, 25, 43 (codes 0, 1, 2) for the grid's byte permutes.
+constexpr uint32_t kGridVals = 0x002B1908u;
 
 // Two adjacent IQ2_XXS tile-blocks (block columns b0, b0 + 1; 16 rows x 512
 // cols) processed interleaved for instruction-level parallelism; returns the
-// sum of both (in lanes t == 0) for rows g and g+8.  Same arithmetic as
-// iq2_tileblock.
+// sum of both (in lanes t == 0) for rows g and g+8.
+// Lane (g, t) owns sub-blocks t and t+4 of rows g and g+8; the mma's B
+// operand is block-diagonal (only lanes with g/2 == t load x, the others hold
+// zeros), so each lane receives the sums of its own sub-blocks and applies
+// its own scales.
 __device__ __forceinline__ void iq2_tileblock2(const D1Smem &sm, const uint8_t *tb, int b0, int lane, float &r0,
                                                float &r1) {
     const int g = lane >> 2, t = lane & 3, p = lane & 15;
     uint4 qa[2], qb[2];
     float d4g[2], d4h[2];
-    const __half *xb[2];
     const bool act = (g >> 1) == t;
+    const __half *xb = sm.xq + (g & 1) * kH + 256 * b0 + 32 * t;
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
         const uint8_t *tbu = tb + u * kTB_IQ2;
@@ -351,9 +365,9 @@ __device__ __forceinline__ void iq2_tileblock2(const D1Smem &sm, const uint8_t *
         const uint32_t dd = *reinterpret_cast<const uint32_t *>(tbu + 1024 + 4 * g);
         d4g[u] = __half2float(__ushort_as_half((unsigned short)(dd & 0xffffu))) * 4194304.0f;
         d4h[u] = __half2float(__ushort_as_half((unsigned short)(dd >> 16))) * 4194304.0f;
-        xb[u] = act ? sm.xq + (g & 1) * kH + 256 * (b0 + u) + 32 * t : sm.zero;
     }
-    const uint2 *gt = sm.gtab + p, *st = sm.stab + (lane & 7);   // entry i at gt[16 i], st[8 i]
+    const uint32_t *gt = sm.gtab + p;   // entry i at gt[kRep i]
+    const uint2 *st = sm.stab + p;      // entry i at st[kRep i]
     float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
     for (int jj = 0; jj < 2; ++jj) {
@@ -366,17 +380,19 @@ __device__ __forceinline__ void iq2_tileblock2(const D1Smem &sm, const uint8_t *
         for (int l = 0; l < 4; ++l) {
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-                const uint4 B4 = *reinterpret_cast<const uint4 *>(xb[u] + 128 * jj + 8 * l);
+                const uint4 B4 = lds128_if(xb + 256 * u + 128 * jj + 8 * l, act);
                 const uint32_t ia = jj ? qa[u].z : qa[u].x, va = jj ? qa[u].w : qa[u].y;
                 const uint32_t ib = jj ? qb[u].z : qb[u].x, vb = jj ? qb[u].w : qb[u].y;
-                const uint2 ga = gt[16 * __byte_perm(ia, 0, 0x4440 + l)];
-                const uint2 gb = gt[16 * __byte_perm(ib, 0, 0x4440 + l)];
-                const uint2 sa = st[8 * bfe7(va, 7 * l)];
-                const uint2 sbv = st[8 * bfe7(vb, 7 * l)];
-                mma_f16(c0[u], prmt(ga.x, sa.x, 0x5140), prmt(gb.x, sbv.x, 0x5140), prmt(ga.x, sa.x, 0x7362),
-                        prmt(gb.x, sbv.x, 0x7362), B4.x, B4.y);
-                mma_f16(c1[u], prmt(ga.y, sa.y, 0x5140), prmt(gb.y, sbv.y, 0x5140), prmt(ga.y, sa.y, 0x7362),
-                        prmt(gb.y, sbv.y, 0x7362), B4.z, B4.w);
+                const uint32_t ca = gt[kRep * __byte_perm(ia, 0, 0x4440 + l)];
+                const uint32_t cb = gt[kRep * __byte_perm(ib, 0, 0x4440 + l)];
+                const uint2 sa = st[kRep * bfe7(va, 7 * l)];
+                const uint2 sbv = st[kRep * bfe7(vb, 7 * l)];
+                const uint32_t gax = prmt(kGridVals, 0u, ca), gay = prmt(kGridVals, 0u, ca >> 16);
+                const uint32_t gbx = prmt(kGridVals, 0u, cb), gby = prmt(kGridVals, 0u, cb >> 16);
+                mma_f16(c0[u], prmt(gax, sa.x, 0x5140), prmt(gbx, sbv.x, 0x5140), prmt(gax, sa.x, 0x7362),
+                        prmt(gbx, sbv.x, 0x7362), B4.x, B4.y);
+                mma_f16(c1[u], prmt(gay, sa.y, 0x5140), prmt(gby, sbv.y, 0x5140), prmt(gay, sa.y, 0x7362),
+                        prmt(gby, sbv.y, 0x7362), B4.z, B4.w);
             }
         }
 #pragma unroll
@@ -394,19 +410,21 @@ __device__ __forceinline__ void iq2_tileblock2(const D1Smem &sm, const uint8_t *
     r1 = acc1;
 }
 
-// One Q2_K tile-block (16 rows x 256 cols) of expert slot k, block column b,
-// against h of slot k (fp16 hi/lo) and its 16-column sums.  Returns this
-// lane's partial for rows g and g+8 (the quad's four lanes sum to the rows).
-__device__ __forceinline__ void q2k_tileblock(const D1Smem &sm, const uint8_t *tb, int k, int b, int lane,
+// One Q2_K tile-block (16 rows x 256 cols), block column b, against h (fp16
+// hi at hq, lo at hq + 2048) and its 16-column sums xs (permuted: sub-block
+// j16 = 4G + t of block b at (4b + t) * 4 + G).  Returns this lane's partial
+// for rows g and g+8 (the quad's four lanes sum to the rows).
+__device__ __forceinline__ void q2k_tileblock(const uint8_t *tb, const __half *hq, const float *xs, int b, int lane,
                                               float &s0, float &s1) {
     const int g = lane >> 2, t = lane & 3;
+    const bool act = (g >> 1) == t;
     const uint4 qa = *reinterpret_cast<const uint4 *>(tb + 16 * lane);
     const uint4 qb = *reinterpret_cast<const uint4 *>(tb + 512 + 16 * lane);
     const uint32_t sca = *reinterpret_cast<const uint32_t *>(tb + 1024 + 4 * lane);
     const uint32_t scb = *reinterpret_cast<const uint32_t *>(tb + 1152 + 4 * lane);
     const uint2 dd = *reinterpret_cast<const uint2 *>(tb + 1280 + 8 * g);
-    const __half *hrow = ((g >> 1) == t) ? sm.hq + ((size_t)k * 2 + (g & 1)) * kF + 256 * b + 16 * t : sm.zero;
-    const float4 X = *reinterpret_cast<const float4 *>(sm.xs16 + (size_t)k * 128 + (b * 4 + t) * 4);
+    const __half *hrow = hq + (g & 1) * kF + 256 * b + 16 * t;
+    const float4 X = *reinterpret_cast<const float4 *>(xs + (b * 4 + t) * 4);
     const float dg = __half2float(__ushort_as_half((unsigned short)(dd.x & 0xffff))) * 16777216.0f;
     const float mg = __half2float(__ushort_as_half((unsigned short)(dd.x >> 16)));
     const float dh = __half2float(__ushort_as_half((unsigned short)(dd.y & 0xffff))) * 16777216.0f;
@@ -418,10 +436,9 @@ __device__ __forceinline__ void q2k_tileblock(const D1Smem &sm, const uint8_t *t
 #pragma unroll
     for (int G = 0; G < 4; ++G) {
         float c[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
-        uint4 hv[2];
-        hv[0] = *reinterpret_cast<const uint4 *>(hrow + 64 * G);
-        hv[1] = *reinterpret_cast<const uint4 *>(hrow + 64 * G + 8);
-        const uint32_t hb[8] = {hv[0].x, hv[0].y, hv[0].z, hv[0].w, hv[1].x, hv[1].y, hv[1].z, hv[1].w};
+        const uint4 h0 = lds128_if(hrow + 64 * G, act);
+        const uint4 h1 = lds128_if(hrow + 64 * G + 8, act);
+        const uint32_t hb[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)
             mma_f16((cc & 1) ? e : c, (Wa[G] >> (4 * cc)) & 0x00030003u, (Wb[G] >> (4 * cc)) & 0x00030003u,
@@ -435,108 +452,15 @@ __device__ __forceinline__ void q2k_tileblock(const D1Smem &sm, const uint8_t *t
     s1 = sh;
 }
 
-// Top-6 of the 256 router logits (sigmoid scores, bias for selection only,
-// ties to the lower id, weights = selected scores renormalised), one warp.
-// The result goes to this CTA's shared memory; CTA 0 also stores it for the
-// caller.  bias_r: this lane's 8 bias values (experts lane + 32 i).
-__device__ void d1_topk(const D1Args &a, const D1Smem &sm, const float (&bias_r)[8], int lane) {
-    float key[8], s[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) s[i] = __ldcg(a.logits + lane + 32 * i);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        s[i] = 1.0f / (1.0f + expf(-s[i]));
-        key[i] = s[i] + bias_r[i];
-    }
-    int sel_e[kK];
-    float sel_s[kK];
-#pragma unroll
-    for (int k = 0; k < kK; ++k) {
-        float bk = -3.0e38f;
-        int be = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int e = lane + 32 * i;
-            if (key[i] > bk || (key[i] == bk && e < be)) {
-                bk = key[i];
-                be = e;
-            }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float ok = __shfl_xor_sync(0xffffffffu, bk, off);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-            if (ok > bk || (ok == bk && oe < be)) {
-                bk = ok;
-                be = oe;
-            }
-        }
-        const int owner = be & 31, slot = be >> 5;
-        float sv = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            if (i == slot) sv = s[i];
-        sv = __shfl_sync(0xffffffffu, sv, owner);
-        if (lane == owner) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if (i == slot) key[i] = -3.0e38f;
-        }
-        sel_e[k] = be;
-        sel_s[k] = sv;
-    }
-    // the producer streams the selected experts' matrices: cache their
-    // pointers here (one global load per pointer, once per CTA)
-    if (lane < 3 * kK) {
-        const int k = lane % kK, m = lane / kK;
-        int e = 0;
-#pragma unroll
-        for (int kk = 0; kk < kK; ++kk)
-            if (kk == k) e = sel_e[kk];
-        const uint8_t *const *tab = m == 0 ? a.gate : m == 1 ? a.up : a.down;
-        const uint8_t *ptr = tab[e];
-        sm.eptr[lane] = (ptr && !((uintptr_t)ptr & 15)) ? ptr : nullptr;
-    }
-    __syncwarp();
-    if (lane == 0) {
-        float sum = 0.f;
-#pragma unroll
-        for (int k = 0; k < kK; ++k) sum += sel_s[k];
-#pragma unroll
-        for (int k = 0; k < kK; ++k) {
-            const float wv = sel_s[k] / sum;
-            sm.ids_s[k] = sel_e[k];
-            sm.wk[k] = wv;
-            if (blockIdx.x == 0) {
-                a.ids[k] = sel_e[k];
-                a.w[k] = wv;
-            }
-        }
-        __threadfence_block();
-        *reinterpret_cast<volatile int *>(&sm.flags[1]) = 1;
-    }
-}
-
-// Jobs of phase p go to CTA (p even ? j : G-1-j) mod G.
+// ------------------------------------------------------------ job lists
+// Jobs of kind p go to CTA (p even ? j : G-1-j) mod G; a CTA's i-th job of
+// kind p is j = i * G + offset.  Group q takes the CTA's jobs i with
+// (i + rot_p) % 4 == q, rot_p = the CTA's job count of the earlier kinds.
 __device__ __forceinline__ int phase_jobs(int p) {
     return p == 0 ? kJR : p == 1 ? kJSG : p == 2 ? kJSD : p == 3 ? kJRG : kJRD;
 }
 __device__ __forceinline__ int phase_off(int p, int c, int G) { return (p & 1) ? (G - 1 - c) : c; }
 __device__ __forceinline__ int phase_pieces(int p) { return (p == 1 || p == 3) ? 2 : 1; }
-
-// The CTA's i-th job -> (phase, job index); false past the end.
-__device__ __forceinline__ bool cta_job(int i, int c, int G, const int (&cnt)[kNPhase], int &p, int &j) {
-#pragma unroll
-    for (int q = 0; q < kNPhase; ++q) {
-        if (i < cnt[q]) {
-            p = q;
-            j = i * G + phase_off(q, c, G);
-            return true;
-        }
-        i -= cnt[q];
-    }
-    return false;
-}
 
 // If this warp's counted job was the last of its 16-row output tile (the
 // counter returned kTileParts - 1), sum the tile's partials in a fixed order:
@@ -555,6 +479,133 @@ __device__ __forceinline__ void finish_tile(const D1Args &a, int tile, uint32_t 
     if (lane == 0) a.sync->tile_cnt[tile] = 0u;
 }
 
+// ------------------------------------------------------------ control warp
+// Top-6 of the 256 router logits (sigmoid scores, bias for selection only,
+// ties to the lower id, weights = selected scores renormalised), then the
+// readiness of the shared h and of each routed slot's h.
+__device__ __forceinline__ void d1_control(const D1Args &a, const D1Smem &sm, int lane) {
+    volatile int *abort_flag = sm.flags;
+    // lane owns experts 8 lane .. 8 lane + 7: bias and matrix pointers are
+    // loaded now, while the router rows stream
+    float bias8[8];
+    const uint8_t *pg[8], *pu[8], *pd[8];
+    {
+        const float4 b0 = __ldg(reinterpret_cast<const float4 *>(a.bias) + 2 * lane);
+        const float4 b1 = __ldg(reinterpret_cast<const float4 *>(a.bias) + 2 * lane + 1);
+        bias8[0] = b0.x;
+        bias8[1] = b0.y;
+        bias8[2] = b0.z;
+        bias8[3] = b0.w;
+        bias8[4] = b1.x;
+        bias8[5] = b1.y;
+        bias8[6] = b1.z;
+        bias8[7] = b1.w;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            pg[i] = a.gate[8 * lane + i];
+            pu[i] = a.up[8 * lane + i];
+            pd[i] = a.down[8 * lane + i];
+        }
+    }
+    bool ok = true;
+    if (lane == 0) ok = spin_geq(&a.sync->router_done, (uint32_t)kJR, abort_flag);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    __syncwarp();
+    if (!ok) {
+        if (lane == 0) d1_abort(a, sm.flags, 0x31u);
+        return;
+    }
+    float s[8];
+    uint32_t key[8];
+    {
+        const float4 l0 = __ldcg(reinterpret_cast<const float4 *>(a.logits) + 2 * lane);
+        const float4 l1 = __ldcg(reinterpret_cast<const float4 *>(a.logits) + 2 * lane + 1);
+        const float lg[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            s[i] = 1.0f / (1.0f + expf(-lg[i]));
+            key[i] = order_key(s[i] + bias8[i] + 0.0f);   // + 0: -0 -> +0
+        }
+    }
+#pragma unroll 1
+    for (int k = 0; k < kK; ++k) {
+        uint32_t m = key[0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) m = max(m, key[i]);
+        m = __reduce_max_sync(0xffffffffu, m);
+        uint32_t cand = 0xffffffffu;
+#pragma unroll
+        for (int i = 7; i >= 0; --i)
+            if (key[i] == m) cand = 8 * lane + i;
+        const uint32_t e = __reduce_min_sync(0xffffffffu, cand);
+        if (lane == (int)(e >> 3)) {
+            const int i0 = e & 7;
+            float sv = 0.f;
+            const uint8_t *g0 = nullptr, *u0 = nullptr, *d0 = nullptr;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (i == i0) {
+                    sv = s[i];
+                    g0 = pg[i];
+                    u0 = pu[i];
+                    d0 = pd[i];
+                    key[i] = 0u;
+                }
+            const bool usable = g0 && u0 && d0 && !(((uintptr_t)g0 | (uintptr_t)u0 | (uintptr_t)d0) & 15);
+            sm.ids_s[k] = (int)e;
+            sm.wk[k] = sv;
+            sm.eptr[k] = usable ? g0 : nullptr;
+            sm.eptr[kK + k] = usable ? u0 : nullptr;
+            sm.eptr[2 * kK + k] = usable ? d0 : nullptr;
+        }
+    }
+    __syncwarp();
+    if (lane == 0) {
+        float sum = 0.f;
+#pragma unroll
+        for (int k = 0; k < kK; ++k) sum += sm.wk[k];
+#pragma unroll
+        for (int k = 0; k < kK; ++k) {
+            const float wv = sm.wk[k] / sum;
+            sm.wk[k] = wv;
+            if (blockIdx.x == 0) {
+                a.ids[k] = sm.ids_s[k];
+                a.w[k] = wv;
+            }
+        }
+        __threadfence_block();
+        *reinterpret_cast<volatile int *>(&sm.flags[1]) = 1;
+    }
+    // readiness: lane 0 the shared h, lanes 1..6 routed slots 0..5
+    bool pending = lane <= kK;
+    const uint32_t *ctr = lane == 0 ? &a.sync->sgu_done : &a.sync->rgu_done[(lane >= 1 && lane <= kK) ? lane - 1 : 0];
+    const uint32_t target = lane == 0 ? (uint32_t)kJSG : (uint32_t)(kF / 16);
+    const long long t0 = clock64();
+    while (__any_sync(0xffffffffu, pending)) {
+        if (pending && ld_acquire(ctr) >= target) {
+            pending = false;
+            if (lane == 0) {
+                // every job that reads xn has finished: the shared h may overwrite it
+                fence_proxy_async_global();
+                tc::mbar_arrive_expect_tx(sm.hsbar, kF * 4);
+                bulk_load(sm.hs, a.h_s, kF * 4, sm.hsbar);
+                __threadfence_block();
+                *reinterpret_cast<volatile int *>(&sm.flags[2]) = 1;
+            } else {
+                __threadfence_block();
+                atomicOr(&sm.flags[3], 1 << (lane - 1));
+            }
+        }
+        if (*abort_flag) break;
+        if (clock64() - t0 > (2ll << 30)) {
+            if (lane == 0) d1_abort(a, sm.flags, 0x32u);
+            break;
+        }
+        __nanosleep(32);
+    }
+}
+
+// ------------------------------------------------------------ kernel
 __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
     const D1Smem sm = d1_smem();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -565,62 +616,95 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
             tc::mbar_init(&sm.full[i], 1);
             tc::mbar_init(&sm.empty[i], kGW);
         }
-        sm.flags[0] = 0;
-        sm.flags[1] = 0;
-        sm.flags[2] = 0;
+        tc::mbar_init(sm.xbar, 1);
+        tc::mbar_init(sm.hsbar, 1);
+        for (int i = 0; i < 8; ++i) sm.flags[i] = 0;
         tc::fence_mbar_init();
     }
     __syncthreads();
-    int cnt[kNPhase];
-#pragma unroll
-    for (int p = 0; p < kNPhase; ++p) {
-        const int off = phase_off(p, c, G), n = phase_jobs(p);
-        cnt[p] = off < n ? (n - off + G - 1) / G : 0;
-    }
 
     if (warp == 0) {
         // ================================================== producers
         // Lane q feeds group q's ring, so the four rings fill in parallel.
         if (lane < kNGrp) {
             const int q = lane;
-            int gi = q, pcq = 0;
-            uint32_t itq = 0;
-            bool ids_known = false;
+            int cnt[kNPhase], cur[kNPhase], rot = 0;
+#pragma unroll
+            for (int p = 0; p < kNPhase; ++p) {
+                const int off = phase_off(p, c, G), n = phase_jobs(p);
+                cnt[p] = off < n ? (n - off + G - 1) / G : 0;
+                cur[p] = ((q - rot) % kNGrp + kNGrp) % kNGrp;
+                rot += cnt[p];
+            }
+            if (q == 0) {
+                // the activation first: every consumer waits for it
+                tc::mbar_arrive_expect_tx(sm.xbar, kH * 4);
+                bulk_load(sm.xn, a.x, kH * 4, sm.xbar);
+            }
+            uint32_t itq = 0, seen = 0;
+            int pend_p = -1, pend_j = 0, turn = 0;
             long long t_idle = clock64();
             while (true) {
                 if (*abort_flag) break;   // consumers leave on abort; nothing more to feed
                 const int s = kSlotsPerGrp * q + (int)(itq % kSlotsPerGrp);
-                if (!tc::mbar_test_wait(&sm.empty[s], ((itq / kSlotsPerGrp) & 1u) ^ 1u)) {
-                    if (clock64() - t_idle > (2ll << 30)) {
-                        // no slot freed for ~1 s: give up, let the groups finish
-                        d1_abort(a, sm.flags, 0x11u);
-                        break;
+                const bool stalled = !tc::mbar_test_wait(&sm.empty[s], ((itq / kSlotsPerGrp) & 1u) ^ 1u);
+                int p = -1, j = 0, pc = 0;
+                if (!stalled) {
+                    if (pend_p >= 0) {
+                        // second piece of a two-piece job
+                        p = pend_p;
+                        j = pend_j;
+                        pc = 1;
+                    } else {
+                        const int ids = *reinterpret_cast<volatile int *>(&sm.flags[1]);
+                        const int hs_ok = *reinterpret_cast<volatile int *>(&sm.flags[2]);
+                        const uint32_t ready = (uint32_t) * reinterpret_cast<volatile int *>(&sm.flags[3]);
+                        const int k4 = (cur[4] * G + phase_off(4, c, G)) / (kH / 16);
+                        if (cur[0] < cnt[0]) {
+                            p = 0;
+                        } else if (ids && cur[3] < cnt[3] && !(turn >= kMix && cur[1] < cnt[1])) {
+                            p = 3;
+                        } else if (cur[1] < cnt[1]) {
+                            p = 1;
+                        } else if (cur[4] < cnt[4] && ((ready >> k4) & 1u)) {
+                            p = 4;
+                        } else if (cur[2] < cnt[2] && hs_ok) {
+                            p = 2;
+                        } else if (cur[2] >= cnt[2] && cur[3] >= cnt[3] && cur[4] >= cnt[4]) {
+                            p = -2;   // every job issued
+                        }
+                        if (p >= 2) __threadfence_block();   // acquire what the flags publish
+                        if (p == 3) ++turn;
+                        if (p == 1) turn = 0;
+                        if (p == 4 && !((seen >> k4) & 1u)) {
+                            fence_proxy_async_global();
+                            seen |= 1u << k4;
+                        }
+                        if (p >= 0) {
+                            j = cur[p] * G + phase_off(p, c, G);
+                            cur[p] += kNGrp;
+                        }
                     }
-                    continue;
                 }
-                int p, j;
-                if (!cta_job(gi, c, G, cnt, p, j)) {
+                if (p == -2) {
                     sm.desc[s].kind = PK_END;
                     tc::mbar_arrive(&sm.full[s]);
                     break;
                 }
-                if ((p == 3 || p == 4) && !ids_known) {
-                    if (*reinterpret_cast<volatile int *>(&sm.flags[1]) == 0) {   // later
-                        if (clock64() - t_idle > (2ll << 30)) {
-                            d1_abort(a, sm.flags, 0x12u);
-                            break;
-                        }
-                        continue;
+                if (p < 0) {
+                    if (clock64() - t_idle > (2ll << 30)) {
+                        // nothing issued for ~1 s: give up, let the groups finish
+                        d1_abort(a, sm.flags, stalled ? 0x11u : 0x12u);
+                        break;
                     }
-                    ids_known = true;
+                    continue;
                 }
-                const int pc = pcq;
                 uint8_t *dst = sm.ring + (size_t)s * kD1Slot;
                 D1Desc d;
                 d.job = j;
                 d.piece = pc;
                 d.e = 0;
-                const void *src = nullptr;
+                const void *src = nullptr, *src2 = nullptr;
                 uint32_t bytes = 0;
                 if (p == 0) {
                     d.kind = PK_ROUTER;
@@ -639,7 +723,7 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
                     const int k = j / (kF / 16), tile = j % (kF / 16);
                     const uint8_t *mat = sm.eptr[(pc ? kK : 0) + k];
                     d.e = k;
-                    if (mat && sm.eptr[k] && sm.eptr[kK + k]) {
+                    if (mat) {
                         src = mat + (size_t)tile * 16 * kTB_IQ2;
                         bytes = 16 * kTB_IQ2;
                     } else {
@@ -653,7 +737,8 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
                     d.e = k;
                     if (mat) {
                         src = mat + (size_t)tile * 8 * kTB_Q2K;
-                        bytes = 8 * kTB_Q2K;
+                        bytes = kRdnW;
+                        src2 = a.hr + (size_t)k * kHSlot;
                     } else {
                         d.e = -1;
                         flag_status(a.status, DS4G_EDEVICE, (uint32_t)sm.ids_s[k]);
@@ -661,44 +746,43 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
                 }
                 sm.desc[s] = d;
                 if (bytes) {
-                    tc::mbar_arrive_expect_tx(&sm.full[s], bytes);
+                    tc::mbar_arrive_expect_tx(&sm.full[s], bytes + (src2 ? (uint32_t)kHSlot : 0u));
                     bulk_load(dst, src, bytes, &sm.full[s]);
+                    if (src2) bulk_load(dst + kRdnW, src2, kHSlot, &sm.full[s]);
                 } else {
                     tc::mbar_arrive(&sm.full[s]);
                 }
                 ++itq;
-                if (++pcq == phase_pieces(p)) {
-                    pcq = 0;
-                    gi += kNGrp;
-                }
+                pend_p = (phase_pieces(p) == 2 && pc == 0) ? p : -1;
+                pend_j = j;
                 t_idle = clock64();
             }
         }
     } else if (warp == 1) {
-        // ================================================== router warp
-        float bias_r[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) bias_r[i] = __ldg(a.bias + lane + 32 * i);
-        bool ok = true;
-        if (lane == 0) ok = spin_geq(&a.sync->router_done, (uint32_t)kJR, abort_flag);
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (ok) {
-            d1_topk(a, sm, bias_r, lane);
-        } else if (lane == 0) {
-            d1_abort(a, sm.flags, 0x31u);
-        }
+        // ================================================== control warp
+        d1_control(a, sm, lane);
     } else {
         // ================================================== consumers
         const int cw = warp - 2, ct = tid - 64;
         const int q = cw / kGW, wq = cw % kGW;
-        // tables and the normalised activation (all 16 consumer warps); the
-        // global loads are issued first, the tables built while they fly
-        float xv[8], ss = 0.f;
+        // tables (all 16 consumer warps) while the activation streams in
+        if (ct < 256) {
+            const unsigned long long grow = __ldg(reinterpret_cast<const unsigned long long *>(a.grid) + ct);
+            uint32_t sel = 0;
+            bool bad = false;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) xv[i] = __ldg(a.x + ct + 512 * i);
-        const uint64_t grow = ct < 256 ? __ldg(reinterpret_cast<const unsigned long long *>(a.grid) + ct) : 0ull;
-        for (int i = ct; i < 128 * 8; i += kD1Cons * 32) {
-            const uint32_t s7 = (uint32_t)(i >> 3);
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t v = (uint32_t)(grow >> (8 * j)) & 0xffu;
+                const uint32_t code = v == 8u ? 0u : v == 25u ? 1u : v == 43u ? 2u : 3u;
+                bad |= code == 3u;
+                sel |= code << (4 * j);
+            }
+            if (bad) flag_status(a.status, DS4G_EUNSUPPORTED, 0x6A1Du);
+#pragma unroll
+            for (int rep = 0; rep < kRep; ++rep) sm.gtab[ct * kRep + rep] = sel;
+        }
+        for (int i = ct; i < 128 * kRep; i += kD1Cons * 32) {
+            const uint32_t s7 = (uint32_t)(i / kRep);
             const uint32_t sg = s7 | ((uint32_t)(__popc(s7) & 1) << 7);
             uint32_t lo = 0, hi = 0;
 #pragma unroll
@@ -708,12 +792,10 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
             }
             sm.stab[i] = make_uint2(lo, hi);
         }
-        if (ct < 128) reinterpret_cast<uint32_t *>(sm.zero)[ct] = 0u;
-        if (ct < 256) {
-            const uint2 v = make_uint2((uint32_t)grow, (uint32_t)(grow >> 32));
+        if (!d1_wait(sm.xbar, 0, abort_flag)) d1_abort(a, sm.flags, 0x20u);
+        float xv[8], ss = 0.f;
 #pragma unroll
-            for (int rep = 0; rep < 16; ++rep) sm.gtab[ct * 16 + rep] = v;
-        }
+        for (int i = 0; i < 8; ++i) xv[i] = sm.xn[ct + 512 * i];
 #pragma unroll
         for (int i = 0; i < 8; ++i) ss = fmaf(xv[i], xv[i], ss);
         ss = warp_sum(ss);
@@ -736,114 +818,25 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
         asm volatile("bar.sync 1, %0;" ::"n"(kD1Cons * 32));
 
         float rg0 = 0.f, rg1 = 0.f, ru0 = 0.f, ru1 = 0.f; // routed gate/up partials, rows g, g+8
+        float sg0 = 0.f, sg1 = 0.f;                       // shared gate partials, rows 2j, 2j+1
         int pend_tile = -1;                               // tile counted by this warp, not yet examined
         uint32_t pend_old = 0u;
-        bool in_down = false;
+        bool hs_ok = false;
         int gpar = 0;
         for (uint32_t it = 0;; ++it) {
             const int s = kSlotsPerGrp * q + (int)(it % kSlotsPerGrp);
             if (!d1_wait(&sm.full[s], (it / kSlotsPerGrp) & 1u, abort_flag)) {
                 d1_abort(a, sm.flags, 0x21u);
-                // still take part in the CTA transition below so no barrier is left waiting
-                if (!in_down) {
-                    asm volatile("bar.sync 1, %0;" ::"n"(kD1Cons * 32));
-                    asm volatile("bar.sync 1, %0;" ::"n"(kD1Cons * 32));
-                    asm volatile("bar.sync 1, %0;" ::"n"(kD1Cons * 32));
-                }
                 break;
             }
             const D1Desc d = sm.desc[s];
-            if (!in_down && (d.kind == PK_END || d.kind == PK_RDN)) {
-                // This group has no routed gate/up work left.  Once all four groups
-                // are here, publish this CTA's routed h, wait for every CTA's, then
-                // load it (over the gate/up tables, which are no longer needed).
-                asm volatile("bar.sync 1, %0;" ::"n"(kD1Cons * 32));
-                if (ct == 0) {
-                    red_add_release(&a.sync->gu_cta, 1u);
-                    if (!spin_geq(&a.sync->gu_cta, (uint32_t)G, abort_flag)) d1_abort(a, sm.flags, 0x22u);
-                }
-                asm volatile("bar.sync 1, %0;" ::"n"(kD1Cons * 32));
-                {
-                    // h of the six slots: 768 groups of 16 columns; thread ct takes
-                    // groups ct and ct + 512 (all loads issued first)
-                    float4 hv[2][4];
-                    const float4 *h4 = reinterpret_cast<const float4 *>(a.h_r);
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int grp = ct + 512 * u;
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            hv[u][j] = grp < kK * 128 ? __ldcg(h4 + 4 * grp + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int grp = ct + 512 * u;
-                        if (grp >= kK * 128) continue;
-                        const int k = grp >> 7, gl = grp & 127;
-                        const float hf[16] = {hv[u][0].x, hv[u][0].y, hv[u][0].z, hv[u][0].w,
-                                              hv[u][1].x, hv[u][1].y, hv[u][1].z, hv[u][1].w,
-                                              hv[u][2].x, hv[u][2].y, hv[u][2].z, hv[u][2].w,
-                                              hv[u][3].x, hv[u][3].y, hv[u][3].z, hv[u][3].w};
-                        float sum = 0.f;
-                        uint32_t hi2[8], lo2[8];
-#pragma unroll
-                        for (int j = 0; j < 16; j += 2) {
-                            sum += hf[j] + hf[j + 1];
-                            __half h0, l0, h1, l1;
-                            split_f16(hf[j], h0, l0);
-                            split_f16(hf[j + 1], h1, l1);
-                            hi2[j / 2] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
-                            lo2[j / 2] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
-                        }
-                        uint4 *dh = reinterpret_cast<uint4 *>(sm.hq + ((size_t)k * 2) * kF + 16 * gl);
-                        uint4 *dl = reinterpret_cast<uint4 *>(sm.hq + ((size_t)k * 2 + 1) * kF + 16 * gl);
-                        dh[0] = make_uint4(hi2[0], hi2[1], hi2[2], hi2[3]);
-                        dh[1] = make_uint4(hi2[4], hi2[5], hi2[6], hi2[7]);
-                        dl[0] = make_uint4(lo2[0], lo2[1], lo2[2], lo2[3]);
-                        dl[1] = make_uint4(lo2[4], lo2[5], lo2[6], lo2[7]);
-                        const int b = gl >> 4, j16 = gl & 15;
-                        sm.xs16[k * 128 + (b * 4 + (j16 & 3)) * 4 + (j16 >> 2)] = sum;
-                    }
-                }
-                asm volatile("bar.sync 1, %0;" ::"n"(kD1Cons * 32));
-                in_down = true;
-            }
             if (d.kind == PK_END) break;
-            if (d.kind == PK_SDN && *reinterpret_cast<volatile int *>(&sm.flags[2]) != 2) {
-                // first shared-down piece of this CTA: one group waits until every
-                // shared gate/up row is stored and loads shared h; others wait for it
-                int role = 0;
-                if (lane == 0 && wq == 0) role = atomicCAS(&sm.flags[2], 0, 1) == 0 ? 1 : 0;
-                role = __shfl_sync(0xffffffffu, role, 0);
-                role = __shfl_sync(0xffffffffu, role, 0);
-                asm volatile("bar.sync %0, %1;" ::"r"(2 + q), "n"(kGW * 32));
-                // broadcast the group's decision through shared memory
-                if (wq == 0 && lane == 0) sm.cta_red[q] = role ? 1.f : 0.f;
-                asm volatile("bar.sync %0, %1;" ::"r"(2 + q), "n"(kGW * 32));
-                const bool loader = sm.cta_red[q] != 0.f;
-                if (loader) {
-                    if (wq == 0 && lane == 0 && !spin_geq(&a.sync->sgu_done, (uint32_t)kJSG, abort_flag))
-                        d1_abort(a, sm.flags, 0x23u);
-                    asm volatile("bar.sync %0, %1;" ::"r"(2 + q), "n"(kGW * 32));
-                    const int gt = wq * 32 + lane;   // 128 threads x 4 float4
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        reinterpret_cast<float4 *>(sm.hs)[gt + 128 * u] =
-                            __ldcg(reinterpret_cast<const float4 *>(a.h_s) + gt + 128 * u);
-                    __threadfence_block();
-                    asm volatile("bar.sync %0, %1;" ::"r"(2 + q), "n"(kGW * 32));
-                    if (wq == 0 && lane == 0) *reinterpret_cast<volatile int *>(&sm.flags[2]) = 2;
-                } else {
-                    const long long t0 = clock64();
-                    while (*reinterpret_cast<volatile int *>(&sm.flags[2]) != 2 && !*abort_flag) {
-                        if (clock64() - t0 > (2ll << 30)) {
-                            d1_abort(a, sm.flags, 0x24u);
-                            break;
-                        }
-                        __nanosleep(64);
-                    }
-                    __threadfence_block();
+            if (d.kind == PK_SDN && !hs_ok) {
+                if (!d1_wait(sm.hsbar, 0, abort_flag)) {
+                    d1_abort(a, sm.flags, 0x23u);
+                    break;
                 }
+                hs_ok = true;
             }
             const uint8_t *slot = sm.ring + (size_t)s * kD1Slot;
             float *red = sm.red + (q * 2 + gpar) * 128;
@@ -854,12 +847,21 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
                 if (lane == 0) red[wq] = v;
                 last = true;
             } else if (d.kind == PK_SGU) {
-                // piece 0: gate rows 2j, 2j+1; piece 1: up rows; warp wq: row wq>>1, half wq&1
-                const __nv_bfloat16 *w = reinterpret_cast<const __nv_bfloat16 *>(slot) + (wq >> 1) * kH + 2048 * (wq & 1);
-                const float *xv = sm.xn + 2048 * (wq & 1);
-                const float v = bf16_dot1024(w, xv, lane) + bf16_dot1024(w + 1024, xv + 1024, lane);
-                if (lane == 0) red[4 * d.piece + wq] = v;
-                last = d.piece == 1;
+                // gate (piece 0) or up (piece 1) rows 2j, 2j+1; warp wq: columns [1024 wq, +1024)
+                float a0, a1;
+                bf16_rows2<4>(reinterpret_cast<const __nv_bfloat16 *>(slot) + 1024 * wq, kH, sm.xn + 1024 * wq,
+                              lane, a0, a1);
+                if (d.piece == 0) {
+                    sg0 = a0;
+                    sg1 = a1;
+                } else {
+                    const float gsum = warp_sum2(sg0, sg1, lane), usum = warp_sum2(a0, a1, lane);
+                    if ((lane & 15) == 0) {
+                        red[2 * wq + (lane >> 4)] = gsum;
+                        red[8 + 2 * wq + (lane >> 4)] = usum;
+                    }
+                    last = true;
+                }
             } else if (d.kind == PK_RGU) {
                 if (d.piece == 0) rg0 = rg1 = ru0 = ru1 = 0.f;
                 if (d.e >= 0) {
@@ -884,17 +886,23 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
                     last = true;
                 }
             } else if (d.kind == PK_SDN) {
-                // shared down rows 4j .. 4j+3; warp wq: row wq, all 2048 columns
-                const __nv_bfloat16 *w = reinterpret_cast<const __nv_bfloat16 *>(slot) + (size_t)wq * kF;
-                const float v = bf16_dot1024(w, sm.hs, lane) + bf16_dot1024(w + 1024, sm.hs + 1024, lane);
-                if (lane == 0) red[wq] = v;
+                // shared down rows 4j .. 4j+3; warp wq: columns [512 wq, +512) of all four
+                const __nv_bfloat16 *w = reinterpret_cast<const __nv_bfloat16 *>(slot) + 512 * wq;
+                const float *hv = sm.hs + 512 * wq;
+                float a0, a1, a2, a3;
+                bf16_rows2<2>(w, kF, hv, lane, a0, a1);
+                bf16_rows2<2>(w + 2 * kF, kF, hv, lane, a2, a3);
+                const float v = warp_sum4(a0, a1, a2, a3, lane);
+                if ((lane & 7) == 0) red[4 * wq + (lane >> 3)] = v;
                 last = true;
             } else {  // PK_RDN: eight Q2_K tile-blocks of one expert; warp wq: tile-blocks 2wq, 2wq+1
                 float s0 = 0.f, s1 = 0.f;
                 if (d.e >= 0) {
+                    const __half *hq = reinterpret_cast<const __half *>(slot + kRdnW);
+                    const float *xs = reinterpret_cast<const float *>(slot + kRdnW + 4 * kF);
                     float a0, a1, b0, b1;
-                    q2k_tileblock(sm, slot + (size_t)(2 * wq) * kTB_Q2K, d.e, 2 * wq, lane, a0, a1);
-                    q2k_tileblock(sm, slot + (size_t)(2 * wq + 1) * kTB_Q2K, d.e, 2 * wq + 1, lane, b0, b1);
+                    q2k_tileblock(slot + (size_t)(2 * wq) * kTB_Q2K, hq, xs, 2 * wq, lane, a0, a1);
+                    q2k_tileblock(slot + (size_t)(2 * wq + 1) * kTB_Q2K, hq, xs, 2 * wq + 1, lane, b0, b1);
                     s0 = a0 + b0;
                     s1 = a1 + b1;
                 }
@@ -922,20 +930,41 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
                     }
                 } else if (d.kind == PK_SGU) {
                     if (lane < 2) {
-                        a.h_s[2 * d.job + lane] = silu_f(red[2 * lane] + red[2 * lane + 1]) *
-                                                  (red[4 + 2 * lane] + red[4 + 2 * lane + 1]);
+                        const float gs = (red[lane] + red[2 + lane]) + (red[4 + lane] + red[6 + lane]);
+                        const float us = (red[8 + lane] + red[10 + lane]) + (red[12 + lane] + red[14 + lane]);
+                        a.h_s[2 * d.job + lane] = silu_f(gs) * us;
                     }
                     __syncwarp();
                     if (lane == 0) red_add_release(&a.sync->sgu_done, 1u);
                 } else if (d.kind == PK_RGU) {
+                    // h of 16 rows of slot k: fp16 hi/lo and the 16-column sum the
+                    // Q2_K down needs, where the routed-down pieces copy them from
+                    const int k = d.job / (kF / 16), tl = d.job % (kF / 16);
+                    float hv = 0.f;
                     if (lane < 16) {
                         const float gs = (red[lane] + red[16 + lane]) + (red[32 + lane] + red[48 + lane]);
                         const float us = (red[64 + lane] + red[80 + lane]) + (red[96 + lane] + red[112 + lane]);
-                        const int k = d.job / (kF / 16), tl = d.job % (kF / 16);
-                        a.h_r[(size_t)k * kF + 16 * tl + lane] = silu_f(gs) * us;
+                        hv = silu_f(gs) * us;
+                        if (!(fabsf(hv) < 65504.f)) flag_status(a.status, DS4G_EDEVICE, 0xF16u);
+                        __half hi, lo;
+                        split_f16(hv, hi, lo);
+                        __half *hq = reinterpret_cast<__half *>(a.hr + (size_t)k * kHSlot);
+                        hq[16 * tl + lane] = hi;
+                        hq[kF + 16 * tl + lane] = lo;
                     }
+                    float sum = hv;
+#pragma unroll
+                    for (int o = 1; o < 16; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+                    if (lane == 0) {
+                        const int b = tl >> 4, j16 = tl & 15;
+                        float *xs = reinterpret_cast<float *>(a.hr + (size_t)k * kHSlot + 4 * kF);
+                        xs[(b * 4 + (j16 & 3)) * 4 + (j16 >> 2)] = sum;
+                    }
+                    __syncwarp();
+                    if (lane == 0) red_add_release(&a.sync->rgu_done[k], 1u);
                 } else if (d.kind == PK_SDN) {
-                    if (lane < 4) a.p_s[4 * d.job + lane] = red[lane];
+                    if (lane < 4)
+                        a.p_s[4 * d.job + lane] = (red[lane] + red[4 + lane]) + (red[8 + lane] + red[12 + lane]);
                     tile = (4 * d.job) / 16;
                 } else {  // routed down partial of one expert, weighted
                     const int k = d.job / (kH / 16), tl = d.job % (kH / 16);
@@ -946,7 +975,7 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
                     tile = tl;
                 }
                 if (tile >= 0) {
-                    // Count this job into its output tile; the last of the tile's 14
+                    // Count this job into its output tile; the last of the tile's ten
                     // jobs sums the partials.  The counter's old value is examined
                     // only at this warp's next job end, so its latency is hidden.
                     finish_tile(a, pend_tile, pend_old, lane);
@@ -970,7 +999,7 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
             // every CTA has finished: reset the coordination block for the next launch
             a.sync->router_done = 0;
             a.sync->sgu_done = 0;
-            a.sync->gu_cta = 0;
+            for (int k = 0; k < 8; ++k) a.sync->rgu_done[k] = 0;
             for (int t = 0; t < kH / 16; ++t) a.sync->tile_cnt[t] = 0;   // already zero unless a launch gave up
             __threadfence();
             a.sync->exit_count = 0;
@@ -980,7 +1009,7 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
 
 // ------------------------------------------------------------------ host
 struct D1Layout {
-    size_t sync, logits, h_r, h_s, p_s, p_r, total;
+    size_t sync, logits, hr, h_s, p_s, p_r, total;
 };
 static D1Layout d1_layout() {
     D1Layout L;
@@ -989,8 +1018,8 @@ static D1Layout d1_layout() {
     off += align_up(sizeof(D1Sync), 256);
     L.logits = off;
     off += align_up(kE * 4, 256);
-    L.h_r = off;
-    off += align_up((size_t)kK * kF * 4, 256);
+    L.hr = off;
+    off += align_up((size_t)kK * kHSlot, 256);
     L.h_s = off;
     off += align_up((size_t)kF * 4, 256);
     L.p_s = off;
@@ -1054,7 +1083,7 @@ extern "C" ds4g_status ds4g_moe_layer_decode(const float *hidden, int normalize,
     a.status = (uint32_t *)ws;
     a.sync = (D1Sync *)(ws + lay.sync);
     a.logits = (float *)(ws + lay.logits);
-    a.h_r = (float *)(ws + lay.h_r);
+    a.hr = ws + lay.hr;
     a.h_s = (float *)(ws + lay.h_s);
     a.p_s = (float *)(ws + lay.p_s);
     a.p_r = (float *)(ws + lay.p_r);

@@ -76,3 +76,37 @@ def check_route(ids_gpu, w_gpu, ids_ref, w_ref, keys, margin):
             assert np.all(keys[t][ids_gpu[t]] >= kth - ROUTE_MARGIN)
         assert abs(float(w_gpu[t].sum()) - 1.0) <= 1e-5
     return near
+
+
+class FullLayer:
+    """All 256 experts of one layer, generated and packed on the device with
+    the seeded generator's CUDA twin (host bytes regenerated on demand)."""
+
+    def __init__(self, seed, cfg, layer, gut=synth.IQ2_XXS, dt=synth.Q2_K, device="cuda"):
+        import torch
+        import bit_quantized_moe_bias_b300 as B
+        self.seed, self.cfg, self.lay, self.gut, self.dt = seed, cfg, layer, gut, dt
+        sizes = {gut: B.ds4g_packed_size(gut, F, H), dt: B.ds4g_packed_size(dt, H, F)}
+        tmp = torch.empty(max(sizes.values()), dtype=torch.uint8, device=device)
+        mats = {}
+        st = torch.cuda.current_stream().cuda_stream
+        for kind, qt, rows, cols in ((synth.KIND_GATE, gut, F, H), (synth.KIND_UP, gut, F, H),
+                                     (synth.KIND_DOWN, dt, H, F)):
+            t = torch.empty(E, sizes[qt], dtype=torch.uint8, device=device)
+            for e in range(E):
+                synth.gguf_matrix_device(qt, rows, cols, seed, synth.stream_id(cfg, layer, kind, e), tmp.data_ptr(), st)
+                B.ds4g_quantize_pack_device(qt, rows, cols, tmp, t[e])
+            mats[kind] = t
+        self.shared = synth.shared(seed, cfg, layer)
+        sh = [torch.from_numpy(a.view(np.int16)).to(device) for a in self.shared]
+        self.grid, g64 = grid_u64(seed)
+        gridt = torch.from_numpy(g64.view(np.int64)).to(device)
+        self.L = B.MoELayer(mats[synth.KIND_GATE], mats[synth.KIND_UP], mats[synth.KIND_DOWN], *sh, gridt, gut, dt)
+        torch.cuda.synchronize()
+
+    def oracle(self, x, ids, w):
+        import oracle
+        gate, up, down = [None] * E, [None] * E, [None] * E
+        for e in sorted(set(int(v) for v in ids.reshape(-1))):
+            gate[e], up[e], down[e] = synth.expert(self.seed, self.cfg, self.lay, e, self.gut, self.dt)
+        return oracle.moe_forward(x, ids, w, gate, up, down, *self.shared, self.grid, self.gut, self.dt)

@@ -10,7 +10,7 @@ import pytest
 
 import oracle
 import synth
-from helpers import E, F, H, K, grid_u64
+from helpers import H, K, FullLayer
 
 torch = pytest.importorskip("torch")
 import bit_quantized_moe_bias_b300 as B  # noqa: E402
@@ -18,37 +18,6 @@ import bit_quantized_moe_bias_b300 as B  # noqa: E402
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 REL_L2 = 1e-2
-
-
-class FullLayer:
-    """All 256 experts of one layer, generated and packed on the device with
-    the seeded generator's CUDA twin (host bytes regenerated on demand)."""
-
-    def __init__(self, seed, cfg, layer, gut=synth.IQ2_XXS, dt=synth.Q2_K):
-        self.seed, self.cfg, self.lay, self.gut, self.dt = seed, cfg, layer, gut, dt
-        sizes = {gut: B.ds4g_packed_size(gut, F, H), dt: B.ds4g_packed_size(dt, H, F)}
-        tmp = torch.empty(max(sizes.values()), dtype=torch.uint8, device=DEV)
-        mats = {}
-        st = torch.cuda.current_stream().cuda_stream
-        for kind, qt, rows, cols in ((synth.KIND_GATE, gut, F, H), (synth.KIND_UP, gut, F, H),
-                                     (synth.KIND_DOWN, dt, H, F)):
-            t = torch.empty(E, sizes[qt], dtype=torch.uint8, device=DEV)
-            for e in range(E):
-                synth.gguf_matrix_device(qt, rows, cols, seed, synth.stream_id(cfg, layer, kind, e), tmp.data_ptr(), st)
-                B.ds4g_quantize_pack_device(qt, rows, cols, tmp, t[e])
-            mats[kind] = t
-        self.shared = synth.shared(seed, cfg, layer)
-        sh = [torch.from_numpy(a.view(np.int16)).to(DEV) for a in self.shared]
-        self.grid, g64 = grid_u64(seed)
-        gridt = torch.from_numpy(g64.view(np.int64)).to(DEV)
-        self.L = B.MoELayer(mats[synth.KIND_GATE], mats[synth.KIND_UP], mats[synth.KIND_DOWN], *sh, gridt, gut, dt)
-        torch.cuda.synchronize()
-
-    def oracle(self, x, ids, w):
-        gate, up, down = [None] * E, [None] * E, [None] * E
-        for e in sorted(set(int(v) for v in ids.reshape(-1))):
-            gate[e], up[e], down[e] = synth.expert(self.seed, self.cfg, self.lay, e, self.gut, self.dt)
-        return oracle.moe_forward(x, ids, w, gate, up, down, *self.shared, self.grid, self.gut, self.dt)
 
 
 @pytest.fixture(scope="module")
