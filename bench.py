@@ -159,12 +159,22 @@ def run_ours(args, rank, world, local_rank):
     rws = B.workspace(B.ds4g_route_workspace(1), dev)
     fws = B.workspace(B.ds4g_forward_workspace(1), dev)
     lws = B.workspace(B.ds4g_layer_decode_workspace(), dev)
-    fused = args.decode_path == "fused"
+    fused = args.decode_path in ("fused", "layer")
+    stacked = args.decode_path == "fused"
     launches_per_step = ntok * nl * (1 if fused else 4)
+    stack = B.DecodeStack([(L.struct, R, b) for L, R, b in layers])
+    ids_all = torch.empty(nl, K, dtype=torch.int32, device=dev)
+    w_all = torch.empty(nl, K, dtype=torch.float32, device=dev)
+    hbuf = torch.empty(2, H, device=dev)
 
     def step(timing=None):
         for i in range(ntok):
             cur = x_dev[i:i + 1]
+            if stacked:
+                # one call per token: 43 layer launches, each after the first a
+                # programmatic dependent of the one before
+                B.ds4g_moe_decode_stack(cur, stack, ids_all, w_all, hbuf, out_all[i], lws)
+                continue
             for l, (L, R, b) in enumerate(layers):
                 dst = out_all[i:i + 1] if l == nl - 1 else act[l & 1]
                 if fused:
@@ -273,7 +283,7 @@ def run_ours(args, rank, world, local_rank):
                    "l2": "no flush: 80 GB of weights streamed per step >> 126 MB L2",
                    "weight_gb_per_token": round(nl * LAYER_BYTES / 1e9, 4),
                    "achieved_hbm_gbs_block": round(value / world * nl * LAYER_BYTES / 1e9, 1),
-                   "setup_s": round(setup_s, 1)},
+                   "decode_path": args.decode_path, "setup_s": round(setup_s, 1)},
         "e2e": {"value": round(tokens / e2e_s, 3), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(x_host.numel() * 4), "d2h_bytes_per_step": int(y_host.numel() * 4)},
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1),
@@ -500,8 +510,9 @@ def main():
     ap.add_argument("--workload", choices=["decode", "prefill"], default="decode",
                     help="decode = 43-layer full-depth decode (headline); prefill = T=2048 chunk, one layer")
     ap.add_argument("--cpu-tokens", type=int, default=8, help="prefill CPU-baseline sample size")
-    ap.add_argument("--decode-path", choices=["fused", "split"], default="fused",
-                    help="fused = one launch per layer; split = rmsnorm, route, gate/up, down launches")
+    ap.add_argument("--decode-path", choices=["fused", "layer", "split"], default="fused",
+                    help="fused = one stack call per token (one launch per layer, programmatic dependent "
+                         "launches); layer = one call per layer; split = rmsnorm, route, gate/up, down launches")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -68,6 +68,8 @@ def lib():
             "ds4g_moe_down": (fwd, i),
             "ds4g_layer_decode_workspace": ([], sz),
             "ds4g_moe_layer_decode": ([vp, i, vp, vp, C.POINTER(ds4g_layer), vp, vp, vp, vp, sz, vp], i),
+            "ds4g_moe_decode_stack": ([vp, i, C.POINTER(vp), C.POINTER(vp), C.POINTER(ds4g_layer), vp, vp, vp, vp,
+                                       vp, sz, vp], i),
             "ds4g_moe_forward_noalloc": ([vp, i, C.POINTER(ds4g_layer), vp, vp, vp, vp], i),
             "ds4g_rmsnorm": ([vp, i, vp, vp], i),
             "ds4g_last_error": ([vp, vp], i),
@@ -204,6 +206,28 @@ def ds4g_moe_layer_decode(hidden, router, bias, layer: ds4g_layer, ids, w, out, 
     _check("ds4g_moe_layer_decode",
            lib().ds4g_moe_layer_decode(_ptr(hidden), 1 if normalize else 0, _ptr(router), _ptr(bias), C.byref(layer),
                                        _ptr(ids), _ptr(w), _ptr(out), _ptr(workspace), workspace.numel(),
+                                       _stream(stream)))
+
+
+class DecodeStack:
+    """Marshalled arguments of ds4g_moe_decode_stack for a fixed list of
+    layers: (ds4g_layer struct, router tensor, bias tensor) per layer."""
+
+    def __init__(self, layers):
+        n = len(layers)
+        self.n = n
+        self.structs = (ds4g_layer * n)(*[l[0] for l in layers])
+        self.routers = (C.c_void_p * n)(*[_ptr(l[1]) for l in layers])
+        self.biases = (C.c_void_p * n)(*[_ptr(l[2]) for l in layers])
+        self.keep = layers
+
+
+def ds4g_moe_decode_stack(hidden, stack: DecodeStack, ids, w, hbuf, out, workspace, stream=None):
+    """One token through stack.n chained layers (programmatic dependent
+    launches between them); ids, w: [n][6]; hbuf: [2][4096] scratch."""
+    _check("ds4g_moe_decode_stack",
+           lib().ds4g_moe_decode_stack(_ptr(hidden), stack.n, stack.routers, stack.biases, stack.structs, _ptr(ids),
+                                       _ptr(w), _ptr(hbuf), _ptr(out), _ptr(workspace), workspace.numel(),
                                        _stream(stream)))
 
 

@@ -35,6 +35,12 @@
 //    in a fixed order.
 // Every wait is bounded (~1 s); a timeout records DS4G_ETIMEOUT.
 //
+// Chained layers (ds4g_moe_decode_stack) launch each layer after the first as
+// a programmatic dependent of the previous one: its CTAs take the SMs that
+// the previous layer's CTAs leave, build their tables and start streaming
+// router and shared-expert pieces, and touch the input and the workspace
+// only after griddepcontrol.wait (the previous layer complete and visible).
+//
 // Arithmetic: router and shared expert in fp32 FMA (bf16 weights widen
 // exactly); routed experts on mma.sync with exact codes (IQ2 grid value or
 // Q2_K quant as an fp16 subnormal, sign from the sign table) against the
@@ -94,6 +100,7 @@ struct D1Sync {
 struct D1Args {
     const float *x;
     int normalize;
+    int pdl;
     const float *router;   // [256][4096]
     const float *bias;     // [256]
     int32_t *ids;          // [6] out
@@ -507,6 +514,11 @@ __device__ __forceinline__ void d1_control(const D1Args &a, const D1Smem &sm, in
             pd[i] = a.down[8 * lane + i];
         }
     }
+    if (a.pdl) asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (lane == 0) {
+        tc::mbar_arrive_expect_tx(sm.xbar, kH * 4);
+        bulk_load(sm.xn, a.x, kH * 4, sm.xbar);
+    }
     bool ok = true;
     if (lane == 0) ok = spin_geq(&a.sync->router_done, (uint32_t)kJR, abort_flag);
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -611,6 +623,7 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, c = blockIdx.x;
     volatile int *abort_flag = sm.flags;
+    if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (tid == 0) {
         for (int i = 0; i < kD1Slots; ++i) {
             tc::mbar_init(&sm.full[i], 1);
@@ -635,11 +648,6 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
                 cnt[p] = off < n ? (n - off + G - 1) / G : 0;
                 cur[p] = ((q - rot) % kNGrp + kNGrp) % kNGrp;
                 rot += cnt[p];
-            }
-            if (q == 0) {
-                // the activation first: every consumer waits for it
-                tc::mbar_arrive_expect_tx(sm.xbar, kH * 4);
-                bulk_load(sm.xn, a.x, kH * 4, sm.xbar);
             }
             uint32_t itq = 0, seen = 0;
             int pend_p = -1, pend_j = 0, turn = 0;
@@ -766,6 +774,7 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
         const int cw = warp - 2, ct = tid - 64;
         const int q = cw / kGW, wq = cw % kGW;
         // tables (all 16 consumer warps) while the activation streams in
+        bool gbad = false;
         if (ct < 256) {
             const unsigned long long grow = __ldg(reinterpret_cast<const unsigned long long *>(a.grid) + ct);
             uint32_t sel = 0;
@@ -777,9 +786,9 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
                 bad |= code == 3u;
                 sel |= code << (4 * j);
             }
-            if (bad) flag_status(a.status, DS4G_EUNSUPPORTED, 0x6A1Du);
 #pragma unroll
             for (int rep = 0; rep < kRep; ++rep) sm.gtab[ct * kRep + rep] = sel;
+            gbad = bad;
         }
         for (int i = ct; i < 128 * kRep; i += kD1Cons * 32) {
             const uint32_t s7 = (uint32_t)(i / kRep);
@@ -792,6 +801,8 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
             }
             sm.stab[i] = make_uint2(lo, hi);
         }
+        if (a.pdl) asm volatile("griddepcontrol.wait;" ::: "memory");
+        if (gbad) flag_status(a.status, DS4G_EUNSUPPORTED, 0x6A1Du);
         if (!d1_wait(sm.xbar, 0, abort_flag)) d1_abort(a, sm.flags, 0x20u);
         float xv[8], ss = 0.f;
 #pragma unroll
@@ -1033,26 +1044,25 @@ static D1Layout d1_layout() {
 static int g_d1_sms = 0;
 static bool g_d1_attr = false;
 
-}  // namespace ds4g
-
-using namespace ds4g;
-
-extern "C" size_t ds4g_layer_decode_workspace(void) { return d1_layout().total; }
-
-extern "C" ds4g_status ds4g_moe_layer_decode(const float *hidden, int normalize, const float *router,
-                                             const float *bias, const ds4g_layer *L, int32_t *ids, float *w,
-                                             float *out, void *workspace, size_t ws_bytes, ds4g_stream_t s) {
+// Host checks shared by the single-layer and the stacked entry points.
+static ds4g_status d1_check(const float *hidden, const float *router, const float *bias, const ds4g_layer *L,
+                            const int32_t *ids, const float *w, const float *out, const void *workspace,
+                            size_t ws_bytes) {
     if (!hidden || !router || !bias || !L || !ids || !w || !out || !workspace) return DS4G_EINVAL;
     if (!L->gate || !L->up || !L->down || !L->sh_gate || !L->sh_up || !L->sh_down) return DS4G_EINVAL;
     if (L->gate_up_type != DS4G_IQ2_XXS || L->down_type != DS4G_Q2_K) return DS4G_EUNSUPPORTED;
     if (!L->iq2_grid) return DS4G_EINVAL;
-    const uintptr_t al = (uintptr_t)hidden | (uintptr_t)router | (uintptr_t)bias | (uintptr_t)ids |
-                         (uintptr_t)w | (uintptr_t)out | (uintptr_t)workspace | (uintptr_t)L->gate |
-                         (uintptr_t)L->up | (uintptr_t)L->down | (uintptr_t)L->sh_gate | (uintptr_t)L->sh_up |
-                         (uintptr_t)L->sh_down | (uintptr_t)L->iq2_grid;
-    if (al & 15) return DS4G_EALIGN;
-    const D1Layout lay = d1_layout();
-    if (ws_bytes < lay.total) return DS4G_ENOSPACE;
+    // ids and w are written element by element: 4-byte alignment suffices (a
+    // stack's per-layer rows of 6 are not 16-byte aligned)
+    const uintptr_t al = (uintptr_t)hidden | (uintptr_t)router | (uintptr_t)bias | (uintptr_t)out |
+                         (uintptr_t)workspace | (uintptr_t)L->gate | (uintptr_t)L->up | (uintptr_t)L->down |
+                         (uintptr_t)L->sh_gate | (uintptr_t)L->sh_up | (uintptr_t)L->sh_down | (uintptr_t)L->iq2_grid;
+    if ((al & 15) || (((uintptr_t)ids | (uintptr_t)w) & 3)) return DS4G_EALIGN;
+    if (ws_bytes < d1_layout().total) return DS4G_ENOSPACE;
+    return DS4G_OK;
+}
+
+static ds4g_status d1_setup() {
     if (!g_d1_sms) {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess) return DS4G_ECUDA;
@@ -1064,10 +1074,17 @@ extern "C" ds4g_status ds4g_moe_layer_decode(const float *hidden, int normalize,
             return DS4G_ECUDA;
         g_d1_attr = true;
     }
+    return DS4G_OK;
+}
+
+static D1Args d1_args(const float *hidden, int normalize, const float *router, const float *bias,
+                      const ds4g_layer *L, int32_t *ids, float *w, float *out, void *workspace) {
+    const D1Layout lay = d1_layout();
     uint8_t *ws = (uint8_t *)workspace;
     D1Args a;
     a.x = hidden;
     a.normalize = normalize ? 1 : 0;
+    a.pdl = 0;
     a.router = router;
     a.bias = bias;
     a.ids = ids;
@@ -1087,6 +1104,62 @@ extern "C" ds4g_status ds4g_moe_layer_decode(const float *hidden, int normalize,
     a.h_s = (float *)(ws + lay.h_s);
     a.p_s = (float *)(ws + lay.p_s);
     a.p_r = (float *)(ws + lay.p_r);
-    decode_t1_kernel<<<g_d1_sms, kD1Threads, kD1SmemBytes, (cudaStream_t)s>>>(a);
-    return cudaGetLastError() == cudaSuccess ? DS4G_OK : DS4G_ECUDA;
+    return a;
+}
+
+// pdl: launch as a programmatic dependent of the previous kernel on s (which
+// must be this kernel: its CTAs may start before that kernel has finished).
+static ds4g_status d1_launch(const D1Args &a, cudaStream_t s, bool pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)g_d1_sms);
+    cfg.blockDim = dim3(kD1Threads);
+    cfg.dynamicSmemBytes = kD1SmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    D1Args b = a;
+    b.pdl = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, decode_t1_kernel, b) == cudaSuccess ? DS4G_OK : DS4G_ECUDA;
+}
+
+}  // namespace ds4g
+
+using namespace ds4g;
+
+extern "C" size_t ds4g_layer_decode_workspace(void) { return d1_layout().total; }
+
+extern "C" ds4g_status ds4g_moe_layer_decode(const float *hidden, int normalize, const float *router,
+                                             const float *bias, const ds4g_layer *L, int32_t *ids, float *w,
+                                             float *out, void *workspace, size_t ws_bytes, ds4g_stream_t s) {
+    ds4g_status st = d1_check(hidden, router, bias, L, ids, w, out, workspace, ws_bytes);
+    if (st != DS4G_OK) return st;
+    if (((uintptr_t)ids | (uintptr_t)w) & 15) return DS4G_EALIGN;
+    if ((st = d1_setup()) != DS4G_OK) return st;
+    return d1_launch(d1_args(hidden, normalize, router, bias, L, ids, w, out, workspace), (cudaStream_t)s, false);
+}
+
+extern "C" ds4g_status ds4g_moe_decode_stack(const float *hidden, int n_layers, const float *const *routers,
+                                             const float *const *biases, const ds4g_layer *layers, int32_t *ids,
+                                             float *w, float *hbuf, float *out, void *workspace, size_t ws_bytes,
+                                             ds4g_stream_t s) {
+    if (n_layers < 1 || n_layers > 1024 || !routers || !biases || !layers || !hbuf || !ids || !w) return DS4G_EINVAL;
+    if (((uintptr_t)hbuf | (uintptr_t)ids | (uintptr_t)w) & 15) return DS4G_EALIGN;
+    for (int l = 0; l < n_layers; ++l) {
+        const ds4g_status st = d1_check(hidden, routers[l], biases[l], &layers[l], ids + kK * l, w + kK * l, out,
+                                        workspace, ws_bytes);
+        if (st != DS4G_OK) return st;
+    }
+    ds4g_status st = d1_setup();
+    if (st != DS4G_OK) return st;
+    for (int l = 0; l < n_layers; ++l) {
+        const float *x = l == 0 ? hidden : hbuf + (size_t)((l - 1) & 1) * kH;
+        float *o = l == n_layers - 1 ? out : hbuf + (size_t)(l & 1) * kH;
+        st = d1_launch(d1_args(x, 1, routers[l], biases[l], &layers[l], ids + kK * l, w + kK * l, o, workspace),
+                       (cudaStream_t)s, l > 0);
+        if (st != DS4G_OK) return st;
+    }
+    return DS4G_OK;
 }

@@ -243,14 +243,44 @@ ds4g_status ds4g_moe_down(const float *hidden, int T, const ds4g_layer *L,
  * expert is summed in fp32 FMA.  workspace dev >= ds4g_layer_decode_workspace()
  * bytes, zeroed once before first use (the kernel leaves its counters at
  * zero); one call at a time per workspace.  Kernel-detected faults (bad
- * expert id, |xn| >= 65504, a bounded wait that expired) are read back with
- * ds4g_last_error(workspace).
+ * expert id, |xn| or |h| >= 65504, a bounded wait that expired) are read
+ * back with ds4g_last_error(workspace); so is an IQ2_XXS grid byte outside
+ * {8, 25, 43}, the format's magnitudes (DS4G_EUNSUPPORTED: this kernel
+ * encodes grid rows as 2-bit codes of those values).
+ * The kernel keeps one CTA on every SM and its CTAs wait on each other
+ * (bounded), so it needs the whole GPU: run nothing else concurrently.
  * ------------------------------------------------------------------------ */
 size_t ds4g_layer_decode_workspace(void);
 ds4g_status ds4g_moe_layer_decode(const float *hidden, int normalize, const float *router,
                                   const float *bias, const ds4g_layer *L, int32_t *ids,
                                   float *w, float *out, void *workspace, size_t ws_bytes,
                                   ds4g_stream_t s);
+
+/* ------------------------------------------------------------------------
+ * One decode token through n_layers chained MoE layers: layer l is
+ * ds4g_moe_layer_decode with normalize = 1 on the input
+ *   x_0 = hidden,  x_l = output of layer l-1  (l >= 1),
+ * i.e. every layer's input is RMS-normalised in the kernel and no residual
+ * is added (the full-depth decode workload of 43 such layers).
+ *   hidden   [4096] f32 dev            routers  host array [n_layers] of dev
+ *   layers   host array [n_layers]       pointers to [256][4096] f32
+ *   biases   host array [n_layers] of dev pointers to [256] f32
+ *   ids      [n_layers][6] int32 dev (out)   w  [n_layers][6] f32 dev (out)
+ *   hbuf     [2][4096] f32 dev: scratch for the intermediate outputs
+ *   out      [4096] f32 dev: the last layer's output
+ *   workspace as for ds4g_moe_layer_decode (one workspace serves all layers).
+ * 1 <= n_layers <= 1024, else DS4G_EINVAL.  All checks of every layer run
+ * before the first launch.  Same results, bit for bit, as n_layers calls of
+ * ds4g_moe_layer_decode.  Each launch after the first uses programmatic
+ * dependent launch: its CTAs start on the SMs that the previous layer's CTAs
+ * leave, build their tables and begin streaming the layer's router and
+ * shared-expert weights, and read their input and the workspace only after
+ * the previous layer has completed.
+ * ------------------------------------------------------------------------ */
+ds4g_status ds4g_moe_decode_stack(const float *hidden, int n_layers, const float *const *routers,
+                                  const float *const *biases, const ds4g_layer *layers,
+                                  int32_t *ids, float *w, float *hbuf, float *out,
+                                  void *workspace, size_t ws_bytes, ds4g_stream_t s);
 
 /* ------------------------------------------------------------------------
  * ds4g_moe_forward without a workspace, for callers that cannot allocate

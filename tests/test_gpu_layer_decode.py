@@ -77,3 +77,71 @@ def test_layer_decode_flags_missing_expert():
     ids, w, out, st = _run(x[0], R, b, L2, ws, normalize=False)
     assert st == 0
     assert_close_fwd(out[None], oracle_forward(x, ids[None], w[None], hx, shared, grid))
+
+
+def test_decode_stack_equals_layer_calls_and_oracle():
+    """Three chained layers through ds4g_moe_decode_stack (programmatic
+    dependent launches) equal three ds4g_moe_layer_decode calls bit for bit,
+    and follow the oracle's chain (rmsnorm between layers, no residual)."""
+    NL, seed = 3, 5
+    x = synth.hidden(seed, 1, 1, layer=11, normalise=False)
+    h = oracle.rmsnorm(x)
+    refs, layers = [], []
+    for l in range(NL):
+        R, b = synth.router(seed, 1, l), synth.bias_normal(seed, 1, l)
+        ids_r, w_r, keys, margin = oracle.route(h, R, b)
+        assert margin[0] > 1e-4     # the seed keeps every layer clear of near-ties
+        L, hx, shared, grid = device_layer(seed, 1, l, ids_r.reshape(-1))
+        out_r = oracle_forward(h, ids_r, w_r, hx, shared, grid)
+        refs.append((ids_r, w_r, keys, margin, out_r))
+        layers.append((L, _t(R), _t(b)))
+        h = oracle.rmsnorm(out_r)
+    stack = B.DecodeStack([(L.struct, R, b) for L, R, b in layers])
+    ids = torch.full((NL, K), -1, dtype=torch.int32, device=DEV)
+    w = torch.zeros(NL, K, dtype=torch.float32, device=DEV)
+    hbuf = torch.zeros(2, H, dtype=torch.float32, device=DEV)
+    out = torch.full((H,), float("nan"), dtype=torch.float32, device=DEV)
+    ws = B.workspace(B.ds4g_layer_decode_workspace())
+    xd = _t(x[0])
+    for _ in range(2):                               # the workspace is reusable call after call
+        B.ds4g_moe_decode_stack(xd, stack, ids, w, hbuf, out, ws)
+        assert B.ds4g_last_error(ws) == 0
+    ids_s, w_s, out_s = ids.cpu().numpy(), w.cpu().numpy(), out.cpu().numpy()
+    for l in range(NL):
+        ids_r, w_r, keys, margin, _ = refs[l]
+        check_route(ids_s[l][None], w_s[l][None], ids_r, w_r, keys, margin)
+    assert_close_fwd(out_s[None], refs[-1][4])
+    # the same layers one call at a time
+    xl = xd
+    for l, (L, R, b) in enumerate(layers):
+        i1 = torch.full((K,), -1, dtype=torch.int32, device=DEV)
+        w1 = torch.zeros(K, dtype=torch.float32, device=DEV)
+        o1 = torch.empty(H, dtype=torch.float32, device=DEV)
+        B.ds4g_moe_layer_decode(xl, R, b, L.struct, i1, w1, o1, ws)
+        assert np.array_equal(i1.cpu().numpy(), ids_s[l]) and np.array_equal(w1.cpu().numpy(), w_s[l])
+        xl = o1
+    assert np.array_equal(xl.cpu().numpy(), out_s)
+    assert B.ds4g_last_error(ws) == 0
+
+
+def test_decode_stack_rejects_bad_arguments():
+    L, _, _, _ = device_layer(0, 1, 0, range(6))
+    R, b = _t(synth.router(0, 1)), _t(synth.bias_normal(0, 1))
+    stack = B.DecodeStack([(L.struct, R, b)])
+    x = torch.zeros(H, device=DEV)
+    ids = torch.zeros(1, K, dtype=torch.int32, device=DEV)
+    w = torch.zeros(1, K, device=DEV)
+    hbuf = torch.zeros(2, H, device=DEV)
+    out = torch.zeros(H, device=DEV)
+    small = B.workspace(1024)
+    with pytest.raises(B.DS4GError) as e:
+        B.ds4g_moe_decode_stack(x, stack, ids, w, hbuf, out, small)
+    assert e.value.code == 3
+    ws = B.workspace(B.ds4g_layer_decode_workspace())
+    with pytest.raises(B.DS4GError) as e:
+        B.ds4g_moe_decode_stack(x, stack, ids, w, hbuf[0, 1:], out, ws)   # misaligned scratch
+    assert e.value.code == 2
+    stack.n = 0
+    with pytest.raises(B.DS4GError) as e:
+        B.ds4g_moe_decode_stack(x, stack, ids, w, hbuf, out, ws)
+    assert e.value.code == 1
