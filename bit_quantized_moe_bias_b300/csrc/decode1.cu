@@ -135,7 +135,8 @@ constexpr uint32_t kOffEptr = kOffIds + 32;      // 18 expert matrix pointers (g
 constexpr uint32_t kOffCred = kOffEptr + 160;
 constexpr uint32_t kOffBar = kOffCred + 64;
 constexpr uint32_t kOffFlags = kOffBar + (2 * kD1Slots + 2) * 8;
-constexpr size_t kD1SmemBytes = kOffFlags + 32;
+constexpr uint32_t kOffJc = kOffFlags + 32;      // per kind: the CTA's next unclaimed job
+constexpr size_t kD1SmemBytes = kOffJc + 32;
 static_assert(kD1SmemBytes <= 232448, "shared memory");
 static_assert((kOffXn % 128) == 0 && (kOffEptr % 8) == 0 && (kOffBar % 8) == 0, "alignment");
 
@@ -154,6 +155,7 @@ struct D1Smem {
     float *cta_red;        // [16]
     uint64_t *full, *empty, *xbar, *hsbar;
     int *flags;            // [0] abort, [1] ids known, [2] shared h requested, [3] routed slots ready (mask)
+    int *jc;               // [5] per job kind: the CTA's next unclaimed local job index
 };
 
 extern __shared__ __align__(1024) uint8_t d1_raw[];
@@ -177,6 +179,7 @@ __device__ __forceinline__ D1Smem d1_smem() {
     s.xbar = s.empty + kD1Slots;
     s.hsbar = s.xbar + 1;
     s.flags = reinterpret_cast<int *>(d1_raw + kOffFlags);
+    s.jc = reinterpret_cast<int *>(d1_raw + kOffJc);
     return s;
 }
 
@@ -632,6 +635,7 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
         tc::mbar_init(sm.xbar, 1);
         tc::mbar_init(sm.hsbar, 1);
         for (int i = 0; i < 8; ++i) sm.flags[i] = 0;
+        for (int i = 0; i < 8; ++i) sm.jc[i] = 0;
         tc::fence_mbar_init();
     }
     __syncthreads();
@@ -639,18 +643,21 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
     if (warp == 0) {
         // ================================================== producers
         // Lane q feeds group q's ring, so the four rings fill in parallel.
+        // The lanes claim the CTA's jobs of each kind from shared cursors, so
+        // a group that finishes early takes more (a routed gate/up job is
+        // several microseconds of one group's time).
         if (lane < kNGrp) {
             const int q = lane;
-            int cnt[kNPhase], cur[kNPhase], rot = 0;
+            int cnt[kNPhase];
 #pragma unroll
             for (int p = 0; p < kNPhase; ++p) {
                 const int off = phase_off(p, c, G), n = phase_jobs(p);
                 cnt[p] = off < n ? (n - off + G - 1) / G : 0;
-                cur[p] = ((q - rot) % kNGrp + kNGrp) % kNGrp;
-                rot += cnt[p];
             }
+            volatile int *jc = sm.jc;
             uint32_t itq = 0, seen = 0;
             int pend_p = -1, pend_j = 0, turn = 0;
+            int held = -1;   // a claimed routed-down job whose slot's h is not complete yet
             long long t_idle = clock64();
             while (true) {
                 if (*abort_flag) break;   // consumers leave on abort; nothing more to feed
@@ -667,30 +674,52 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
                         const int ids = *reinterpret_cast<volatile int *>(&sm.flags[1]);
                         const int hs_ok = *reinterpret_cast<volatile int *>(&sm.flags[2]);
                         const uint32_t ready = (uint32_t) * reinterpret_cast<volatile int *>(&sm.flags[3]);
-                        const int k4 = (cur[4] * G + phase_off(4, c, G)) / (kH / 16);
-                        if (cur[0] < cnt[0]) {
-                            p = 0;
-                        } else if (ids && cur[3] < cnt[3] && !(turn >= kMix && cur[1] < cnt[1])) {
-                            p = 3;
-                        } else if (cur[1] < cnt[1]) {
-                            p = 1;
-                        } else if (cur[4] < cnt[4] && ((ready >> k4) & 1u)) {
-                            p = 4;
-                        } else if (cur[2] < cnt[2] && hs_ok) {
-                            p = 2;
-                        } else if (cur[2] >= cnt[2] && cur[3] >= cnt[3] && cur[4] >= cnt[4]) {
-                            p = -2;   // every job issued
+                        const int off4 = phase_off(4, c, G);
+                        int want = -1;
+                        if (held >= 0) {
+                            if ((ready >> (held / (kH / 16))) & 1u) {
+                                p = 4;
+                                j = held;
+                                held = -1;
+                            }
+                        }
+                        if (p < 0) {
+                            const bool a0 = jc[0] < cnt[0], a1 = jc[1] < cnt[1], a2 = jc[2] < cnt[2];
+                            const bool a3 = jc[3] < cnt[3], a4 = jc[4] < cnt[4];
+                            if (a0) {
+                                want = 0;
+                            } else if (ids && a3 && !(turn >= kMix && a1)) {
+                                want = 3;
+                            } else if (a1) {
+                                want = 1;
+                            } else if (held < 0 && a4 && ((ready >> ((jc[4] * G + off4) / (kH / 16))) & 1u)) {
+                                want = 4;
+                            } else if (a2 && hs_ok) {
+                                want = 2;
+                            } else if (!a2 && !a3 && !a4 && held < 0) {
+                                p = -2;   // every job of this CTA claimed and issued
+                            }
+                            if (want >= 0) {
+                                const int i = atomicAdd(&sm.jc[want], 1);
+                                if (i < cnt[want]) {
+                                    j = i * G + phase_off(want, c, G);
+                                    p = want;
+                                    if (p == 4 && !((ready >> (j / (kH / 16))) & 1u)) {
+                                        held = j;   // another lane took the ready one first
+                                        p = -1;
+                                    }
+                                }
+                            }
                         }
                         if (p >= 2) __threadfence_block();   // acquire what the flags publish
                         if (p == 3) ++turn;
                         if (p == 1) turn = 0;
-                        if (p == 4 && !((seen >> k4) & 1u)) {
-                            fence_proxy_async_global();
-                            seen |= 1u << k4;
-                        }
-                        if (p >= 0) {
-                            j = cur[p] * G + phase_off(p, c, G);
-                            cur[p] += kNGrp;
+                        if (p == 4) {
+                            const int k4 = j / (kH / 16);
+                            if (!((seen >> k4) & 1u)) {
+                                fence_proxy_async_global();
+                                seen |= 1u << k4;
+                            }
                         }
                     }
                 }
