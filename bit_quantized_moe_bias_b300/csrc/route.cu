@@ -138,41 +138,78 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteArgs a) {
     if (threadIdx.x == 0) *a.cnt = 0u;
 }
 
-// grid (ceil(T/32), 4), block 256: fp32 tile 32 tokens x 64 experts.
-__global__ void __launch_bounds__(256) route_tiled_kernel(RouteArgs a) {
-    __shared__ float xs[kTileT][kTileK + 1];
-    __shared__ float rs[kTileE][kTileK + 1];
+// grid (ceil(T/32), 4), block 128: fp32 tile 32 tokens x 64 experts; thread
+// (ty, tx) accumulates tokens 4ty..4ty+3 x experts 4tx..4tx+3 (16 FMA per
+// two 16-byte shared loads).  Tiles are stored k-major; the next K chunk is
+// loaded into registers while the current one is multiplied.  The last of the
+// four expert tiles of a token tile runs the top-6 of its 32 tokens.
+constexpr int kRouteTiledThreads = 128;
+__global__ void __launch_bounds__(kRouteTiledThreads) route_tiled_kernel(RouteArgs a) {
+    __shared__ __align__(16) float xs[2][kTileK][kTileT];
+    __shared__ __align__(16) float rs[2][kTileK][kTileE];
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
     const int t0 = blockIdx.x * kTileT, e0 = blockIdx.y * kTileE;
-    float acc[2][4] = {};
+    // global -> register staging: x tile 32 x 32 (2 float4 per thread), R tile 64 x 32 (4)
+    float4 xr[2], rr[4];
+    auto load = [&](int k0) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int i = tid + kRouteTiledThreads * u, tt = i >> 3, kq = i & 7;
+            xr[u] = (t0 + tt < a.T) ? __ldg(reinterpret_cast<const float4 *>(a.x + (size_t)(t0 + tt) * kH + k0) + kq)
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = tid + kRouteTiledThreads * u, ee = i >> 3, kq = i & 7;
+            rr[u] = __ldg(reinterpret_cast<const float4 *>(a.R + (size_t)(e0 + ee) * kH + k0) + kq);
+        }
+    };
+    auto store = [&](int buf) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int i = tid + kRouteTiledThreads * u, tt = i >> 3, k = 4 * (i & 7);
+            xs[buf][k][tt] = xr[u].x;
+            xs[buf][k + 1][tt] = xr[u].y;
+            xs[buf][k + 2][tt] = xr[u].z;
+            xs[buf][k + 3][tt] = xr[u].w;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = tid + kRouteTiledThreads * u, ee = i >> 3, k = 4 * (i & 7);
+            rs[buf][k][ee] = rr[u].x;
+            rs[buf][k + 1][ee] = rr[u].y;
+            rs[buf][k + 2][ee] = rr[u].z;
+            rs[buf][k + 3][ee] = rr[u].w;
+        }
+    };
+    float acc[4][4] = {};
+    load(0);
+    store(0);
+    __syncthreads();
+    int buf = 0;
     for (int k0 = 0; k0 < kH; k0 += kTileK) {
-        for (int i = tid; i < kTileT * kTileK; i += 256) {
-            const int tt = i / kTileK, kk = i % kTileK;
-            xs[tt][kk] = (t0 + tt < a.T) ? a.x[(size_t)(t0 + tt) * kH + k0 + kk] : 0.f;
-        }
-        for (int i = tid; i < kTileE * kTileK; i += 256) {
-            const int ee = i / kTileK, kk = i % kTileK;
-            rs[ee][kk] = a.R[(size_t)(e0 + ee) * kH + k0 + kk];
-        }
-        __syncthreads();
+        const bool more = k0 + kTileK < kH;
+        if (more) load(k0 + kTileK);
 #pragma unroll 8
         for (int kk = 0; kk < kTileK; ++kk) {
-            const float x0 = xs[ty][kk], x1 = xs[ty + 16][kk];
+            const float4 xv = *reinterpret_cast<const float4 *>(&xs[buf][kk][4 * ty]);
+            const float4 rv = *reinterpret_cast<const float4 *>(&rs[buf][kk][4 * tx]);
+            const float xa[4] = {xv.x, xv.y, xv.z, xv.w}, ra[4] = {rv.x, rv.y, rv.z, rv.w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float rv = rs[tx + 16 * j][kk];
-                acc[0][j] = fmaf(x0, rv, acc[0][j]);
-                acc[1][j] = fmaf(x1, rv, acc[1][j]);
-            }
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(xa[i], ra[j], acc[i][j]);
         }
+        if (more) store(buf ^ 1);
         __syncthreads();
+        buf ^= 1;
     }
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int t = t0 + ty + 16 * i;
+    for (int i = 0; i < 4; ++i) {
+        const int t = t0 + 4 * ty + i;
         if (t < a.T)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) a.part[(size_t)t * kE + e0 + tx + 16 * j] = acc[i][j];
+            *reinterpret_cast<float4 *>(a.part + (size_t)t * kE + e0 + 4 * tx) =
+                make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
     }
     __threadfence();
     __shared__ uint32_t last;
@@ -184,9 +221,10 @@ __global__ void __launch_bounds__(256) route_tiled_kernel(RouteArgs a) {
     __syncthreads();
     if (!last) return;
     __threadfence();
-    __shared__ float lg[8][kE];
+    constexpr int kW = kRouteTiledThreads / 32;
+    __shared__ float lg[kW][kE];
     const int warp = tid >> 5, lane = tid & 31;
-    for (int tt = warp; tt < kTileT; tt += 8) {
+    for (int tt = warp; tt < kTileT; tt += kW) {
         const int t = t0 + tt;
         if (t >= a.T) break;
         for (int i = lane; i < kE; i += 32) lg[warp][i] = __ldcg(a.part + (size_t)t * kE + i);
@@ -235,7 +273,7 @@ extern "C" ds4g_status ds4g_moe_route(const float *hidden, int T, const float *r
     if (T <= kRouteSmallT) {
         route_small_kernel<<<dim3(kE / 8, kRouteKS), 256, 0, st>>>(a);
     } else {
-        route_tiled_kernel<<<dim3((unsigned)ntile, kE / kTileE), 256, 0, st>>>(a);
+        route_tiled_kernel<<<dim3((unsigned)ntile, kE / kTileE), kRouteTiledThreads, 0, st>>>(a);
     }
     return cudaGetLastError() == cudaSuccess ? DS4G_OK : DS4G_ECUDA;
 }
