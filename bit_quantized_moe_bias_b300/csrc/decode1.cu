@@ -8,13 +8,14 @@
 // kinds — router rows, shared gate/up row pairs, shared down 4-row groups,
 // routed gate/up (slot, 16-row tile), routed down (slot, 16-row tile) — each
 // kind dealt round-robin over the CTAs (alternating direction per kind, so
-// per-CTA bytes balance) and over a CTA's four groups.  Producer lane q feeds
-// group q's two-slot shared-memory ring with contiguous bulk copies of about
-// 16 KB (a bulk copy has a fixed cost, so pieces are kept large), choosing
-// the group's next job by readiness: router rows first; routed gate/up as
-// soon as the expert ids are known, alternating with shared gate/up; then
-// routed down of the slots whose h is complete; then shared down once the
-// shared h is complete.  A group splits each piece over its four warps,
+// per-CTA bytes balance).  Producer lane q feeds group q's two-slot
+// shared-memory ring with contiguous bulk copies of about 16 KB (a bulk copy
+// has a fixed cost, so pieces are kept large); the four lanes claim the
+// CTA's jobs of each kind from shared cursors, so a group that finishes early
+// takes more, and each picks its next job by readiness: router rows first;
+// routed gate/up as soon as the expert ids are known, alternating with shared
+// gate/up; then routed down of the slots whose h is complete; then shared
+// down once the shared h is complete.  A group splits each piece over its four warps,
 // keeps partials in registers until the job's last piece and reduces them in
 // a fixed order behind a four-warp barrier.
 //
