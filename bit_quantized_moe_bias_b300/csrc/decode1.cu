@@ -446,18 +446,28 @@ __device__ __forceinline__ void q2k_tileblock(const uint8_t *tb, const __half *h
     float sg = 0.f, sh = 0.f;
 #pragma unroll
     for (int G = 0; G < 4; ++G) {
-        float c[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
+        // Quant slot s (columns 4(s>>1) + 2(s&1) + {0,1}) sits at bits 2s and
+        // 16 + 2s of the word, slot s + 4 eight bits higher: a mask leaves it
+        // in place as the exact subnormal q * 4^s * 2^-24, so mma s takes slots
+        // s and s + 4 of both rows with one AND each, and its accumulator is
+        // scaled back by 4^-s.
         const uint4 h0 = lds128_if(hrow + 64 * G, act);
         const uint4 h1 = lds128_if(hrow + 64 * G + 8, act);
         const uint32_t hb[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+        const uint32_t wa = Wa[G], wb = Wb[G], wa8 = Wa[G] >> 8, wb8 = Wb[G] >> 8;
+        float r[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-            mma_f16((cc & 1) ? e : c, (Wa[G] >> (4 * cc)) & 0x00030003u, (Wb[G] >> (4 * cc)) & 0x00030003u,
-                    (Wa[G] >> (4 * cc + 2)) & 0x00030003u, (Wb[G] >> (4 * cc + 2)) & 0x00030003u, hb[2 * cc],
-                    hb[2 * cc + 1]);
+        for (int sl = 0; sl < 4; ++sl) {
+            const uint32_t m = 0x00030003u << (2 * sl);
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_f16(c, wa & m, wb & m, wa8 & m, wb8 & m, hb[sl], hb[sl + 4]);
+            const float f = 1.0f / (float)(1 << (2 * sl));
+#pragma unroll
+            for (int i = 0; i < 4; ++i) r[i] = fmaf(c[i], f, r[i]);
+        }
         const uint32_t ba = (sca >> (8 * G)) & 0xffu, bb = (scb >> (8 * G)) & 0xffu;
-        sg += dg * small_u2f(ba & 15u) * ((c[0] + c[1]) + (e[0] + e[1])) - mg * small_u2f(ba >> 4) * Xg[G];
-        sh += dh * small_u2f(bb & 15u) * ((c[2] + c[3]) + (e[2] + e[3])) - mh * small_u2f(bb >> 4) * Xg[G];
+        sg += dg * small_u2f(ba & 15u) * (r[0] + r[1]) - mg * small_u2f(ba >> 4) * Xg[G];
+        sh += dh * small_u2f(bb & 15u) * (r[2] + r[3]) - mh * small_u2f(bb >> 4) * Xg[G];
     }
     s0 = sg;
     s1 = sh;
