@@ -137,6 +137,18 @@ def build_model(dev, nlayer, cfg=CFG):
     return layers
 
 
+def max_over_ranks(times, world, dev):
+    """Element-wise maximum of per-rank timings: the slowest replica sets the
+    step time of the whole job (replicas only; no data-path collective)."""
+    if world <= 1:
+        return list(times)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(times, device=dev, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import bit_quantized_moe_bias_b300 as B
@@ -259,13 +271,7 @@ def run_ours(args, rank, world, local_rank):
     if st:
         raise RuntimeError(f"device status {st} after the timed region")
 
-    times = [dev_s, e2e_s]
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor(times, device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        times = t.tolist()
-    dev_s, e2e_s = times
+    dev_s, e2e_s = max_over_ranks([dev_s, e2e_s], world, dev)
     if rank != 0:
         return None
     tokens = ntok * args.steps * world
@@ -373,13 +379,7 @@ def run_prefill(args, rank, world, local_rank):
     st = B.ds4g_last_error(rws) or B.ds4g_last_error(fws)
     if st:
         raise RuntimeError(f"device status {st} after the timed region")
-    times = [dev_s, e2e_s]
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor(times, device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        times = t.tolist()
-    dev_s, e2e_s = times
+    dev_s, e2e_s = max_over_ranks([dev_s, e2e_s], world, dev)
     if rank != 0:
         return None
     tokens = T * args.steps * world

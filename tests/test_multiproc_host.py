@@ -1,0 +1,60 @@
+"""Host logic of the N > 1 bench path on CPU: world-size-2 ranks over the
+gloo backend (the path shards into independent replicas, so its only
+collective is the max-over-ranks timing), and the reference arm's rule that
+only rank 0 prints."""
+import contextlib
+import io
+import os
+import socket
+import sys
+
+import pytest
+
+torch = pytest.importorskip("torch")
+import torch.distributed as dist  # noqa: E402
+import torch.multiprocessing as mp  # noqa: E402
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+    try:
+        # rank r measured (1 + r) s on the device and (5 - r) s end to end
+        got = bench.max_over_ranks([1.0 + rank, 5.0 - rank], world, "cpu")
+        out[rank] = got
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world2():
+    world = 2
+    port = _free_port()
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.start_processes(_rank_main, args=(world, port, out), nprocs=world, join=True, start_method="spawn")
+        res = dict(out)
+    assert res[0] == [2.0, 5.0] and res[1] == [2.0, 5.0]
+
+
+def test_max_over_ranks_single_rank_is_identity():
+    assert bench.max_over_ranks([0.25, 0.5], 1, "cpu") == [0.25, 0.5]
+
+
+def test_reference_arm_prints_only_on_rank0(monkeypatch):
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("LOCAL_RANK", "1")
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference", "--steps", "1", "--warmup", "0"])
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        bench.main()
+    assert buf.getvalue() == ""
