@@ -38,13 +38,19 @@ CFG = 1
 ROUTED_BYTES = 6 * (2 * 2162688 + 2752512)          # 42,467,328
 SHARED_BYTES = 3 * F * H * 2                        # 50,331,648
 ROUTER_BYTES = E * H * 4                            # 4,194,304
+ROUTED_BYTES_Q4 = 6 * 3 * 4718592                   # Q4_K gate/up/down: 84,934,656
+Q4_LAYERS = 6                                       # q2-q4 model: the last 6 layers at Q4_K
 ACT_BYTES = 2 * H * 4 + E * 4                       # x in, out, bias
 LAYER_BYTES = ROUTED_BYTES + SHARED_BYTES + ROUTER_BYTES + ACT_BYTES
+LAYER_BYTES_Q4 = ROUTED_BYTES_Q4 + SHARED_BYTES + ROUTER_BYTES + ACT_BYTES
 # gate/up launch (dominant kernel): routed gate+up + shared gate+up + x
 GATEUP_BYTES = 6 * 2 * 2162688 + 2 * F * H * 2 + H * 4
 METRIC = "routed-MoE tokens/s (decode, prefill) and achieved HBM GB/s vs B300 peak"
 WORKLOAD = ("config1 full-depth decode: 43 MoE layers x 256 experts (IQ2_XXS gate/up, Q2_K down, "
             "bf16 shared, fp32 router), 1 token at a time, 64 tokens per step")
+WORKLOAD_Q2Q4 = ("q2-q4 full-depth decode: 43 MoE layers x 256 experts, layers 0-36 IQ2_XXS gate/up + Q2_K "
+                 "down, layers 37-42 Q4_K gate/up/down, bf16 shared, fp32 router, 1 token at a time, "
+                 "64 tokens per step")
 
 
 def peaks():
@@ -111,17 +117,20 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ our arm
-def build_model(dev, nlayer, cfg=CFG):
+def build_model(dev, nlayer, cfg=CFG, q4_layers=0):
+    """nlayer layers of 256 experts generated on the device; the last
+    q4_layers of them with Q4_K gate/up/down, the others IQ2_XXS/Q2_K."""
     import torch
     import bit_quantized_moe_bias_b300 as B
     grid = torch.from_numpy(np.ascontiguousarray(synth.iq2_grid(SEED)).view(np.int64).reshape(256)).to(dev)
-    sizes = {0: B.ds4g_packed_size(0, F, H), 1: B.ds4g_packed_size(1, H, F)}
-    tmp = torch.empty(max(sizes.values()), dtype=torch.uint8, device=dev)
+    tmp = torch.empty(B.ds4g_packed_size(2, F, H), dtype=torch.uint8, device=dev)
     layers = []
     for l in range(nlayer):
+        gut, dt = (2, 2) if l >= nlayer - q4_layers else (0, 1)
         mats = {}
-        for kind, qt, rows, cols in ((synth.KIND_GATE, 0, F, H), (synth.KIND_UP, 0, F, H), (synth.KIND_DOWN, 1, H, F)):
-            t = torch.empty(E, sizes[qt], dtype=torch.uint8, device=dev)
+        for kind, qt, rows, cols in ((synth.KIND_GATE, gut, F, H), (synth.KIND_UP, gut, F, H),
+                                     (synth.KIND_DOWN, dt, H, F)):
+            t = torch.empty(E, B.ds4g_packed_size(qt, rows, cols), dtype=torch.uint8, device=dev)
             for e in range(E):
                 synth.gguf_matrix_device(qt, rows, cols, SEED, synth.stream_id(cfg, l, kind, e), tmp.data_ptr(),
                                          torch.cuda.current_stream().cuda_stream)
@@ -129,7 +138,8 @@ def build_model(dev, nlayer, cfg=CFG):
             mats[kind] = t
         shg, shu, shd = synth.shared(SEED, cfg, l)
         sh = [torch.from_numpy(a.view(np.int16)).to(dev) for a in (shg, shu, shd)]
-        L = B.MoELayer(mats[synth.KIND_GATE], mats[synth.KIND_UP], mats[synth.KIND_DOWN], *sh, grid)
+        L = B.MoELayer(mats[synth.KIND_GATE], mats[synth.KIND_UP], mats[synth.KIND_DOWN], *sh,
+                       grid if gut == 0 else None, gut, dt)
         R = torch.from_numpy(synth.router(SEED, cfg, l)).to(dev)
         b = torch.from_numpy(synth.bias_normal(SEED, cfg, l)).to(dev)
         layers.append((L, R, b))
@@ -156,8 +166,11 @@ def run_ours(args, rank, world, local_rank):
     dev = f"cuda:{local_rank}"
     ntok = args.tokens
     nl = args.layers
+    q4 = min(Q4_LAYERS, nl) if args.model == "q2-q4" else 0
+    if q4 and args.decode_path != "fused":
+        raise SystemExit("--model q2-q4 runs through the decode stack (--decode-path fused)")
     t_setup = time.time()
-    layers = build_model(dev, nl)
+    layers = build_model(dev, nl, q4_layers=q4)
     setup_s = time.time() - t_setup
     # per-step inputs: fresh N(0,1) hidden vectors, one per token
     x_host = torch.from_numpy(synth.hidden(SEED + rank, CFG, ntok, layer=999, normalise=False)).pin_memory()
@@ -170,10 +183,11 @@ def run_ours(args, rank, world, local_rank):
     w = torch.empty(1, K, dtype=torch.float32, device=dev)
     rws = B.workspace(B.ds4g_route_workspace(1), dev)
     fws = B.workspace(B.ds4g_forward_workspace(1), dev)
-    lws = B.workspace(B.ds4g_layer_decode_workspace(), dev)
+    lws = B.workspace(B.ds4g_decode_stack_workspace() if q4 else B.ds4g_layer_decode_workspace(), dev)
     fused = args.decode_path in ("fused", "layer")
     stacked = args.decode_path == "fused"
-    launches_per_step = ntok * nl * (1 if fused else 4)
+    # q4 layers of the stack: rmsnorm, route, gate/up and down kernels
+    launches_per_step = ntok * ((nl - q4) * (1 if fused else 4) + 4 * q4)
     stack = B.DecodeStack([(L.struct, R, b) for L, R, b in layers])
     ids_all = torch.empty(nl, K, dtype=torch.int32, device=dev)
     w_all = torch.empty(nl, K, dtype=torch.float32, device=dev)
@@ -279,27 +293,36 @@ def run_ours(args, rank, world, local_rank):
     hbm, kind = peaks()
     kbytes = LAYER_BYTES if fused else GATEUP_BYTES
     kname = "decode_t1_kernel (whole layer)" if fused else "gateup_decode_kernel"
+    token_bytes = (nl - q4) * LAYER_BYTES + q4 * LAYER_BYTES_Q4
+    workload = WORKLOAD
+    if q4:
+        # mixed stack: the figure is the whole step's, layer bytes averaged
+        # over the 43 layers (a q2 layer is one fused launch, a q4 layer four)
+        kbytes = token_bytes // nl
+        kname = "whole stack (decode_t1_kernel for q2 layers; rmsnorm, route, gate/up, down for q4 layers)"
+        workload = WORKLOAD_Q2Q4
     achieved = kbytes / (gu_us * 1e-6) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dev_s / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "layers": nl, "tokens_per_step": ntok, "global_batch": 1,
+        "config": {"workload": workload, "layers": nl, "q4_layers": q4, "tokens_per_step": ntok, "global_batch": 1,
                    "seq_len": 1, "parallelism": "replicas" if world > 1 else "single",
-                   "l2": "no flush: 80 GB of weights streamed per step >> 126 MB L2",
-                   "weight_gb_per_token": round(nl * LAYER_BYTES / 1e9, 4),
-                   "achieved_hbm_gbs_block": round(value / world * nl * LAYER_BYTES / 1e9, 1),
+                   "l2": f"no flush: each token streams {token_bytes / 1e9:.2f} GB of weights >> 126 MB L2",
+                   "weight_gb_per_token": round(token_bytes / 1e9, 4),
+                   "achieved_hbm_gbs_block": round(value / world * token_bytes / 1e9, 1),
                    "decode_path": args.decode_path, "setup_s": round(setup_s, 1)},
         "e2e": {"value": round(tokens / e2e_s, 3), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(x_host.numel() * 4), "d2h_bytes_per_step": int(y_host.numel() * 4)},
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1),
                      "peak": hbm, "peak_kind": kind, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                      "bytes_per_launch": kbytes, "launch_us": round(gu_us, 3),
-                     "traffic": traffic_record("decode_t1_kernel" if fused else "gateup_decode_kernel")},
+                     "traffic": None if q4 else traffic_record("decode_t1_kernel" if fused else
+                                                               "gateup_decode_kernel")},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and not q4:
         line["cpu_baseline"] = cpu_baseline(args.cpu_layers)
     return line
 
@@ -510,6 +533,8 @@ def main():
     ap.add_argument("--workload", choices=["decode", "prefill"], default="decode",
                     help="decode = 43-layer full-depth decode (headline); prefill = T=2048 chunk, one layer")
     ap.add_argument("--cpu-tokens", type=int, default=8, help="prefill CPU-baseline sample size")
+    ap.add_argument("--model", choices=["q2", "q2-q4"], default="q2",
+                    help="decode model: q2 = every layer IQ2_XXS/Q2_K (headline); q2-q4 = last 6 layers Q4_K")
     ap.add_argument("--decode-path", choices=["fused", "layer", "split"], default="fused",
                     help="fused = one stack call per token (one launch per layer, programmatic dependent "
                          "launches); layer = one call per layer; split = rmsnorm, route, gate/up, down launches")

@@ -67,6 +67,7 @@ def lib():
             "ds4g_moe_gate_up": (fwd, i),
             "ds4g_moe_down": (fwd, i),
             "ds4g_layer_decode_workspace": ([], sz),
+            "ds4g_decode_stack_workspace": ([], sz),
             "ds4g_moe_layer_decode": ([vp, i, vp, vp, C.POINTER(ds4g_layer), vp, vp, vp, vp, sz, vp], i),
             "ds4g_moe_decode_stack": ([vp, i, C.POINTER(vp), C.POINTER(vp), C.POINTER(ds4g_layer), vp, vp, vp, vp,
                                        vp, sz, vp], i),
@@ -200,6 +201,10 @@ def ds4g_layer_decode_workspace() -> int:
     return lib().ds4g_layer_decode_workspace()
 
 
+def ds4g_decode_stack_workspace() -> int:
+    return lib().ds4g_decode_stack_workspace()
+
+
 def ds4g_moe_layer_decode(hidden, router, bias, layer: ds4g_layer, ids, w, out, workspace, normalize=True,
                           stream=None):
     """rmsnorm (optional) + route + forward of one token in one launch."""
@@ -223,8 +228,9 @@ class DecodeStack:
 
 
 def ds4g_moe_decode_stack(hidden, stack: DecodeStack, ids, w, hbuf, out, workspace, stream=None):
-    """One token through stack.n chained layers (programmatic dependent
-    launches between them); ids, w: [n][6]; hbuf: [2][4096] scratch."""
+    """One token through stack.n chained layers (IQ2_XXS/Q2_K layers fused,
+    programmatic dependent launches between them; Q4_K layers as rmsnorm +
+    route + forward); ids, w: [n][6]; hbuf: [2][4096] scratch."""
     _check("ds4g_moe_decode_stack",
            lib().ds4g_moe_decode_stack(_ptr(hidden), stack.n, stack.routers, stack.biases, stack.structs, _ptr(ids),
                                        _ptr(w), _ptr(hbuf), _ptr(out), _ptr(workspace), workspace.numel(),

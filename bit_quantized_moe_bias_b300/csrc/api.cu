@@ -4,9 +4,6 @@
 #include "ds4g_internal.cuh"
 
 namespace ds4g {
-size_t decode_workspace(int T);
-ds4g_status decode_forward(const float *hidden, int T, const ds4g_layer *L, const int32_t *ids,
-                           const float *w, float *out, void *workspace, cudaStream_t st, int phases);
 size_t prefill_workspace(int T);
 ds4g_status prefill_forward(const float *hidden, int T, const ds4g_layer *L, const int32_t *ids, const float *w,
                             float *out, void *workspace, cudaStream_t st, int phases);

@@ -55,6 +55,7 @@ struct DecodeArgs {
     float *part_s;        // [128][kSplitS][2][T][16]
     __half *hq;           // [6T][2][2048]  routed h as fp16 (hi, lo)
     float *xs16;          // [6T][8][4][4]  sums of h over 16 consecutive entries
+    float *hsc16;         // [6T][8][4][4]  power-of-two scale of each 16 entries of hq (layout of xs16)
     __nv_bfloat16 *hs;    // [T][2][2048]   shared h as bf16 (hi, lo)
     float *part_dr;       // [T][256][8][16]
     float *part_ds;       // [256][8][T][16]
@@ -99,8 +100,18 @@ struct GUSmem {
     __nv_bfloat16 *xb;  // [T][2][4096] activation bf16 (hi, lo)
 };
 
+// Exponent e >= 0 such that every |h| <= m of a group, scaled by 2^-e, is
+// below 2^15 (then its fp16 hi/lo pair is exact to ~2^-22 of the group's
+// largest value); e = 0 when m < 2^15.
+__device__ __forceinline__ int h_group_exp(float m) {
+    const int E = (int)((__float_as_uint(m) >> 23) & 255u) - 126;   // m < 2^E for normal m
+    return E > 15 ? E - 15 : 0;
+}
+
 // Reduction of one (slot, tile) of routed gate/up: 8 split partials in fixed
-// order -> h = silu(g) * u -> fp16 hi/lo, plus the 16-row sum of h.
+// order -> h = silu(g) * u; the 16 values, scaled by a power of two 2^-e
+// shared by the tile (so that any finite h fits the fp16 range), as fp16
+// hi/lo; 2^e; and the 16-row sum of the unscaled h.
 __device__ __forceinline__ void gu_routed_finish(const DecodeArgs &a, int slot, int tile) {
     const int lane = threadIdx.x & 31;
     float h = 0.f;
@@ -113,9 +124,16 @@ __device__ __forceinline__ void gu_routed_finish(const DecodeArgs &a, int slot, 
             us += __ldcg(base + s * 32 + 16 + lane);
         }
         h = silu_f(gs) * us;
-        if (!(fabsf(h) < 65504.f)) flag_status(a.status, DS4G_EDEVICE, 0xF16u);
+        if (!(fabsf(h) <= 3.4028235e38f)) flag_status(a.status, DS4G_EDEVICE, 0xF16u);   // inf or NaN
+    }
+    float m = fabsf(h);
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    const int e = h_group_exp(m);
+    const int b = tile >> 4, j = tile & 15;
+    if (lane < 16) {
         __half hi, lo;
-        split_f16(h, hi, lo);
+        split_f16(h * __uint_as_float((uint32_t)(127 - e) << 23), hi, lo);
         a.hq[((size_t)slot * 2 + 0) * kF + tile * 16 + lane] = hi;
         a.hq[((size_t)slot * 2 + 1) * kF + tile * 16 + lane] = lo;
     }
@@ -123,8 +141,8 @@ __device__ __forceinline__ void gu_routed_finish(const DecodeArgs &a, int slot, 
 #pragma unroll
     for (int off = 8; off > 0; off >>= 1) h += __shfl_xor_sync(0xffffffffu, h, off);
     if (lane == 0) {
-        const int b = tile >> 4, j = tile & 15;
         a.xs16[(size_t)slot * 128 + (b * 4 + (j & 3)) * 4 + (j >> 2)] = h;
+        a.hsc16[(size_t)slot * 128 + (b * 4 + (j & 3)) * 4 + (j >> 2)] = __uint_as_float((uint32_t)(127 + e) << 23);
     }
 }
 
@@ -434,6 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(DecodeArgs a
 struct DNSmem {
     __half *hq;          // [6T][2][2048]
     float *xs;           // [6T][128]
+    float *hsc;          // [6T][128] scale of each 16 entries of hq
     __nv_bfloat16 *hs;   // [T][2][2048]
 };
 
@@ -502,6 +521,7 @@ __device__ __forceinline__ void dn_routed_q2k(const DecodeArgs &a, const DNSmem 
         const float wk = a.w[slot];
         const __half *hrow = sm.hq + ((size_t)slot * 2 + (g & 1)) * kF + 256 * b + 16 * t;
         const float4 X = *reinterpret_cast<const float4 *>(sm.xs + (size_t)slot * 128 + (b * 4 + t) * 4);
+        const float4 S = *reinterpret_cast<const float4 *>(sm.hsc + (size_t)slot * 128 + (b * 4 + t) * 4);
         const float dg = __half2float(__ushort_as_half((unsigned short)(dd[k].x & 0xffff))) * 16777216.0f;
         const float mg = __half2float(__ushort_as_half((unsigned short)(dd[k].x >> 16)));
         const float dh = __half2float(__ushort_as_half((unsigned short)(dd[k].y & 0xffff))) * 16777216.0f;
@@ -509,6 +529,7 @@ __device__ __forceinline__ void dn_routed_q2k(const DecodeArgs &a, const DNSmem 
         const uint32_t Wa[4] = {qa[k].x, qa[k].y, qa[k].z, qa[k].w};
         const uint32_t Wb[4] = {qb[k].x, qb[k].y, qb[k].z, qb[k].w};
         const float Xg[4] = {X.x, X.y, X.z, X.w};
+        const float Sg[4] = {S.x, S.y, S.z, S.w};
         float sg = 0.f, sh = 0.f;
 #pragma unroll
         for (int G = 0; G < 4; ++G) {
@@ -520,8 +541,8 @@ __device__ __forceinline__ void dn_routed_q2k(const DecodeArgs &a, const DNSmem 
                         (Wa[G] >> (4 * cc + 2)) & 0x00030003u, (Wb[G] >> (4 * cc + 2)) & 0x00030003u, bv.x, bv.y);
             }
             const uint32_t ba = (sca[k] >> (8 * G)) & 0xffu, bb = (scb[k] >> (8 * G)) & 0xffu;
-            sg += dg * small_u2f(ba & 15u) * (c[0] + c[1]) - mg * small_u2f(ba >> 4) * Xg[G];
-            sh += dh * small_u2f(bb & 15u) * (c[2] + c[3]) - mh * small_u2f(bb >> 4) * Xg[G];
+            sg += dg * small_u2f(ba & 15u) * ((c[0] + c[1]) * Sg[G]) - mg * small_u2f(ba >> 4) * Xg[G];
+            sh += dh * small_u2f(bb & 15u) * ((c[2] + c[3]) * Sg[G]) - mh * small_u2f(bb >> 4) * Xg[G];
         }
         racc[0] = fmaf(wk, sg, racc[0]);
         racc[1] = fmaf(wk, sh, racc[1]);
@@ -567,9 +588,12 @@ __device__ __forceinline__ void dn_routed_q4k(const DecodeArgs &a, const DNSmem 
         for (int jj = 0; jj < 2; ++jj) {
             const int j = 4 * jj + t;  // 32-col sub-block = 16-col sub-blocks 2j, 2j+1
             const int ja = 2 * j, jb = 2 * j + 1;
-            const float X = sm.xs[(size_t)slot * 128 + (b * 4 + (ja & 3)) * 4 + (ja >> 2)] +
-                            sm.xs[(size_t)slot * 128 + (b * 4 + (jb & 3)) * 4 + (jb >> 2)];
-            float c[4] = {0.f, 0.f, 0.f, 0.f};
+            const int ia = (b * 4 + (ja & 3)) * 4 + (ja >> 2), ib = (b * 4 + (jb & 3)) * 4 + (jb >> 2);
+            const float X = sm.xs[(size_t)slot * 128 + ia] + sm.xs[(size_t)slot * 128 + ib];
+            const float Sa = sm.hsc[(size_t)slot * 128 + ia], Sb = sm.hsc[(size_t)slot * 128 + ib];
+            // columns of the 16-entry groups ja (cc < 4) and jb (cc >= 4) of h
+            // carry their own scales: one accumulator each
+            float c[4] = {0.f, 0.f, 0.f, 0.f}, cb[4] = {0.f, 0.f, 0.f, 0.f};
             const uint32_t wa[4] = {q[0][jj].x, q[0][jj].y, q[0][jj].z, q[0][jj].w};
             const uint32_t wb[4] = {q[1][jj].x, q[1][jj].y, q[1][jj].z, q[1][jj].w};
 #pragma unroll
@@ -577,8 +601,8 @@ __device__ __forceinline__ void dn_routed_q4k(const DecodeArgs &a, const DNSmem 
                 const uint2 bv = active ? *reinterpret_cast<const uint2 *>(hrow + 32 * j + 4 * cc) : make_uint2(0, 0);
                 const uint32_t Wa = wa[cc >> 1], Wb = wb[cc >> 1];
                 const int s0 = 8 * (cc & 1);
-                mma_f16(c, (Wa >> s0) & 0x000F000Fu, (Wb >> s0) & 0x000F000Fu, (Wa >> (s0 + 4)) & 0x000F000Fu,
-                        (Wb >> (s0 + 4)) & 0x000F000Fu, bv.x, bv.y);
+                mma_f16(cc < 4 ? c : cb, (Wa >> s0) & 0x000F000Fu, (Wb >> s0) & 0x000F000Fu,
+                        (Wa >> (s0 + 4)) & 0x000F000Fu, (Wb >> (s0 + 4)) & 0x000F000Fu, bv.x, bv.y);
             }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -593,7 +617,8 @@ __device__ __forceinline__ void dn_routed_q4k(const DecodeArgs &a, const DNSmem 
                     sc = (s2b & 15u) | ((s0 >> 6) << 4);
                     mn = (s2b >> 4) | ((s1 >> 6) << 4);
                 }
-                const float dot = h ? (c[2] + c[3]) : (c[0] + c[1]);
+                const float dot = h ? (c[2] + c[3]) * Sa + (cb[2] + cb[3]) * Sb
+                                    : (c[0] + c[1]) * Sa + (cb[0] + cb[1]) * Sb;
                 racc[h] = fmaf(wk, dgv[h] * small_u2f(sc) * dot - dmv[h] * small_u2f(mn) * X, racc[h]);
             }
         }
@@ -634,7 +659,8 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(DecodeArgs a) 
     const int nslot = kK * a.T;
     sm.hq = reinterpret_cast<__half *>(smem_raw);
     sm.xs = reinterpret_cast<float *>(sm.hq + (size_t)nslot * 2 * kF);
-    sm.hs = reinterpret_cast<__nv_bfloat16 *>(sm.xs + (size_t)nslot * 128);
+    sm.hsc = sm.xs + (size_t)nslot * 128;
+    sm.hs = reinterpret_cast<__nv_bfloat16 *>(sm.hsc + (size_t)nslot * 128);
     const int tid = threadIdx.x;
     {
         const uint4 *src = reinterpret_cast<const uint4 *>(a.hq);
@@ -643,6 +669,9 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(DecodeArgs a) 
         const uint4 *s2 = reinterpret_cast<const uint4 *>(a.xs16);
         uint4 *d2 = reinterpret_cast<uint4 *>(sm.xs);
         for (int i = tid; i < nslot * 128 / 4; i += kThreads) d2[i] = __ldcg(s2 + i);
+        const uint4 *s4 = reinterpret_cast<const uint4 *>(a.hsc16);
+        uint4 *d4 = reinterpret_cast<uint4 *>(sm.hsc);
+        for (int i = tid; i < nslot * 128 / 4; i += kThreads) d4[i] = __ldcg(s4 + i);
         const uint4 *s3 = reinterpret_cast<const uint4 *>(a.hs);
         uint4 *d3 = reinterpret_cast<uint4 *>(sm.hs);
         for (int i = tid; i < a.T * 2 * kF / 8; i += kThreads) d3[i] = __ldcg(s3 + i);
@@ -661,7 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1) down_decode_kernel(DecodeArgs a) 
 
 // ------------------------------------------------------------------ host
 struct WsLayout {
-    size_t cnt_gu, cnt_dn, part_r, part_s, hq, xs16, hs, part_dr, part_ds, total;
+    size_t cnt_gu, cnt_dn, part_r, part_s, hq, xs16, hsc16, hs, part_dr, part_ds, total;
 };
 
 static WsLayout ws_layout(int T) {
@@ -680,6 +709,8 @@ static WsLayout ws_layout(int T) {
     off += align_up(ns * 2 * kF * 2, 256);
     L.xs16 = off;
     off += align_up(ns * 128 * 4, 256);
+    L.hsc16 = off;
+    off += align_up(ns * 128 * 4, 256);
     L.hs = off;
     off += align_up((size_t)T * 2 * kF * 2, 256);
     L.part_dr = off;
@@ -695,7 +726,8 @@ size_t decode_workspace(int T) { return ws_layout(T).total; }
 static int g_num_sms = 0;
 
 ds4g_status decode_forward(const float *hidden, int T, const ds4g_layer *L, const int32_t *ids,
-                           const float *w, float *out, void *workspace, cudaStream_t st, int phases) {
+                           const float *w, float *out, void *workspace, cudaStream_t st, int phases,
+                           uint32_t *status_word) {
     if (!g_num_sms) {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess) return DS4G_ECUDA;
@@ -719,20 +751,21 @@ ds4g_status decode_forward(const float *hidden, int T, const ds4g_layer *L, cons
     a.out = out;
     uint8_t *ws = (uint8_t *)workspace;
     const WsLayout wl = ws_layout(T);
-    a.status = (uint32_t *)ws;
+    a.status = status_word ? status_word : (uint32_t *)ws;
     a.cnt_gu = (uint32_t *)(ws + wl.cnt_gu);
     a.cnt_dn = (uint32_t *)(ws + wl.cnt_dn);
     a.part_r = (float *)(ws + wl.part_r);
     a.part_s = (float *)(ws + wl.part_s);
     a.hq = (__half *)(ws + wl.hq);
     a.xs16 = (float *)(ws + wl.xs16);
+    a.hsc16 = (float *)(ws + wl.hsc16);
     a.hs = (__nv_bfloat16 *)(ws + wl.hs);
     a.part_dr = (float *)(ws + wl.part_dr);
     a.part_ds = (float *)(ws + wl.part_ds);
 
     const size_t ns = (size_t)kK * T;
     const size_t smem_gu = 256 * 16 * 8 + 128 * 16 * 8 + (size_t)T * 2 * kH * 2 * 2;
-    const size_t smem_dn = ns * 2 * kF * 2 + ns * 128 * 4 + (size_t)T * 2 * kF * 2;
+    const size_t smem_dn = ns * 2 * kF * 2 + 2 * ns * 128 * 4 + (size_t)T * 2 * kF * 2;
     static bool attr_done = false;
     if (!attr_done) {
         if (cudaFuncSetAttribute(gateup_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=

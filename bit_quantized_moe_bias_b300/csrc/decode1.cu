@@ -41,6 +41,9 @@
 // the previous layer's CTAs leave, build their tables and start streaming
 // router and shared-expert pieces, and touch the input and the workspace
 // only after griddepcontrol.wait (the previous layer complete and visible).
+// A stack's Q4_K layers (the last six of the q2-q4 model, chenxutan ds4
+// article §2.1) run as rmsnorm + route + the decode path of the forward; the
+// fused layer that follows one of them is launched in plain stream order.
 //
 // Arithmetic: router and shared expert in fp32 FMA (bf16 weights widen
 // exactly); routed experts on mma.sync with exact codes (IQ2 grid value or
@@ -1081,6 +1084,36 @@ static D1Layout d1_layout() {
     return L;
 }
 
+// Layers of a stack that are not IQ2_XXS/Q2_K (the q4 layers: Q4_K
+// gate/up/down) run as rmsnorm + route + the decode path of the forward.
+// Their scratch follows the fused kernel's part of the workspace: the
+// normalised input, the route's ids and weights (16-byte aligned rows), and
+// the route's and the forward's own workspaces.  Faults are recorded in the
+// workspace's header, as for the fused layers.
+struct StackLayout {
+    size_t xn, ids, w, route_ws, fwd_ws, total;
+};
+static StackLayout stack_layout() {
+    StackLayout L;
+    size_t off = align_up(d1_layout().total, 256);
+    L.xn = off;
+    off += align_up((size_t)kH * 4, 256);
+    L.ids = off;
+    off += 256;
+    L.w = off;
+    off += 256;
+    L.route_ws = off;
+    off += align_up(ds4g_route_workspace(1), 256);
+    L.fwd_ws = off;
+    off += align_up(decode_workspace(1), 256);
+    L.total = off;
+    return L;
+}
+
+static bool d1_fused(const ds4g_layer *L) {
+    return L->gate_up_type == DS4G_IQ2_XXS && L->down_type == DS4G_Q2_K;
+}
+
 static int g_d1_sms = 0;
 static bool g_d1_attr = false;
 
@@ -1099,6 +1132,47 @@ static ds4g_status d1_check(const float *hidden, const float *router, const floa
                          (uintptr_t)L->sh_gate | (uintptr_t)L->sh_up | (uintptr_t)L->sh_down | (uintptr_t)L->iq2_grid;
     if ((al & 15) || (((uintptr_t)ids | (uintptr_t)w) & 3)) return DS4G_EALIGN;
     if (ws_bytes < d1_layout().total) return DS4G_ENOSPACE;
+    return DS4G_OK;
+}
+
+// Host checks of one stack layer: the fused kernel's for IQ2_XXS/Q2_K
+// layers; for Q4_K layers the forward's, against the larger workspace.
+static ds4g_status stack_layer_check(const float *hidden, const float *router, const float *bias,
+                                     const ds4g_layer *L, const int32_t *ids, const float *w, const float *out,
+                                     const void *workspace, size_t ws_bytes) {
+    if (!L) return DS4G_EINVAL;
+    if (d1_fused(L)) return d1_check(hidden, router, bias, L, ids, w, out, workspace, ws_bytes);
+    if (L->gate_up_type != DS4G_Q4_K || L->down_type != DS4G_Q4_K) return DS4G_EUNSUPPORTED;
+    if (!hidden || !router || !bias || !ids || !w || !out || !workspace) return DS4G_EINVAL;
+    if (!L->gate || !L->up || !L->down || !L->sh_gate || !L->sh_up || !L->sh_down) return DS4G_EINVAL;
+    const uintptr_t al = (uintptr_t)hidden | (uintptr_t)router | (uintptr_t)bias | (uintptr_t)out |
+                         (uintptr_t)workspace | (uintptr_t)L->gate | (uintptr_t)L->up | (uintptr_t)L->down |
+                         (uintptr_t)L->sh_gate | (uintptr_t)L->sh_up | (uintptr_t)L->sh_down;
+    if ((al & 15) || (((uintptr_t)ids | (uintptr_t)w) & 3)) return DS4G_EALIGN;
+    if (ws_bytes < stack_layout().total) return DS4G_ENOSPACE;
+    return DS4G_OK;
+}
+
+// One Q4_K layer of a stack: xn = rmsnorm(x); ids, w = route(xn); o = the
+// decode forward of xn.  ids/w rows of the stack are only 4-byte aligned,
+// so the route writes aligned scratch rows that are then copied out.
+static ds4g_status stack_run_unfused(const float *x, const float *router, const float *bias, const ds4g_layer *L,
+                                     int32_t *ids, float *w, float *o, void *workspace, cudaStream_t s) {
+    const StackLayout lay = stack_layout();
+    uint8_t *ws = (uint8_t *)workspace;
+    float *xn = (float *)(ws + lay.xn);
+    int32_t *ids_t = (int32_t *)(ws + lay.ids);
+    float *w_t = (float *)(ws + lay.w);
+    ds4g_status st = ds4g_rmsnorm(x, 1, xn, (ds4g_stream_t)s);
+    if (st != DS4G_OK) return st;
+    st = ds4g_moe_route(xn, 1, router, bias, ids_t, w_t, ws + lay.route_ws, ds4g_route_workspace(1),
+                        (ds4g_stream_t)s);
+    if (st != DS4G_OK) return st;
+    st = decode_forward(xn, 1, L, ids_t, w_t, o, ws + lay.fwd_ws, s, 3, (uint32_t *)ws);
+    if (st != DS4G_OK) return st;
+    if (cudaMemcpyAsync(ids, ids_t, kK * sizeof(int32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(w, w_t, kK * sizeof(float), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+        return DS4G_ECUDA;
     return DS4G_OK;
 }
 
@@ -1171,6 +1245,8 @@ using namespace ds4g;
 
 extern "C" size_t ds4g_layer_decode_workspace(void) { return d1_layout().total; }
 
+extern "C" size_t ds4g_decode_stack_workspace(void) { return stack_layout().total; }
+
 extern "C" ds4g_status ds4g_moe_layer_decode(const float *hidden, int normalize, const float *router,
                                              const float *bias, const ds4g_layer *L, int32_t *ids, float *w,
                                              float *out, void *workspace, size_t ws_bytes, ds4g_stream_t s) {
@@ -1188,8 +1264,8 @@ extern "C" ds4g_status ds4g_moe_decode_stack(const float *hidden, int n_layers, 
     if (n_layers < 1 || n_layers > 1024 || !routers || !biases || !layers || !hbuf || !ids || !w) return DS4G_EINVAL;
     if (((uintptr_t)hbuf | (uintptr_t)ids | (uintptr_t)w) & 15) return DS4G_EALIGN;
     for (int l = 0; l < n_layers; ++l) {
-        const ds4g_status st = d1_check(hidden, routers[l], biases[l], &layers[l], ids + kK * l, w + kK * l, out,
-                                        workspace, ws_bytes);
+        const ds4g_status st = stack_layer_check(hidden, routers[l], biases[l], &layers[l], ids + kK * l,
+                                                 w + kK * l, out, workspace, ws_bytes);
         if (st != DS4G_OK) return st;
     }
     ds4g_status st = d1_setup();
@@ -1197,8 +1273,16 @@ extern "C" ds4g_status ds4g_moe_decode_stack(const float *hidden, int n_layers, 
     for (int l = 0; l < n_layers; ++l) {
         const float *x = l == 0 ? hidden : hbuf + (size_t)((l - 1) & 1) * kH;
         float *o = l == n_layers - 1 ? out : hbuf + (size_t)(l & 1) * kH;
-        st = d1_launch(d1_args(x, 1, routers[l], biases[l], &layers[l], ids + kK * l, w + kK * l, o, workspace),
-                       (cudaStream_t)s, l > 0);
+        if (d1_fused(&layers[l])) {
+            // a programmatic dependent only of the same kernel (a fused previous layer)
+            const bool pdl = l > 0 && d1_fused(&layers[l - 1]);
+            st = d1_launch(
+                d1_args(x, 1, routers[l], biases[l], &layers[l], ids + kK * l, w + kK * l, o, workspace),
+                (cudaStream_t)s, pdl);
+        } else {
+            st = stack_run_unfused(x, routers[l], biases[l], &layers[l], ids + kK * l, w + kK * l, o, workspace,
+                                   (cudaStream_t)s);
+        }
         if (st != DS4G_OK) return st;
     }
     return DS4G_OK;

@@ -59,6 +59,15 @@ __device__ inline void flag_status(uint32_t *ws_status, uint32_t code, uint32_t 
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Decode path of the MoE block (decode.cu, 1 <= T <= 64): workspace bytes,
+// and the launch of its kernels (phases: 1 gate/up, 2 down, 3 both).
+// status_word: where its kernels record a fault (nullptr: the workspace's
+// own header).
+size_t decode_workspace(int T);
+ds4g_status decode_forward(const float *hidden, int T, const ds4g_layer *L, const int32_t *ids, const float *w,
+                           float *out, void *workspace, cudaStream_t st, int phases,
+                           uint32_t *status_word = nullptr);
+
 // An expert id is usable if it is in range and its packed matrices are
 // non-NULL and 16-byte aligned (a misaligned vector load would fault).
 __device__ __forceinline__ bool expert_ok(int e, const void *const *a, const void *const *b,

@@ -197,8 +197,10 @@ typedef struct {
  * are summed).  Two paths, chosen by T:
  *  - T < 64 (decode): per-slot dequant-in-register GEMV, processed in chunks
  *    of 3 tokens.  Codes enter the tensor cores exactly; activations as an
- *    fp16 hi+lo pair (|x| < 65504 required, else DS4G_EDEVICE); fp32
- *    accumulation.  Expected error ~1e-5 relative.
+ *    fp16 hi+lo pair (|x| < 65504 required, else DS4G_EDEVICE); h as an
+ *    fp16 hi+lo pair scaled by a power of two per 16 entries (any finite h;
+ *    inf/NaN is DS4G_EDEVICE); fp32 accumulation.  Expected error ~1e-5
+ *    relative.
  *  - T >= 64 (chunked prefill, large batches): tokens bucketed by expert,
  *    grouped tcgen05 GEMM.  Weights are the fp32 block formula rounded to
  *    nearest even: fp16 with fp16 activations for the routed gate/up
@@ -257,26 +259,35 @@ ds4g_status ds4g_moe_layer_decode(const float *hidden, int normalize, const floa
                                   ds4g_stream_t s);
 
 /* ------------------------------------------------------------------------
- * One decode token through n_layers chained MoE layers: layer l is
- * ds4g_moe_layer_decode with normalize = 1 on the input
- *   x_0 = hidden,  x_l = output of layer l-1  (l >= 1),
- * i.e. every layer's input is RMS-normalised in the kernel and no residual
- * is added (the full-depth decode workload of 43 such layers).
+ * One decode token through n_layers chained MoE layers on the input
+ *   x_0 = hidden,  x_l = output of layer l-1  (l >= 1);
+ * every layer's input is RMS-normalised and no residual is added (the
+ * full-depth decode workload of 43 such layers).  Layer l is
+ *  - IQ2_XXS gate/up + Q2_K down: ds4g_moe_layer_decode with normalize = 1;
+ *  - Q4_K gate/up/down (the q4 layers of the q2-q4 model, chenxutan ds4
+ *    article §2.1): ds4g_rmsnorm, then ds4g_moe_route, then the T = 1
+ *    ds4g_moe_forward, all on s;
+ *  - any other type combination: DS4G_EUNSUPPORTED.
  *   hidden   [4096] f32 dev            routers  host array [n_layers] of dev
  *   layers   host array [n_layers]       pointers to [256][4096] f32
  *   biases   host array [n_layers] of dev pointers to [256] f32
  *   ids      [n_layers][6] int32 dev (out)   w  [n_layers][6] f32 dev (out)
  *   hbuf     [2][4096] f32 dev: scratch for the intermediate outputs
  *   out      [4096] f32 dev: the last layer's output
- *   workspace as for ds4g_moe_layer_decode (one workspace serves all layers).
+ *   workspace dev, zeroed once before first use, one call at a time; one
+ *            workspace serves all layers: >= ds4g_layer_decode_workspace()
+ *            bytes if every layer is IQ2_XXS/Q2_K, >=
+ *            ds4g_decode_stack_workspace() bytes if any layer is Q4_K (else
+ *            DS4G_ENOSPACE).  Faults are read with ds4g_last_error.
  * 1 <= n_layers <= 1024, else DS4G_EINVAL.  All checks of every layer run
- * before the first launch.  Same results, bit for bit, as n_layers calls of
- * ds4g_moe_layer_decode.  Each launch after the first uses programmatic
- * dependent launch: its CTAs start on the SMs that the previous layer's CTAs
- * leave, build their tables and begin streaming the layer's router and
- * shared-expert weights, and read their input and the workspace only after
- * the previous layer has completed.
+ * before the first launch.  Same results, bit for bit, as the per-layer
+ * calls listed above.  A fused layer that follows a fused layer is a
+ * programmatic dependent launch: its CTAs start on the SMs that the previous
+ * layer's CTAs leave, build their tables and begin streaming the layer's
+ * router and shared-expert weights, and read their input and the workspace
+ * only after the previous layer has completed.
  * ------------------------------------------------------------------------ */
+size_t ds4g_decode_stack_workspace(void);
 ds4g_status ds4g_moe_decode_stack(const float *hidden, int n_layers, const float *const *routers,
                                   const float *const *biases, const ds4g_layer *layers,
                                   int32_t *ids, float *w, float *hbuf, float *out,

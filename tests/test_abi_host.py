@@ -137,6 +137,32 @@ def test_gpu_entry_points_validate_before_launch():
     assert L.ds4g_quantize_pack_device(1, 16, 256, odd, fake, None) == 2
 
 
+def test_decode_stack_validates_layer_types_and_workspace():
+    """The stack checks every layer before any CUDA call: Q4_K layers need
+    the larger stack workspace, mixed IQ2/Q4_K types are refused."""
+    L = B.lib()
+    fake = 0x10000000
+    q2 = B.ds4g_layer(0, 1, fake, fake, fake, fake, fake, fake, fake)
+    q4 = B.ds4g_layer(2, 2, fake, fake, fake, fake, fake, fake, None)
+    mix = B.ds4g_layer(0, 2, fake, fake, fake, fake, fake, fake, fake)
+    q4_odd = B.ds4g_layer(2, 2, fake, fake, fake, fake + 8, fake, fake, None)
+    small, big = B.ds4g_layer_decode_workspace(), B.ds4g_decode_stack_workspace()
+    assert small < big
+
+    def stack(layers, ws_bytes, routers=True):
+        n = len(layers)
+        structs = (B.ds4g_layer * n)(*layers)
+        ptrs = (C.c_void_p * n)(*([fake] * n))
+        return L.ds4g_moe_decode_stack(fake, n, ptrs if routers else None, ptrs, structs, fake, fake, fake, fake,
+                                       fake, ws_bytes, None)
+
+    assert stack([q2, q4], small) == 3          # q4 layers use scratch beyond the fused kernel's
+    assert stack([q4], big - 1) == 3
+    assert stack([q2, mix], big) == 5
+    assert stack([q4_odd], big) == 2
+    assert stack([q2, q4], big, routers=False) == 1
+
+
 def test_workspace_sizes_grow_with_T():
     assert B.ds4g_route_workspace(0) == 0
     assert B.ds4g_route_workspace(1) < B.ds4g_route_workspace(2048)

@@ -145,3 +145,65 @@ def test_decode_stack_rejects_bad_arguments():
     with pytest.raises(B.DS4GError) as e:
         B.ds4g_moe_decode_stack(x, stack, ids, w, hbuf, out, ws)
     assert e.value.code == 1
+
+
+def test_decode_stack_q2_q4_layers():
+    """A stack of IQ2_XXS/Q2_K and Q4_K layers (the q2-q4 model keeps its
+    last layers at Q4_K): the fused kernel runs the q2 layers, rmsnorm +
+    route + forward the q4 layers.  Equal bit for bit to those calls made
+    one at a time, and following the oracle's chain."""
+    seed, cfg = 5, 4
+    kinds = [(synth.IQ2_XXS, synth.Q2_K), (synth.Q4_K, synth.Q4_K), (synth.Q4_K, synth.Q4_K),
+             (synth.IQ2_XXS, synth.Q2_K)]
+    NL = len(kinds)
+    x = synth.hidden(seed, cfg, 1, layer=11, normalise=False)
+    h = oracle.rmsnorm(x)
+    refs, layers = [], []
+    for l, (gut, dt) in enumerate(kinds):
+        R, b = synth.router(seed, cfg, l), synth.bias_normal(seed, cfg, l)
+        ids_r, w_r, keys, margin = oracle.route(h, R, b)
+        assert margin[0] > 1e-3
+        L, hx, shared, grid = device_layer(seed, cfg, l, ids_r.reshape(-1), gut, dt)
+        out_r = oracle_forward(h, ids_r, w_r, hx, shared, grid, gut, dt)
+        refs.append((ids_r, w_r, keys, margin, out_r))
+        layers.append((L, _t(R), _t(b)))
+        h = oracle.rmsnorm(out_r)
+    stack = B.DecodeStack([(L.struct, R, b) for L, R, b in layers])
+    ids = torch.full((NL, K), -1, dtype=torch.int32, device=DEV)
+    w = torch.zeros(NL, K, dtype=torch.float32, device=DEV)
+    hbuf = torch.zeros(2, H, dtype=torch.float32, device=DEV)
+    out = torch.full((H,), float("nan"), dtype=torch.float32, device=DEV)
+    xd = _t(x[0])
+    assert B.ds4g_decode_stack_workspace() > B.ds4g_layer_decode_workspace()
+    with pytest.raises(B.DS4GError) as e:       # q4 layers need the larger workspace
+        B.ds4g_moe_decode_stack(xd, stack, ids, w, hbuf, out, B.workspace(B.ds4g_layer_decode_workspace()))
+    assert e.value.code == 3
+    ws = B.workspace(B.ds4g_decode_stack_workspace())
+    for _ in range(2):                               # the workspace is reusable call after call
+        B.ds4g_moe_decode_stack(xd, stack, ids, w, hbuf, out, ws)
+        assert B.ds4g_last_error(ws) == 0
+    ids_s, w_s, out_s = ids.cpu().numpy(), w.cpu().numpy(), out.cpu().numpy()
+    for l in range(NL):
+        ids_r, w_r, keys, margin, _ = refs[l]
+        check_route(ids_s[l][None], w_s[l][None], ids_r, w_r, keys, margin)
+    assert_close_fwd(out_s[None], refs[-1][4])
+    # the same layers one call at a time
+    wsl = B.workspace(B.ds4g_layer_decode_workspace())
+    rws = B.workspace(B.ds4g_route_workspace(1))
+    fws = B.workspace(B.ds4g_forward_workspace(1))
+    xl = xd[None]
+    for l, ((gut, _), (L, R, b)) in enumerate(zip(kinds, layers)):
+        i1 = torch.full((1, K), -1, dtype=torch.int32, device=DEV)
+        w1 = torch.zeros(1, K, dtype=torch.float32, device=DEV)
+        o1 = torch.empty(1, H, dtype=torch.float32, device=DEV)
+        if gut == synth.IQ2_XXS:
+            B.ds4g_moe_layer_decode(xl[0], R, b, L.struct, i1[0], w1[0], o1[0], wsl)
+        else:
+            xn = torch.empty(1, H, dtype=torch.float32, device=DEV)
+            B.ds4g_rmsnorm(xl, xn)
+            B.ds4g_moe_route(xn, R, b, i1, w1, rws)
+            B.ds4g_moe_forward(xn, L.struct, i1, w1, o1, fws)
+        assert np.array_equal(i1.cpu().numpy()[0], ids_s[l]) and np.array_equal(w1.cpu().numpy()[0], w_s[l])
+        xl = o1
+    assert np.array_equal(xl.cpu().numpy()[0], out_s)
+    assert B.ds4g_last_error(wsl) == 0 and B.ds4g_last_error(fws) == 0

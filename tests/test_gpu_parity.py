@@ -226,3 +226,25 @@ def test_forward_large_activation_flagged():
     L, _, _, _ = device_layer(0, 0, 0, range(6))
     _, st = _forward_gpu(x, ids, w, L)
     assert st == 7
+
+
+@pytest.mark.parametrize("gut,dt", [(synth.IQ2_XXS, synth.Q2_K), (synth.Q4_K, synth.Q4_K)])
+def test_forward_decode_h_beyond_fp16_range(gut, dt):
+    """h = silu(g) * u far beyond the fp16 range (inputs with a large common
+    mode, as a chain of layers produces) is carried by a power-of-two scale
+    per 16 entries: no flag, oracle parity."""
+    rng = np.random.default_rng(11)
+    if gut == synth.Q4_K:   # Q4_K weights have a positive mean: a near-constant x adds up
+        x = oracle.rmsnorm((1.0 + 0.1 * rng.standard_normal((2, H))).astype(np.float32))
+    else:
+        x = (60.0 * rng.standard_normal((2, H))).astype(np.float32)
+    ids, w, _, _ = oracle.route(x, synth.router(6, 4), synth.bias_normal(6, 4))
+    L, hx, shared, grid = device_layer(6, 4, 5, ids.reshape(-1), gut, dt)
+    g, u, _ = hx[int(ids[0, 0])]
+    G = oracle.dequantize(gut, g, 2048, H, grid).astype(np.float64)
+    U = oracle.dequantize(gut, u, 2048, H, grid).astype(np.float64)
+    gg, uu = G @ x[0].astype(np.float64), U @ x[0].astype(np.float64)
+    assert np.abs(gg * 0.5 * (1.0 + np.tanh(0.5 * gg)) * uu).max() > 1e5   # the case this test is about
+    got, st = _forward_gpu(x, ids, w, L)
+    assert st == 0
+    assert_close_fwd(got, oracle_forward(x, ids, w, hx, shared, grid, gut, dt))
