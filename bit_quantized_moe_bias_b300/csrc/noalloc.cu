@@ -9,7 +9,7 @@
 namespace ds4g {
 
 // Scratch of the per-slot decode kernels for one chunk of kDecodeMaxT tokens
-// (the layout of decode_workspace(kDecodeMaxT), 4.68 MB).  Every device
+// (the layout of decode_workspace(kDecodeMaxT), 4.92 MB).  Every device
 // that loads the library holds this array until the process exits.
 constexpr size_t kNoAllocScratchBytes = 5 * 1024 * 1024;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
