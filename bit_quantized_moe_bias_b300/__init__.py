@@ -37,6 +37,11 @@ class ds4g_layer(C.Structure):
                 ("sh_up", C.c_void_p), ("sh_down", C.c_void_p), ("iq2_grid", C.c_void_p)]
 
 
+class ds4g_host_experts(C.Structure):
+    _fields_ = [("gate_up_type", C.c_int), ("down_type", C.c_int), ("gate", C.c_void_p),
+                ("up", C.c_void_p), ("down", C.c_void_p)]
+
+
 _lib = None
 _FWD_SIG = None
 
@@ -72,6 +77,14 @@ def lib():
             "ds4g_moe_decode_stack": ([vp, i, C.POINTER(vp), C.POINTER(vp), C.POINTER(ds4g_layer), vp, vp, vp, vp,
                                        vp, sz, vp], i),
             "ds4g_moe_forward_noalloc": ([vp, i, C.POINTER(ds4g_layer), vp, vp, vp, vp], i),
+            "ds4g_expert_cache_pool_bytes": ([i, i, i], sz),
+            "ds4g_expert_cache_create": ([i, i, i, i, vp, sz, C.POINTER(vp)], i),
+            "ds4g_expert_cache_destroy": ([vp], i),
+            "ds4g_expert_cache_stats": ([vp, C.POINTER(C.c_uint64), C.POINTER(C.c_uint64),
+                                         C.POINTER(C.c_uint64)], i),
+            "ds4g_moe_forward_streamed": ([vp, i, i, C.POINTER(ds4g_host_experts), vp, vp, vp, vp, vp, vp, vp, vp,
+                                           vp, sz, vp], i),
+            "ds4g_expert_lru_simulate": ([i, i, vp, vp, vp, vp], i),
             "ds4g_rmsnorm": ([vp, i, vp, vp], i),
             "ds4g_last_error": ([vp, vp], i),
         }
@@ -243,6 +256,87 @@ def ds4g_moe_forward_noalloc(hidden, layer: ds4g_layer, ids, w, out, stream=None
     _check("ds4g_moe_forward_noalloc",
            lib().ds4g_moe_forward_noalloc(_ptr(hidden), T, C.byref(layer), _ptr(ids), _ptr(w), _ptr(out),
                                           _stream(stream)))
+
+
+class HostExperts:
+    """Routed experts of one layer in host memory for ds4g_moe_forward_streamed:
+    gate/up/down map expert id -> packed bytes (uint8 tensors or arrays in
+    pinned host memory); missing ids are NULL."""
+
+    def __init__(self, gate, up, down, gate_up_type=DS4G_IQ2_XXS, down_type=DS4G_Q2_K):
+        self.keep = (gate, up, down)
+        tabs = []
+        for m in (gate, up, down):
+            arr = (C.c_void_p * N_EXPERT)()
+            for e, t in m.items():
+                arr[int(e)] = _ptr(t)
+            tabs.append(arr)
+        self.tabs = tabs
+        self.struct = ds4g_host_experts(gate_up_type, down_type, C.cast(tabs[0], C.c_void_p).value,
+                                        C.cast(tabs[1], C.c_void_p).value, C.cast(tabs[2], C.c_void_p).value)
+
+
+class ExpertCache:
+    """An HBM expert cache of n_slots slots (pool allocated here as a torch
+    tensor) for ds4g_moe_forward_streamed."""
+
+    def __init__(self, n_slots, max_tokens=1, gate_up_type=DS4G_IQ2_XXS, down_type=DS4G_Q2_K, device="cuda"):
+        import torch
+        nbytes = lib().ds4g_expert_cache_pool_bytes(gate_up_type, down_type, n_slots)
+        if nbytes == 0:
+            raise DS4GError("ds4g_expert_cache_pool_bytes", 1)
+        self.pool = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        h = C.c_void_p()
+        _check("ds4g_expert_cache_create",
+               lib().ds4g_expert_cache_create(gate_up_type, down_type, n_slots, max_tokens, self.pool.data_ptr(),
+                                              nbytes, C.byref(h)))
+        self.handle = h
+
+    def stats(self):
+        hits, misses, nbytes = C.c_uint64(), C.c_uint64(), C.c_uint64()
+        _check("ds4g_expert_cache_stats",
+               lib().ds4g_expert_cache_stats(self.handle, C.byref(hits), C.byref(misses), C.byref(nbytes)))
+        return hits.value, misses.value, nbytes.value
+
+    def close(self):
+        if self.handle is not None and self.handle.value:
+            _check("ds4g_expert_cache_destroy", lib().ds4g_expert_cache_destroy(self.handle))
+        self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def ds4g_moe_forward_streamed(hidden, layer_key, src: HostExperts, sh_gate, sh_up, sh_down, grid, ids, w, out,
+                              cache: ExpertCache, workspace, stream=None):
+    """ds4g_moe_forward whose routed experts are copied on demand from host
+    memory into the cache (blocks until the stream drains: ids are read back)."""
+    T = hidden.shape[0]
+    _check("ds4g_moe_forward_streamed",
+           lib().ds4g_moe_forward_streamed(_ptr(hidden), T, layer_key, C.byref(src.struct), _ptr(sh_gate),
+                                           _ptr(sh_up), _ptr(sh_down), _ptr(grid), _ptr(ids), _ptr(w), _ptr(out),
+                                           cache.handle, _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def ds4g_expert_lru_simulate(n_slots, calls):
+    """The cache's slot policy on the host: calls = list of key lists; returns
+    (slots, misses) lists of the same shape."""
+    sizes = np.array([len(c) for c in calls], np.int32)
+    keys = np.array([k for c in calls for k in c], np.int64)
+    slot = np.zeros(len(keys), np.int32)
+    miss = np.zeros(len(keys), np.uint8)
+    _check("ds4g_expert_lru_simulate",
+           lib().ds4g_expert_lru_simulate(n_slots, len(calls), sizes.ctypes.data, keys.ctypes.data,
+                                          slot.ctypes.data, miss.ctypes.data))
+    out_s, out_m, o = [], [], 0
+    for n in sizes:
+        out_s.append(slot[o:o + n].tolist())
+        out_m.append(miss[o:o + n].astype(bool).tolist())
+        o += n
+    return out_s, out_m
 
 
 def ds4g_rmsnorm(x, y, stream=None):

@@ -693,14 +693,15 @@ struct WsLayout {
     size_t cnt_gu, cnt_dn, part_r, part_s, hq, xs16, hsc16, hs, part_dr, part_ds, total;
 };
 
+// Tile counters at fixed offsets (sized for kDecodeMaxT tokens), scratch after.
+static_assert(((size_t)kK * kDecodeMaxT + 1) * kTilesGU * 4 + (size_t)kTilesDN * 4 <= kWsDecCntBytes,
+              "decode tile counters exceed their area");
 static WsLayout ws_layout(int T) {
     const size_t ns = (size_t)kK * T;
     WsLayout L;
-    size_t off = kWsHeader;
-    L.cnt_gu = off;
-    off += align_up((ns + 1) * kTilesGU * 4, 256);
-    L.cnt_dn = off;
-    off += align_up((size_t)kTilesDN * 4, 256);
+    L.cnt_gu = kWsDecCnt;
+    L.cnt_dn = kWsDecCnt + ((size_t)kK * kDecodeMaxT + 1) * kTilesGU * 4;
+    size_t off = kWsScratch;
     L.part_r = off;
     off += align_up(ns * kTilesGU * kSplitR * 32 * 4, 256);
     L.part_s = off;

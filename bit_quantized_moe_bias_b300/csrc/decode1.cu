@@ -1065,11 +1065,11 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
 struct D1Layout {
     size_t sync, logits, hr, h_s, p_s, p_r, total;
 };
+static_assert(sizeof(D1Sync) <= kWsD1SyncBytes, "coordination block exceeds its area");
 static D1Layout d1_layout() {
     D1Layout L;
-    size_t off = kWsHeader;
-    L.sync = off;
-    off += align_up(sizeof(D1Sync), 256);
+    L.sync = kWsD1Sync;
+    size_t off = kWsScratch;
     L.logits = off;
     off += align_up(kE * 4, 256);
     L.hr = off;

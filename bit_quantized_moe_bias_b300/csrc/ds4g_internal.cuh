@@ -53,6 +53,18 @@ __host__ __device__ inline int tile_block_bytes(int t) { return 16 * gguf_block_
 // ---------------------------------------------------------------------------
 constexpr size_t kWsHeader = 256;
 
+// Counter area of the forward family's workspaces (ds4g_moe_forward, the
+// fused layer kernel, the decode stack): after the status header come the
+// fused kernel's coordination block and the per-slot decode kernels' tile
+// counters, at the same offsets whatever T or path.  Every kernel leaves its
+// counters at zero, and no path writes scratch below kWsScratch, so one
+// zeroed workspace serves any sequence of calls and token counts.
+constexpr size_t kWsD1Sync = kWsHeader;                      // decode1.cu coordination block
+constexpr size_t kWsD1SyncBytes = 1280;
+constexpr size_t kWsDecCnt = kWsD1Sync + kWsD1SyncBytes;     // decode.cu tile counters
+constexpr size_t kWsDecCntBytes = 10752;
+constexpr size_t kWsScratch = kWsDecCnt + kWsDecCntBytes;    // first byte of any path's scratch
+
 __device__ inline void flag_status(uint32_t *ws_status, uint32_t code, uint32_t detail) {
     if (atomicCAS(ws_status, 0u, code) == 0u) ws_status[1] = detail;
 }

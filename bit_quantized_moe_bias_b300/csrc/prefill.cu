@@ -744,7 +744,7 @@ struct PFLayout {
 static PFLayout pf_layout(int T) {
     PFLayout L;
     const size_t nslot = (size_t)kK * T, nrow = nslot + T;
-    size_t off = kWsHeader;
+    size_t off = kWsScratch;   // the counter area below stays untouched
     L.counts = off;
     off += align_up(kE * 4, 256);
     L.offsets = off;

@@ -243,16 +243,21 @@ static size_t route_part_bytes(int T) {
     return T <= kRouteSmallT ? (size_t)kRouteKS * T * kE * 4 : (size_t)T * kE * 4;
 }
 
+// Ticket counters at a fixed offset, sized for DS4G_ROUTE_MAX_T tokens, so
+// that a workspace reused with another T never finds old partials where its
+// (zero) counters should be; partials after them.
+constexpr size_t kRouteCntBytes = ((size_t)(DS4G_ROUTE_MAX_T / kTileT + 1) * 4 + 255) / 256 * 256;
+
 extern "C" size_t ds4g_route_workspace(int T) {
-    if (T < 1) return 0;
-    const size_t ntile = (size_t)(T + kTileT - 1) / kTileT;
-    return kWsHeader + align_up(ntile * 4 + 4, 256) + align_up(route_part_bytes(T), 256);
+    if (T < 1 || T > DS4G_ROUTE_MAX_T) return 0;
+    return kWsHeader + kRouteCntBytes + align_up(route_part_bytes(T), 256);
 }
 
 extern "C" ds4g_status ds4g_moe_route(const float *hidden, int T, const float *router,
                                       const float *bias, int32_t *ids, float *w, void *workspace,
                                       size_t ws_bytes, ds4g_stream_t s) {
     if (!hidden || !router || !bias || !ids || !w || !workspace || T < 1) return DS4G_EINVAL;
+    if (T > DS4G_ROUTE_MAX_T) return DS4G_EUNSUPPORTED;
     if (((uintptr_t)hidden | (uintptr_t)router | (uintptr_t)bias | (uintptr_t)ids | (uintptr_t)w |
          (uintptr_t)workspace) & 15)
         return DS4G_EALIGN;
@@ -268,7 +273,7 @@ extern "C" ds4g_status ds4g_moe_route(const float *hidden, int T, const float *r
     a.status = (uint32_t *)ws;
     const size_t ntile = (size_t)(T + kTileT - 1) / kTileT;
     a.cnt = (uint32_t *)(ws + kWsHeader);
-    a.part = (float *)(ws + kWsHeader + align_up(ntile * 4 + 4, 256));
+    a.part = (float *)(ws + kWsHeader + kRouteCntBytes);
     cudaStream_t st = (cudaStream_t)s;
     if (T <= kRouteSmallT) {
         route_small_kernel<<<dim3(kE / 8, kRouteKS), 256, 0, st>>>(a);

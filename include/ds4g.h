@@ -140,8 +140,14 @@ ds4g_status ds4g_dequantize(ds4g_qtype t, const void *packed, int rows, int cols
  *   w[t][k] = s_{ids[t][k]} / sum_k' s_{ids[t][k']}
  * hidden [T][4096] f32 dev, router [256][4096] f32 dev, bias [256] f32 dev,
  * ids [T][6] int32 dev, w [T][6] f32 dev, workspace dev of at least
- * ds4g_route_workspace(T) bytes (holds the status word and the logits).
+ * ds4g_route_workspace(T) bytes (the status word, ticket counters and the
+ * logits), zeroed once before first use: the kernels leave the counters at
+ * zero, and they sit at the same offsets for every T, so one workspace
+ * serves calls with any T it is large enough for.
+ * 1 <= T <= DS4G_ROUTE_MAX_T, else DS4G_EINVAL / DS4G_EUNSUPPORTED
+ * (ds4g_route_workspace returns 0 outside that range).
  * ------------------------------------------------------------------------ */
+#define DS4G_ROUTE_MAX_T (1 << 20)
 size_t ds4g_route_workspace(int T);
 ds4g_status ds4g_moe_route(const float *hidden, int T, const float *router,
                            const float *bias, int32_t *ids, float *w,
@@ -208,7 +214,12 @@ typedef struct {
  *    down projection, bf16 throughout for the shared expert; fp32
  *    accumulation.  Expected error ~1e-3 relative L2 per token.
  * workspace dev >= ds4g_forward_workspace(T) bytes (about 200 KB per token
- * on the prefill path).
+ * on the prefill path), zeroed once before first use; one call at a time.
+ * Workspace reuse: every workspace of this family (ds4g_moe_forward,
+ * ds4g_moe_layer_decode, ds4g_moe_decode_stack) keeps its kernels' counters
+ * in one area at fixed offsets after the status word, which every kernel
+ * leaves at zero and no call uses as scratch; so one workspace, large enough
+ * for each call, serves any sequence of these calls and token counts.
  * ------------------------------------------------------------------------ */
 size_t ds4g_forward_workspace(int T);
 ds4g_status ds4g_moe_forward(const float *hidden, int T, const ds4g_layer *L,
@@ -324,6 +335,84 @@ ds4g_status ds4g_moe_decode_stack(const float *hidden, int n_layers, const float
 ds4g_status ds4g_moe_forward_noalloc(const float *hidden, int T, const ds4g_layer *L,
                                      const int32_t *ids, const float *w, float *out,
                                      ds4g_stream_t s);
+
+/* ------------------------------------------------------------------------
+ * Expert streaming: routed experts held in host memory, an HBM expert cache.
+ * [P1] §3.5 "SSD streaming" and the yudady DS-4 DwarfStar page, section
+ * "SSD Streaming": when the model does not fit the GPU's memory, the
+ * non-routed weights stay resident and a routed expert that misses the cache
+ * is loaded, used, and its space later released.  Here the routed experts of
+ * any number of layers live in host memory; a device pool of n_slots expert
+ * slots (gate + up + down of one expert each) keeps the most recently used
+ * ones, evicting the least recently used slot that the current call does not
+ * need; a slot is keyed by (layer_key, expert).
+ *
+ * ds4g_expert_cache_pool_bytes: device bytes of the pool for n_slots slots
+ *   of the type pair (the slots plus a 6 KB pointer table); 0 for an
+ *   unsupported pair or n_slots < 1.
+ * ds4g_expert_cache_create: pool dev, 16-byte aligned, >= pool_bytes, owned
+ *   by the caller and kept alive until destroy.  The cache object and two
+ *   small pinned host staging buffers are allocated here (create/destroy are
+ *   not hot calls).  max_tokens bounds T of the forwards.  Errors:
+ *   DS4G_EINVAL (NULL argument, n_slots < 6, max_tokens < 1 or > 2^20),
+ *   DS4G_EUNSUPPORTED (type pair), DS4G_EALIGN, DS4G_ENOSPACE (pool too
+ *   small), DS4G_ECUDA (staging allocation failed).
+ * ds4g_expert_cache_destroy: frees what create allocated (not the pool); no
+ *   forward using the cache may be in flight.
+ * ds4g_expert_cache_stats: since create, the distinct experts per call that
+ *   were resident (hits) or copied in (misses), and the bytes copied.
+ *
+ * ds4g_moe_forward_streamed: ds4g_moe_forward for T tokens of one layer whose
+ * routed experts come from host memory.
+ *   src->gate/up/down: host arrays [256] of host pointers to each expert's
+ *     packed matrices (layout of ds4g_quantize_pack; pinned memory, e.g. from
+ *     cudaHostAlloc, so that the copies are asynchronous); NULL for an expert
+ *     the caller does not provide.  Types must equal the cache's.
+ *   layer_key >= 0 names the layer in the cache's keys.
+ *   sh_*, iq2_grid (dev), hidden, ids, w, out, workspace as for
+ *     ds4g_moe_forward.
+ * Steps, on s: copy ids to the host and synchronise s (this also retires the
+ * kernels of every earlier call on s, so any slot may be rewritten); give
+ * each distinct selected expert its slot, copying those not resident (three
+ * cudaMemcpyAsync each); copy the pointer tables; run ds4g_moe_forward.
+ * Output bit-identical to ds4g_moe_forward with the same experts resident.
+ * Errors: T < 1 or > max_tokens, NULL argument, a selected expert whose host
+ * pointer is NULL: DS4G_EINVAL; more distinct experts than n_slots:
+ * DS4G_ENOSPACE; types differing from the cache's: DS4G_EUNSUPPORTED; then
+ * the errors of ds4g_moe_forward.  An id outside [0,256) is left to the
+ * kernels (DS4G_EDEVICE in the workspace).  The host blocks until s drains:
+ * use one stream for all calls on a cache.
+ *
+ * ds4g_expert_lru_simulate (exported for tests; no GPU): runs the cache's
+ * slot policy over n_calls calls of call_sizes[c] keys each (keys host
+ * int64, concatenated; < 0 = skipped) on n_slots empty slots and writes, per
+ * key, its slot (-1 for a skipped key) and 1 if it would be copied in; a
+ * call with more distinct keys than slots gets slot -2 for all its keys
+ * (the forward's DS4G_ENOSPACE) and the next call proceeds.
+ * ------------------------------------------------------------------------ */
+typedef struct ds4g_expert_cache ds4g_expert_cache;
+typedef struct {
+    ds4g_qtype gate_up_type;
+    ds4g_qtype down_type;
+    const void *const *gate;   /* host [256] of host pointers */
+    const void *const *up;
+    const void *const *down;
+} ds4g_host_experts;
+size_t ds4g_expert_cache_pool_bytes(ds4g_qtype gate_up_type, ds4g_qtype down_type, int n_slots);
+ds4g_status ds4g_expert_cache_create(ds4g_qtype gate_up_type, ds4g_qtype down_type, int n_slots,
+                                     int max_tokens, void *pool, size_t pool_bytes,
+                                     ds4g_expert_cache **cache);
+ds4g_status ds4g_expert_cache_destroy(ds4g_expert_cache *cache);
+ds4g_status ds4g_expert_cache_stats(const ds4g_expert_cache *cache, uint64_t *hits,
+                                    uint64_t *misses, uint64_t *bytes_copied);
+ds4g_status ds4g_moe_forward_streamed(const float *hidden, int T, int layer_key,
+                                      const ds4g_host_experts *src, const uint16_t *sh_gate,
+                                      const uint16_t *sh_up, const uint16_t *sh_down,
+                                      const uint64_t *iq2_grid, const int32_t *ids,
+                                      const float *w, float *out, ds4g_expert_cache *cache,
+                                      void *workspace, size_t ws_bytes, ds4g_stream_t s);
+ds4g_status ds4g_expert_lru_simulate(int n_slots, int n_calls, const int32_t *call_sizes,
+                                     const int64_t *keys, int32_t *slot_out, uint8_t *miss_out);
 
 /* RMS norm between chained layers (pages silent; reading: eps = 1e-6, no
  * learned gain): y[t] = x[t] / sqrt(mean_j x[t][j]^2 + 1e-6).  In place

@@ -8,7 +8,7 @@ import pytest
 
 import oracle
 import synth
-from helpers import (E, H, K, assert_close_fwd, check_route, device_layer, grid_u64,
+from helpers import (E, H, K, FullLayer, assert_close_fwd, check_route, device_layer, grid_u64,
                      oracle_forward)
 
 torch = pytest.importorskip("torch")
@@ -248,3 +248,55 @@ def test_forward_decode_h_beyond_fp16_range(gut, dt):
     got, st = _forward_gpu(x, ids, w, L)
     assert st == 0
     assert_close_fwd(got, oracle_forward(x, ids, w, hx, shared, grid, gut, dt))
+
+
+def test_workspace_reused_across_T_and_paths():
+    """One zeroed workspace serves forward calls of any T (decode chunks and
+    the prefill path) and the fused layer kernel, in any order: each result
+    equals the same call on a fresh workspace bit for bit (the counters sit
+    at fixed offsets that no call uses as scratch)."""
+    experts = [2, 9, 31, 64, 100, 150, 151, 199, 230, 255]
+    rng = np.random.default_rng(8)
+    Tmax = 64
+    x = synth.hidden(5, 0, Tmax)
+    ids = np.stack([rng.choice(experts, K, replace=False) for _ in range(Tmax)]).astype(np.int32)
+    w = rng.dirichlet(np.ones(K), Tmax).astype(np.float32)
+    L = FullLayer(5, 0, 0).L            # all 256 experts, generated on the device
+    xd, idd, wd = _t(x), _t(ids), _t(w)
+    R, b = synth.router(5, 0), synth.bias_normal(5, 0)
+    ws = B.workspace(max(B.ds4g_forward_workspace(Tmax), B.ds4g_layer_decode_workspace()))
+
+    def fwd(T, wsp):
+        out = torch.full((T, H), float("nan"), device=DEV)
+        B.ds4g_moe_forward(xd[:T], L.struct, idd[:T], wd[:T], out, wsp)
+        assert B.ds4g_last_error(wsp) == 0
+        return out.cpu().numpy()
+
+    def layer(wsp):
+        i1 = torch.full((K,), -1, dtype=torch.int32, device=DEV)
+        w1 = torch.zeros(K, device=DEV)
+        o1 = torch.full((H,), float("nan"), device=DEV)
+        B.ds4g_moe_layer_decode(xd[0], _t(R), _t(b), L.struct, i1, w1, o1, wsp)
+        assert B.ds4g_last_error(wsp) == 0
+        return i1.cpu().numpy(), w1.cpu().numpy(), o1.cpu().numpy()
+
+    for T in [1, 2, 3, 64, 2, 5, 1, 64, 3]:
+        got = fwd(T, ws)
+        ref = fwd(T, B.workspace(B.ds4g_forward_workspace(T)))
+        assert np.array_equal(got, ref), f"T={T}"
+        if T == 64:
+            # the fused layer kernel on the same workspace, then forward again
+            a, c = layer(ws), layer(B.workspace(B.ds4g_layer_decode_workspace()))
+            assert all(np.array_equal(u, v) for u, v in zip(a, c))
+    # the router's workspace across T, past 64 tiles of 32 tokens
+    xr = _t(synth.hidden(5, 0, 2100))
+    Rd, bd = _t(R), _t(b)
+    rws = B.workspace(B.ds4g_route_workspace(2100))
+    for T in [1, 2100, 5, 2100, 1]:
+        outs = []
+        for wsp in (rws, B.workspace(B.ds4g_route_workspace(T))):
+            i = torch.full((T, K), -1, dtype=torch.int32, device=DEV)
+            ww = torch.zeros(T, K, device=DEV)
+            B.ds4g_moe_route(xr[:T], Rd, bd, i, ww, wsp)
+            outs.append((i.cpu().numpy(), ww.cpu().numpy()))
+        assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1]), f"route T={T}"
