@@ -100,14 +100,6 @@ struct GUSmem {
     __nv_bfloat16 *xb;  // [T][2][4096] activation bf16 (hi, lo)
 };
 
-// Exponent e >= 0 such that every |h| <= m of a group, scaled by 2^-e, is
-// below 2^15 (then its fp16 hi/lo pair is exact to ~2^-22 of the group's
-// largest value); e = 0 when m < 2^15.
-__device__ __forceinline__ int h_group_exp(float m) {
-    const int E = (int)((__float_as_uint(m) >> 23) & 255u) - 126;   // m < 2^E for normal m
-    return E > 15 ? E - 15 : 0;
-}
-
 // Reduction of one (slot, tile) of routed gate/up: 8 split partials in fixed
 // order -> h = silu(g) * u; the 16 values, scaled by a power of two 2^-e
 // shared by the tile (so that any finite h fits the fp16 range), as fp16
@@ -133,7 +125,7 @@ __device__ __forceinline__ void gu_routed_finish(const DecodeArgs &a, int slot, 
     const int b = tile >> 4, j = tile & 15;
     if (lane < 16) {
         __half hi, lo;
-        split_f16(h * __uint_as_float((uint32_t)(127 - e) << 23), hi, lo);
+        split_f16(h * pow2f(-e), hi, lo);
         a.hq[((size_t)slot * 2 + 0) * kF + tile * 16 + lane] = hi;
         a.hq[((size_t)slot * 2 + 1) * kF + tile * 16 + lane] = lo;
     }
@@ -142,7 +134,7 @@ __device__ __forceinline__ void gu_routed_finish(const DecodeArgs &a, int slot, 
     for (int off = 8; off > 0; off >>= 1) h += __shfl_xor_sync(0xffffffffu, h, off);
     if (lane == 0) {
         a.xs16[(size_t)slot * 128 + (b * 4 + (j & 3)) * 4 + (j >> 2)] = h;
-        a.hsc16[(size_t)slot * 128 + (b * 4 + (j & 3)) * 4 + (j >> 2)] = __uint_as_float((uint32_t)(127 + e) << 23);
+        a.hsc16[(size_t)slot * 128 + (b * 4 + (j & 3)) * 4 + (j >> 2)] = pow2f(e);
     }
 }
 

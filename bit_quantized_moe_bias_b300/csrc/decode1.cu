@@ -62,8 +62,8 @@ constexpr int kGW = 4;                           // warps per group
 constexpr int kD1Cons = kNGrp * kGW;             // 16 consumer warps
 constexpr int kD1Threads = (2 + kD1Cons) * 32;   // producer + control + consumers
 constexpr int kRdnW = 8 * kTB_Q2K;               // routed down piece: 16 rows x 2048 (10.5 KB)
-constexpr int kHSlot = 2 * kF * 2 + 128 * 4;     // routed h of one slot: fp16 hi, lo, 16-col sums
-constexpr int kD1Slot = kRdnW + kHSlot;          // 19456 B: the largest piece
+constexpr int kHSlot = 2 * kF * 2 + 2 * 128 * 4; // routed h of one slot: fp16 hi, lo, 16-col sums, scales
+constexpr int kD1Slot = kRdnW + kHSlot;          // 19968 B: the largest piece
 static_assert(kD1Slot >= 16 * kTB_IQ2 && kD1Slot >= 4 * kH && (kD1Slot % 128) == 0, "slot size");
 constexpr int kSlotsPerGrp = 2;                  // one piece in flight while one is computed
 constexpr int kD1Slots = kNGrp * kSlotsPerGrp;   // 8
@@ -118,7 +118,7 @@ struct D1Args {
     uint32_t *status;
     D1Sync *sync;
     float *logits;         // [256]
-    uint8_t *hr;           // [6][kHSlot]: fp16 h hi [2048], lo [2048], 16-col sums [128] (fp32)
+    uint8_t *hr;           // [6][kHSlot]: fp16 h hi [2048], lo [2048], 16-col sums [128], scales [128] (fp32)
     float *h_s;            // [2048]
     float *p_s;            // [4096] shared-expert output
     float *p_r;            // [6][4096] weighted routed outputs
@@ -425,9 +425,10 @@ __device__ __forceinline__ void iq2_tileblock2(const D1Smem &sm, const uint8_t *
 }
 
 // One Q2_K tile-block (16 rows x 256 cols), block column b, against h (fp16
-// hi at hq, lo at hq + 2048) and its 16-column sums xs (permuted: sub-block
-// j16 = 4G + t of block b at (4b + t) * 4 + G).  Returns this lane's partial
-// for rows g and g+8 (the quad's four lanes sum to the rows).
+// hi at hq, lo at hq + 2048, each 16 entries scaled by 2^-e), its 16-column
+// sums xs and the scales 2^e at xs + 128 (both permuted: sub-block j16 =
+// 4G + t of block b at (4b + t) * 4 + G).  Returns this lane's partial for
+// rows g and g+8 (the quad's four lanes sum to the rows).
 __device__ __forceinline__ void q2k_tileblock(const uint8_t *tb, const __half *hq, const float *xs, int b, int lane,
                                               float &s0, float &s1) {
     const int g = lane >> 2, t = lane & 3;
@@ -439,6 +440,7 @@ __device__ __forceinline__ void q2k_tileblock(const uint8_t *tb, const __half *h
     const uint2 dd = *reinterpret_cast<const uint2 *>(tb + 1280 + 8 * g);
     const __half *hrow = hq + (g & 1) * kF + 256 * b + 16 * t;
     const float4 X = *reinterpret_cast<const float4 *>(xs + (b * 4 + t) * 4);
+    const float4 S = *reinterpret_cast<const float4 *>(xs + 128 + (b * 4 + t) * 4);
     const float dg = __half2float(__ushort_as_half((unsigned short)(dd.x & 0xffff))) * 16777216.0f;
     const float mg = __half2float(__ushort_as_half((unsigned short)(dd.x >> 16)));
     const float dh = __half2float(__ushort_as_half((unsigned short)(dd.y & 0xffff))) * 16777216.0f;
@@ -446,6 +448,7 @@ __device__ __forceinline__ void q2k_tileblock(const uint8_t *tb, const __half *h
     const uint32_t Wa[4] = {qa.x, qa.y, qa.z, qa.w};
     const uint32_t Wb[4] = {qb.x, qb.y, qb.z, qb.w};
     const float Xg[4] = {X.x, X.y, X.z, X.w};
+    const float Sg[4] = {S.x, S.y, S.z, S.w};
     float sg = 0.f, sh = 0.f;
 #pragma unroll
     for (int G = 0; G < 4; ++G) {
@@ -469,8 +472,8 @@ __device__ __forceinline__ void q2k_tileblock(const uint8_t *tb, const __half *h
             for (int i = 0; i < 4; ++i) r[i] = fmaf(c[i], f, r[i]);
         }
         const uint32_t ba = (sca >> (8 * G)) & 0xffu, bb = (scb >> (8 * G)) & 0xffu;
-        sg += dg * small_u2f(ba & 15u) * (r[0] + r[1]) - mg * small_u2f(ba >> 4) * Xg[G];
-        sh += dh * small_u2f(bb & 15u) * (r[2] + r[3]) - mh * small_u2f(bb >> 4) * Xg[G];
+        sg += dg * small_u2f(ba & 15u) * ((r[0] + r[1]) * Sg[G]) - mg * small_u2f(ba >> 4) * Xg[G];
+        sh += dh * small_u2f(bb & 15u) * ((r[2] + r[3]) * Sg[G]) - mh * small_u2f(bb >> 4) * Xg[G];
     }
     s0 = sg;
     s1 = sh;
@@ -991,28 +994,37 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
                     __syncwarp();
                     if (lane == 0) red_add_release(&a.sync->sgu_done, 1u);
                 } else if (d.kind == PK_RGU) {
-                    // h of 16 rows of slot k: fp16 hi/lo and the 16-column sum the
-                    // Q2_K down needs, where the routed-down pieces copy them from
+                    // h of 16 rows of slot k: fp16 hi/lo of 2^-e h (one power of two
+                    // per 16 entries, so any finite h fits), the 16-column sum of h
+                    // the Q2_K down needs, and 2^e, where the routed-down pieces
+                    // copy them from
                     const int k = d.job / (kF / 16), tl = d.job % (kF / 16);
                     float hv = 0.f;
                     if (lane < 16) {
                         const float gs = (red[lane] + red[16 + lane]) + (red[32 + lane] + red[48 + lane]);
                         const float us = (red[64 + lane] + red[80 + lane]) + (red[96 + lane] + red[112 + lane]);
                         hv = silu_f(gs) * us;
-                        if (!(fabsf(hv) < 65504.f)) flag_status(a.status, DS4G_EDEVICE, 0xF16u);
+                        if (!(fabsf(hv) <= 3.4028235e38f)) flag_status(a.status, DS4G_EDEVICE, 0xF16u);
+                    }
+                    float sum = hv, m = fabsf(hv);
+#pragma unroll
+                    for (int o = 1; o < 16; o <<= 1) {
+                        sum += __shfl_xor_sync(0xffffffffu, sum, o);
+                        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                    }
+                    const int e = h_group_exp(m);
+                    if (lane < 16) {
                         __half hi, lo;
-                        split_f16(hv, hi, lo);
+                        split_f16(hv * pow2f(-e), hi, lo);
                         __half *hq = reinterpret_cast<__half *>(a.hr + (size_t)k * kHSlot);
                         hq[16 * tl + lane] = hi;
                         hq[kF + 16 * tl + lane] = lo;
                     }
-                    float sum = hv;
-#pragma unroll
-                    for (int o = 1; o < 16; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
                     if (lane == 0) {
                         const int b = tl >> 4, j16 = tl & 15;
                         float *xs = reinterpret_cast<float *>(a.hr + (size_t)k * kHSlot + 4 * kF);
                         xs[(b * 4 + (j16 & 3)) * 4 + (j16 >> 2)] = sum;
+                        xs[128 + (b * 4 + (j16 & 3)) * 4 + (j16 >> 2)] = pow2f(e);
                     }
                     __syncwarp();
                     if (lane == 0) red_add_release(&a.sync->rgu_done[k], 1u);

@@ -159,4 +159,14 @@ __device__ __forceinline__ void split_bf16(float x, __nv_bfloat16 &hi, __nv_bflo
 
 __device__ __forceinline__ float silu_f(float v) { return v / (1.0f + expf(-v)); }
 
+// Exponent e >= 0 such that every |h| <= m of a group, scaled by 2^-e, is
+// below 2^15 (then its fp16 hi/lo pair is exact to ~2^-22 of the group's
+// largest value); e = 0 when m < 2^15.  The routed h of the decode paths is
+// stored as 2^-e * h per 16 entries, with 2^e beside it.
+__device__ __forceinline__ int h_group_exp(float m) {
+    const int E = (int)((__float_as_uint(m) >> 23) & 255u) - 126;   // m < 2^E for normal m
+    return E > 15 ? E - 15 : 0;
+}
+__device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
+
 }  // namespace ds4g

@@ -255,8 +255,10 @@ ds4g_status ds4g_moe_down(const float *hidden, int T, const ds4g_layer *L,
  * Arithmetic as the decode path of ds4g_moe_forward, except that the shared
  * expert is summed in fp32 FMA.  workspace dev >= ds4g_layer_decode_workspace()
  * bytes, zeroed once before first use (the kernel leaves its counters at
- * zero); one call at a time per workspace.  Kernel-detected faults (bad
- * expert id, |xn| or |h| >= 65504, a bounded wait that expired) are read
+ * zero); one call at a time per workspace.  h enters the down projection
+ * as an fp16 hi+lo pair scaled by a power of two per 16 entries (any finite
+ * h).  Kernel-detected faults (bad expert id, |xn| >= 65504, a non-finite h,
+ * a bounded wait that expired) are read
  * back with ds4g_last_error(workspace); so is an IQ2_XXS grid byte outside
  * {8, 25, 43}, the format's magnitudes (DS4G_EUNSUPPORTED: this kernel
  * encodes grid rows as 2-bit codes of those values).

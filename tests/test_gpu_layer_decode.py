@@ -207,3 +207,20 @@ def test_decode_stack_q2_q4_layers():
         xl = o1
     assert np.array_equal(xl.cpu().numpy()[0], out_s)
     assert B.ds4g_last_error(wsl) == 0 and B.ds4g_last_error(fws) == 0
+
+
+def test_layer_decode_h_beyond_fp16_range():
+    """An input for which h = silu(g) * u reaches ~3e6 (far beyond fp16):
+    the fused kernel carries h with a power-of-two scale per 16 entries, so
+    no flag and oracle parity."""
+    rng = np.random.default_rng(11)
+    x = (60.0 * rng.standard_normal((1, H))).astype(np.float32)
+    R, b = synth.router(6, 4), synth.bias_normal(6, 4)
+    ids_r, w_r, keys, margin = oracle.route(x, R, b)
+    assert margin[0] > 1e-3
+    L, hx, shared, grid = device_layer(6, 4, 5, ids_r.reshape(-1))
+    ws = B.workspace(B.ds4g_layer_decode_workspace())
+    ids, w, out, st = _run(x[0], R, b, L, ws, normalize=False)
+    assert st == 0
+    check_route(ids[None], w[None], ids_r, w_r, keys, margin)
+    assert_close_fwd(out[None], oracle_forward(x, ids[None], w[None], hx, shared, grid))
