@@ -25,9 +25,9 @@
 //    logits are stored and computes the top-6 itself (the pointer tables of
 //    its 8 experts per lane are already in registers);
 //  - routed h of slot k: complete when its 128 gate/up tiles are stored; each
-//    routed-down piece carries a copy of that h (fp16 hi/lo + 16-column
-//    sums, written by the gate/up jobs) next to its weights, so no CTA-wide
-//    transition is needed;
+//    routed-down piece carries a copy of that h (fp16 hi/lo scaled by a power
+//    of two per 16 entries, the 16-column sums and the scales, written by the
+//    gate/up jobs) next to its weights, so no CTA-wide transition is needed;
 //  - shared h: complete when its 1024 row pairs are stored; the control warp
 //    then copies it once into the CTA (over the activation, which every job
 //    that reads it has finished by then);
@@ -48,8 +48,8 @@
 // Arithmetic: router and shared expert in fp32 FMA (bf16 weights widen
 // exactly); routed experts on mma.sync with exact codes (IQ2 grid value or
 // Q2_K quant as an fp16 subnormal, sign from the sign table) against the
-// activation as an fp16 hi + lo pair; block and sub-block scales applied in
-// fp32 to each 32- or 16-column partial.  The IQ2_XXS grid values must lie in
+// activation as an fp16 hi + lo pair (h: scaled per 16 entries); block,
+// sub-block and h scales applied in fp32 to each 32- or 16-column partial.  The IQ2_XXS grid values must lie in
 // {8, 25, 43} (the format's magnitudes): the grid table holds, per row, 8
 // nibble codes that select the value bytes with one byte permute.
 #include "ds4g_internal.cuh"
