@@ -242,6 +242,19 @@ __device__ __forceinline__ bool d1_wait(uint64_t *bar, uint32_t parity, volatile
     }
 }
 
+// Bounded wait for one barrier phase before the CTA exits.  It ignores the
+// abort flag: a bulk copy still in flight must land before the CTA's shared
+// memory is released.  Gives up after ~1 s and records DS4G_ETIMEOUT.
+__device__ __forceinline__ void d1_drain(const D1Args &a, uint64_t *bar, uint32_t parity, uint32_t where) {
+    const long long t0 = clock64();
+    while (!tc::mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > (2ll << 30)) {
+            flag_status(a.status, DS4G_ETIMEOUT, where);
+            return;
+        }
+    }
+}
+
 __device__ __forceinline__ void d1_abort(const D1Args &a, int *abort_flag, uint32_t where) {
     atomicExch(abort_flag, 1);
     flag_status(a.status, DS4G_ETIMEOUT, where);
@@ -743,6 +756,7 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
                 if (p == -2) {
                     sm.desc[s].kind = PK_END;
                     tc::mbar_arrive(&sm.full[s]);
+                    ++itq;   // a use of slot s like any piece (the drain below counts it)
                     break;
                 }
                 if (p < 0) {
@@ -811,10 +825,23 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
                 pend_j = j;
                 t_idle = clock64();
             }
+            // The last piece issued into each of the group's slots has landed
+            // (already so when the group consumed everything; after an abort
+            // this keeps copies from writing shared memory after exit).
+            for (uint32_t u = 0; u < (uint32_t)kSlotsPerGrp; ++u) {
+                if (itq <= u) continue;   // slot never used
+                const uint32_t last = itq - 1 - (itq - 1 - u) % kSlotsPerGrp;
+                d1_drain(a, &sm.full[kSlotsPerGrp * q + (int)u], (last / kSlotsPerGrp) & 1u, 0x40u + q);
+            }
         }
     } else if (warp == 1) {
         // ================================================== control warp
         d1_control(a, sm, lane);
+        // its copies (the activation; the shared h once issued) have landed
+        if (lane == 0) {
+            d1_drain(a, sm.xbar, 0, 0x44u);
+            if (*reinterpret_cast<volatile int *>(&sm.flags[2])) d1_drain(a, sm.hsbar, 0, 0x45u);
+        }
     } else {
         // ================================================== consumers
         const int cw = warp - 2, ct = tid - 64;
