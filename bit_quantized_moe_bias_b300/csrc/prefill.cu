@@ -82,6 +82,7 @@ struct PFSmem {
     uint64_t *full_a, *full_b, *empty, *acc_full, *acc_empty;
     uint32_t *tmem_base;
     int *abort_flag;
+    uint64_t *drain;       // the MMA thread's final commit: all its MMAs complete
 };
 
 constexpr size_t kSmemTables = 256 * 8 * 16 + 128 * 8 * 16 + 1040;   // 48 KB of tables + task prefix
@@ -109,6 +110,7 @@ __device__ __forceinline__ PFSmem carve(uint8_t *raw) {
     p += (3 * kStages + 4) * 8;
     s.tmem_base = (uint32_t *)p;
     s.abort_flag = (int *)(p + 4);
+    s.drain = (uint64_t *)(p + 8);
     return s;
 }
 
@@ -155,6 +157,19 @@ __device__ __noinline__ bool pf_wait(uint64_t *bar, uint32_t parity, volatile in
             if (tc::mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
         if (clock64() - t0 > (4ll << 30)) return false;  // ~2 s at 2 GHz
+    }
+}
+
+// Bounded wait for one barrier phase at teardown.  It ignores the abort
+// flag: a TMA load or an MMA still in flight must finish before the CTA
+// releases its shared memory and TMEM.  Gives up after ~2 s (DS4G_ETIMEOUT).
+__device__ __forceinline__ void pf_drain(const PFArgs &a, uint64_t *bar, uint32_t parity, uint32_t where) {
+    const long long t0 = clock64();
+    while (!tc::mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > (4ll << 30)) {
+            flag_status(a.status, DS4G_ETIMEOUT, where);
+            return;
+        }
     }
 }
 
@@ -364,6 +379,7 @@ __global__ void __launch_bounds__(kPFThreads, 1)
             tc::mbar_init(&sm.acc_full[i], 1);
             tc::mbar_init(&sm.acc_empty[i], 4);
         }
+        tc::mbar_init(sm.drain, 1);
         *sm.abort_flag = 0;
         tc::fence_mbar_init();
         tc::prefetch_tmap(&tmB16);
@@ -482,6 +498,14 @@ __global__ void __launch_bounds__(kPFThreads, 1)
                     }
                 }
             }
+            // the last load issued into each stage has landed (already so when
+            // the MMA thread consumed everything; after an abort this keeps
+            // loads from writing shared memory after exit)
+            for (uint32_t u = 0; u < (uint32_t)kStages; ++u) {
+                if (it <= u) continue;   // stage never used
+                const uint32_t last = it - 1 - (it - 1 - u) % kStages;
+                pf_drain(a, &sm.full_b[u], (last / kStages) & 1u, 0x500u + u);
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
@@ -523,6 +547,9 @@ __global__ void __launch_bounds__(kPFThreads, 1)
                 if (!ok) break;
                 tc::mma_commit(&sm.acc_full[ab]);
             }
+            // every MMA issued here has completed before TMEM is released
+            tc::mma_commit(sm.drain);
+            pf_drain(a, sm.drain, 0, 0x600u);
         }
     } else if (warp < 6) {
         // --------------------------------------------------------- epilogue
