@@ -595,10 +595,11 @@ def _cached(key, fn):
     return _CACHE[key]
 
 
-def oracle_sample(nlayers):
+def oracle_sample(nlayers, nthreads=0):
     """Oracle on 1 token through the first `nlayers` layers of the config-1
-    chain; returns (seconds of oracle compute, threads).  Generating the
-    synthetic weights is not timed (and is cached between samples)."""
+    chain with `nthreads` OpenMP threads (0 = all cores); returns (seconds of
+    oracle compute, threads).  Generating the synthetic weights is not timed
+    (and is cached between samples)."""
     import oracle
     x = synth.hidden(SEED, CFG, 1, layer=999, normalise=False)
     grid = synth.iq2_grid(SEED)
@@ -614,17 +615,32 @@ def oracle_sample(nlayers):
         for e in ids[0]:
             gate[e], up[e], down[e] = _cached(("X", l, int(e)), lambda: synth.expert(SEED, CFG, l, int(e)))
         t0 = time.perf_counter()
-        x = oracle.moe_forward(xn, ids, w, gate, up, down, *sh, grid)
+        x = oracle.moe_forward(xn, ids, w, gate, up, down, *sh, grid, nthreads=nthreads)
         t += time.perf_counter() - t0
-    return t, os.cpu_count()
+    return t, (nthreads or os.cpu_count())
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or "unknown"
 
 
 def cpu_baseline(nlayers):
     t, cores = oracle_sample(nlayers)
     per_token = t * NLAYER / nlayers
+    t1, _ = oracle_sample(1, nthreads=1)          # the same oracle on one core: its first layer
     return {"value": round(1.0 / per_token, 5), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "value_1thread": round(1.0 / (t1 * NLAYER), 5), "cpu_model": cpu_model(),
             "sample": f"1 token through the first {nlayers} of {NLAYER} layers (oracle rmsnorm + route + "
-                      f"forward, fp64, OpenMP over rows), extrapolated linearly to {NLAYER} layers"}
+                      f"forward, fp64, OpenMP over rows), extrapolated linearly to {NLAYER} layers; "
+                      f"value_1thread: its first layer on one thread, extrapolated to {NLAYER}"}
 
 
 def run_reference(args):
