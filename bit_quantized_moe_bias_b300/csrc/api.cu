@@ -105,22 +105,26 @@ static ds4g_status run_forward(const float *hidden, int T, const ds4g_layer *L, 
 extern "C" ds4g_status ds4g_moe_forward(const float *hidden, int T, const ds4g_layer *L,
                                         const int32_t *ids, const float *w, float *out,
                                         void *workspace, size_t ws_bytes, ds4g_stream_t s) {
+    DS4G_TRACE();
     return run_forward(hidden, T, L, ids, w, out, workspace, ws_bytes, s, 3);
 }
 
 extern "C" ds4g_status ds4g_moe_gate_up(const float *hidden, int T, const ds4g_layer *L,
                                         const int32_t *ids, const float *w, float *out,
                                         void *workspace, size_t ws_bytes, ds4g_stream_t s) {
+    DS4G_TRACE();
     return run_forward(hidden, T, L, ids, w, out, workspace, ws_bytes, s, 1);
 }
 
 extern "C" ds4g_status ds4g_moe_down(const float *hidden, int T, const ds4g_layer *L,
                                      const int32_t *ids, const float *w, float *out,
                                      void *workspace, size_t ws_bytes, ds4g_stream_t s) {
+    DS4G_TRACE();
     return run_forward(hidden, T, L, ids, w, out, workspace, ws_bytes, s, 2);
 }
 
 extern "C" ds4g_status ds4g_rmsnorm(const float *x, int T, float *y, ds4g_stream_t s) {
+    DS4G_TRACE();
     if (!x || !y || T < 1) return DS4G_EINVAL;
     if (((uintptr_t)x | (uintptr_t)y) & 15) return DS4G_EALIGN;
     rmsnorm_kernel<<<T, 256, 0, (cudaStream_t)s>>>(x, y);

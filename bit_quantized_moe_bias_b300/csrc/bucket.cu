@@ -87,6 +87,7 @@ extern "C" size_t ds4g_bucket_workspace(int T) { return T < 1 ? 0 : kWsHeader; }
 extern "C" ds4g_status ds4g_moe_bucket(const int32_t *ids, int T, int32_t *counts, int32_t *offsets,
                                        int32_t *perm, int32_t *inv, void *workspace, size_t ws_bytes,
                                        ds4g_stream_t s) {
+    DS4G_TRACE();
     if (!ids || !counts || !offsets || !perm || !inv || !workspace || T < 1) return DS4G_EINVAL;
     if (((uintptr_t)ids | (uintptr_t)counts | (uintptr_t)offsets | (uintptr_t)perm | (uintptr_t)inv |
          (uintptr_t)workspace) & 15)

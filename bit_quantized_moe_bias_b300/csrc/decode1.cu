@@ -1289,6 +1289,7 @@ extern "C" size_t ds4g_decode_stack_workspace(void) { return stack_layout().tota
 extern "C" ds4g_status ds4g_moe_layer_decode(const float *hidden, int normalize, const float *router,
                                              const float *bias, const ds4g_layer *L, int32_t *ids, float *w,
                                              float *out, void *workspace, size_t ws_bytes, ds4g_stream_t s) {
+    DS4G_TRACE();
     ds4g_status st = d1_check(hidden, router, bias, L, ids, w, out, workspace, ws_bytes);
     if (st != DS4G_OK) return st;
     if (((uintptr_t)ids | (uintptr_t)w) & 15) return DS4G_EALIGN;
@@ -1300,6 +1301,7 @@ extern "C" ds4g_status ds4g_moe_decode_stack(const float *hidden, int n_layers, 
                                              const float *const *biases, const ds4g_layer *layers, int32_t *ids,
                                              float *w, float *hbuf, float *out, void *workspace, size_t ws_bytes,
                                              ds4g_stream_t s) {
+    DS4G_TRACE();
     if (n_layers < 1 || n_layers > 1024 || !routers || !biases || !layers || !hbuf || !ids || !w) return DS4G_EINVAL;
     if (((uintptr_t)hbuf | (uintptr_t)ids | (uintptr_t)w) & 15) return DS4G_EALIGN;
     for (int l = 0; l < n_layers; ++l) {

@@ -91,6 +91,7 @@ using namespace ds4g;
 extern "C" ds4g_status ds4g_dequantize(ds4g_qtype t, const void *packed, int rows, int cols,
                                        const uint64_t *iq2_grid, float *out_f32, uint16_t *out_bf16,
                                        ds4g_stream_t s) {
+    DS4G_TRACE();
     if (!packed || (!out_f32 && !out_bf16)) return DS4G_EINVAL;
     if (t != DS4G_IQ2_XXS && t != DS4G_Q2_K && t != DS4G_Q4_K) return DS4G_EINVAL;
     if (t == DS4G_IQ2_XXS && !iq2_grid) return DS4G_EINVAL;

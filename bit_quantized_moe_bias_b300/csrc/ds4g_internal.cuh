@@ -5,6 +5,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include "../../include/ds4g.h"
@@ -70,6 +71,17 @@ __device__ inline void flag_status(uint32_t *ws_status, uint32_t code, uint32_t 
 }
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Tracing: every GPU entry point opens an NVTX range named after itself, so
+// its launches group under that name in a profiler's timeline (Nsight
+// Systems / Compute); with no tool attached a range costs a few nanoseconds.
+struct TraceRange {
+    explicit TraceRange(const char *name) { nvtxRangePushA(name); }
+    ~TraceRange() { nvtxRangePop(); }
+    TraceRange(const TraceRange &) = delete;
+    TraceRange &operator=(const TraceRange &) = delete;
+};
+#define DS4G_TRACE() ::ds4g::TraceRange ds4g_trace_range_(__func__)
 
 // Decode path of the MoE block (decode.cu, 1 <= T <= 64): workspace bytes,
 // and the launch of its kernels (phases: 1 gate/up, 2 down, 3 both).

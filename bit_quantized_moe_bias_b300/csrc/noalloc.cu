@@ -40,6 +40,7 @@ using namespace ds4g;
 extern "C" ds4g_status ds4g_moe_forward_noalloc(const float *hidden, int T, const ds4g_layer *L,
                                                 const int32_t *ids, const float *w, float *out,
                                                 ds4g_stream_t s) {
+    DS4G_TRACE();
     if (!hidden || !L || !ids || !w || !out || T < 1) return DS4G_EINVAL;
     if (T > DS4G_NOALLOC_MAX_T) return DS4G_ENOSPACE;
     if (!L->gate || !L->up || !L->down || !L->sh_gate || !L->sh_up || !L->sh_down) return DS4G_EINVAL;

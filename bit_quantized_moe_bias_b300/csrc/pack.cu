@@ -194,6 +194,7 @@ extern "C" ds4g_status ds4g_unpack(ds4g_qtype t, int rows, int cols, const void 
 extern "C" ds4g_status ds4g_quantize_pack_device(ds4g_qtype t, int rows, int cols,
                                                  const void *gguf_dev, void *packed_dev,
                                                  ds4g_stream_t s) {
+    DS4G_TRACE();
     if (!gguf_dev || !packed_dev) return DS4G_EINVAL;
     if (t != DS4G_IQ2_XXS && t != DS4G_Q2_K && t != DS4G_Q4_K) return DS4G_EINVAL;
     if (!shape_ok(t, rows, cols)) return DS4G_EUNSUPPORTED;

@@ -256,6 +256,7 @@ extern "C" size_t ds4g_route_workspace(int T) {
 extern "C" ds4g_status ds4g_moe_route(const float *hidden, int T, const float *router,
                                       const float *bias, int32_t *ids, float *w, void *workspace,
                                       size_t ws_bytes, ds4g_stream_t s) {
+    DS4G_TRACE();
     if (!hidden || !router || !bias || !ids || !w || !workspace || T < 1) return DS4G_EINVAL;
     if (T > DS4G_ROUTE_MAX_T) return DS4G_EUNSUPPORTED;
     if (((uintptr_t)hidden | (uintptr_t)router | (uintptr_t)bias | (uintptr_t)ids | (uintptr_t)w |

@@ -204,6 +204,7 @@ extern "C" ds4g_status ds4g_moe_forward_streamed(const float *hidden, int T, int
                                                  const uint64_t *iq2_grid, const int32_t *ids, const float *w,
                                                  float *out, ds4g_expert_cache *c, void *workspace,
                                                  size_t ws_bytes, ds4g_stream_t s) {
+    DS4G_TRACE();
     if (!c || !src || !src->gate || !src->up || !src->down || !ids || layer_key < 0) return DS4G_EINVAL;
     if (T < 1 || T > c->max_tokens) return DS4G_EINVAL;
     if (src->gate_up_type != c->gut || src->down_type != c->dt) return DS4G_EUNSUPPORTED;
