@@ -43,7 +43,6 @@ class ds4g_host_experts(C.Structure):
 
 
 _lib = None
-_FWD_SIG = None
 
 
 def lib():
