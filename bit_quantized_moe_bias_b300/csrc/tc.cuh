@@ -51,14 +51,6 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Wait until the phase with the given parity has completed.  Gives up after
-// `limit` polls (each poll may suspend the thread for a short,
-// hardware-chosen time) and returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t limit = 1u << 24) {
-    for (uint32_t i = 0; i < limit; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
-}
 
 // ---------------------------------------------------------------- fences
 // Make this thread's generic-proxy shared-memory writes visible to the async
