@@ -40,6 +40,10 @@
  *    workspace, sized by the matching *_workspace() query.
  *  - Row-major everywhere: hidden[T][4096]; a weight matrix [rows][cols] has
  *    rows = output features, cols = input features.
+ *  - One GPU per process: kernel attributes (dynamic shared memory) and the
+ *    SM count that sizes the persistent grids are set up on first use, for
+ *    the device current at that time.  Driving several GPUs from one process
+ *    is not supported; run one process per GPU.
  */
 #ifndef DS4G_H
 #define DS4G_H
