@@ -1,6 +1,8 @@
 // stream.cu — routed experts streamed from host memory through an HBM expert
-// cache.  chenxutan ds4 article §3.5 (SSD streaming: when the model does not
-// fit in memory the engine keeps running and pages weights in on demand) and
+// cache.  chenxutan ds4 article §3.3 (routed experts are not all loaded onto
+// the GPU but brought in as the router selects them), §3.5 (SSD streaming:
+// when the model does not fit in memory the engine keeps running and pages
+// weights in on demand) and
 // the yudady DS-4 DwarfStar page, section "SSD Streaming" (the non-routed
 // weights stay resident; a routed expert that misses the cache is loaded,
 // used, and its space is later released).

@@ -344,7 +344,8 @@ ds4g_status ds4g_moe_forward_noalloc(const float *hidden, int T, const ds4g_laye
 
 /* ------------------------------------------------------------------------
  * Expert streaming: routed experts held in host memory, an HBM expert cache.
- * [P1] §3.5 "SSD streaming" and the yudady DS-4 DwarfStar page, section
+ * [P1] §3.3 (routed experts loaded as the router selects them), §3.5 "SSD
+ * streaming", and the yudady DS-4 DwarfStar page, section
  * "SSD Streaming": when the model does not fit the GPU's memory, the
  * non-routed weights stay resident and a routed expert that misses the cache
  * is loaded, used, and its space later released.  Here the routed experts of
