@@ -1,8 +1,9 @@
 """CPU oracle of the routed-MoE block — TEST INFRASTRUCTURE.
 
 Only tests/, ``__graft_entry__.smoke()`` and bench.py's CPU-baseline leg (and
-its ``--impl reference`` arm, which times this oracle) may import this package.  It wraps ``oracle.c`` (plain C11, fp64 accumulation, no
-code shared with the CUDA library) through ctypes and numpy.
+its ``--impl reference`` arm, which times this oracle) may import this
+package.  It wraps ``oracle.c`` (plain C11, fp64 accumulation, no code shared
+with the CUDA library) through ctypes and numpy.
 
 Parity status: real-model numerics: parity unpinned (no real IQ2_XXS
 codebook, weights or test vectors are available); every function is pinned by
