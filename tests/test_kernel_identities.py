@@ -102,3 +102,16 @@ def test_small_integer_conversions():
     as_f = (np.uint32(0x4B000000) | n).view(np.float32)
     assert np.array_equal(as_f - np.float32(8388608.0), n.astype(np.float32))
     assert np.array_equal(as_f - np.float32(8388607.5), n.astype(np.float32) + np.float32(0.5))
+
+
+def test_q4k_nibble_masks_give_exact_subnormals():
+    # The per-slot Q4_K down takes nibbles (w >> s0) & 0x000F000F and
+    # (w >> (s0 + 4)) & 0x000F000F, s0 in {0, 8}: each half is the fp16
+    # subnormal q * 2^-24 of one 4-bit quant.
+    words = np.concatenate([RNG.integers(0, 2**32, 20000, dtype=np.uint64),
+                            np.arange(2**16, dtype=np.uint64) * 0x10001]).astype(np.uint32)
+    for sh in (0, 4, 8, 12):
+        v = (words >> np.uint32(sh)) & np.uint32(0x000F000F)
+        for half in (0, 16):
+            q = (words >> np.uint32(half + sh)) & np.uint32(15)
+            assert np.array_equal(f16((v >> np.uint32(half)) & np.uint32(0xFFFF)), q * 2.0**-24)
