@@ -117,9 +117,10 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ our arm
-def build_model(dev, nlayer, cfg=CFG, q4_layers=0):
+def build_model(dev, nlayer, cfg=CFG, q4_layers=0, zipf=False):
     """nlayer layers of 256 experts generated on the device; the last
-    q4_layers of them with Q4_K gate/up/down, the others IQ2_XXS/Q2_K."""
+    q4_layers of them with Q4_K gate/up/down, the others IQ2_XXS/Q2_K; the
+    router bias ~N(0, 0.1^2), or Zipf(1.1)-ranked with zipf=True."""
     import torch
     import bit_quantized_moe_bias_b300 as B
     grid = torch.from_numpy(np.ascontiguousarray(synth.iq2_grid(SEED)).view(np.int64).reshape(256)).to(dev)
@@ -141,7 +142,7 @@ def build_model(dev, nlayer, cfg=CFG, q4_layers=0):
         L = B.MoELayer(mats[synth.KIND_GATE], mats[synth.KIND_UP], mats[synth.KIND_DOWN], *sh,
                        grid if gut == 0 else None, gut, dt)
         R = torch.from_numpy(synth.router(SEED, cfg, l)).to(dev)
-        b = torch.from_numpy(synth.bias_normal(SEED, cfg, l)).to(dev)
+        b = torch.from_numpy((synth.bias_zipf if zipf else synth.bias_normal)(SEED, cfg, l)).to(dev)
         layers.append((L, R, b))
     torch.cuda.synchronize()
     return layers
@@ -157,6 +158,28 @@ def max_over_ranks(times, world, dev):
     t = torch.tensor(times, device=dev, dtype=torch.float64)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return t.tolist()
+
+
+def graph_kernels(graph):
+    """Kernel nodes of a captured CUDA graph (captured with keep_graph=True),
+    or None if the graph cannot be inspected."""
+    try:
+        from cuda.bindings import runtime as rt
+        g = rt.cudaGraph_t(init_value=graph.raw_cuda_graph())
+        err, _, n = rt.cudaGraphGetNodes(g, 0)
+        if err != rt.cudaError_t.cudaSuccess:
+            return None
+        err, nodes, n = rt.cudaGraphGetNodes(g, n)
+        if err != rt.cudaError_t.cudaSuccess:
+            return None
+        kern = 0
+        for nd in nodes[:n]:
+            err, ty = rt.cudaGraphNodeGetType(nd)
+            if err == rt.cudaError_t.cudaSuccess and ty == rt.cudaGraphNodeType.cudaGraphNodeTypeKernel:
+                kern += 1
+        return kern
+    except Exception:   # noqa: BLE001 - an inspection failure only loses the count
+        return None
 
 
 def run_ours(args, rank, world, local_rank):
@@ -323,7 +346,7 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline and not q4:
-        line["cpu_baseline"] = cpu_baseline(args.cpu_layers)
+        line["cpu_baseline"] = cpu_baseline("decode", args.cpu_size or NLAYER, 1)
     return line
 
 
@@ -555,37 +578,261 @@ def run_prefill(args, rank, world, local_rank):
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": kind, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "flop_per_launch": PF_GATEUP_FLOP,
                      "launch_us": round(gu_us, 2), "traffic": None},
-        "gpu_launches": 7 * args.steps,
+        "gpu_launches": 6 * args.steps,   # route, bucket, permute, 2 x gemm, combine
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_prefill(args.cpu_tokens)
+        line["cpu_baseline"] = cpu_baseline("prefill", args.cpu_size, 1)
     return line
 
 
-def cpu_baseline_prefill(ntok):
-    """Oracle (route + forward) on the first `ntok` tokens of the prefill
-    chunk; tokens are independent given the routing, so tokens/s scales."""
-    import oracle
-    x = synth.hidden(SEED, PF_CFG, ntok)
-    R, b = synth.router(SEED, PF_CFG, 0), synth.bias_normal(SEED, PF_CFG, 0)
-    sh = synth.shared(SEED, PF_CFG, 0)
-    grid = synth.iq2_grid(SEED)
+# --------------------------------------------------- batched decode workload
+B2_T, B2_CFG, B2_COPIES = 32, 2, 8
+B2_WORKLOAD = ("config2 batched decode: T=32 independent tokens through 1 MoE layer x 256 experts (IQ2_XXS gate/up, "
+               "Q2_K down, bf16 shared, fp32 router), router bias Zipf(1.1)-ranked; a step = route + forward of the "
+               "batch on each of 8 independent layer copies in turn")
+EXPERT_BYTES_Q2 = 2 * 2162688 + 2752512             # 7,077,888
+
+
+def _barrier(world):
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+
+
+def run_batched(args, rank, world, local_rank):
+    """Config 2: T = 32 tokens per layer call with Zipf-skewed routing, so
+    the six selections of the 32 tokens overlap heavily.  Eight independent
+    layer copies (1.86 GB each) are used in turn, so every call finds its
+    weights cold in L2.  Algorithmic bytes per call: the distinct selected
+    experts' packed bytes + shared expert + router + activations."""
+    import torch
+    import bit_quantized_moe_bias_b300 as B
+    torch.cuda.set_device(local_rank)
+    dev = f"cuda:{local_rank}"
+    T, nc = B2_T, B2_COPIES
+    t_setup = time.time()
+    layers = build_model(dev, nc, B2_CFG, zipf=True)
+    setup_s = time.time() - t_setup
+    x_host = torch.from_numpy(synth.hidden(SEED + rank, B2_CFG, T)).pin_memory()
+    y_host = torch.empty(nc, T, H, dtype=torch.float32).pin_memory()
+    x = x_host.to(dev)
+    ids = torch.empty(nc, T, K, dtype=torch.int32, device=dev)
+    w = torch.empty(nc, T, K, dtype=torch.float32, device=dev)
+    out = torch.empty(nc, T, H, device=dev)
+    rws = B.workspace(B.ds4g_route_workspace(T), dev)
+    fws = B.workspace(B.ds4g_forward_workspace(T), dev)
+
+    def step(ev=None):
+        for c, (L, R, b) in enumerate(layers):
+            B.ds4g_moe_route(x, R, b, ids[c], w[c], rws)
+            if ev is not None:
+                ev[c][0].record()
+            B.ds4g_moe_forward(x, L.struct, ids[c], w[c], out[c], fws)
+            if ev is not None:
+                ev[c][1].record()
+
+    step()
+    torch.cuda.synchronize()
+    st = B.ds4g_last_error(rws) or B.ds4g_last_error(fws)
+    if st:
+        raise RuntimeError(f"device status {st} during warm-up")
+    ids_h = ids.cpu().numpy()
+    distinct = [len(set(ids_h[c].reshape(-1).tolist())) for c in range(nc)]
+    step_bytes = sum(u * EXPERT_BYTES_Q2 + SHARED_BYTES + ROUTER_BYTES + E * 4 + 2 * T * H * 4 for u in distinct)
+    graph = torch.cuda.CUDAGraph(keep_graph=True)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            step()
+    torch.cuda.current_stream().wait_stream(s)
+    nkern = graph_kernels(graph)
+    graph.instantiate()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _barrier(world)
+    with ClockSampler(local_rank) as clk:
+        ev0.record()
+        for _ in range(args.steps):
+            graph.replay()
+        ev1.record()
+        torch.cuda.synchronize()
+    _barrier(world)
+    dev_s = ev0.elapsed_time(ev1) / 1e3
+    _barrier(world)
     t0 = time.perf_counter()
-    ids, w, _, _ = oracle.route(x, R, b)
-    t_route = time.perf_counter() - t0
-    gate, up, down = [None] * E, [None] * E, [None] * E
-    for e in sorted(set(int(v) for v in ids.reshape(-1))):
-        gate[e], up[e], down[e] = synth.expert(SEED, PF_CFG, 0, e)
+    for _ in range(args.steps):
+        x.copy_(x_host, non_blocking=True)
+        graph.replay()
+        y_host.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    _barrier(world)
+    # the forward alone (eager, CUDA events on the launching stream), per copy
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    fw_us = []
+    for _ in range(3):
+        evs = [(mk(), mk()) for _ in range(nc)]
+        step(evs)
+        torch.cuda.synchronize()
+        fw_us.append([a.elapsed_time(b) * 1e3 for a, b in evs])
+    fw_us = [statistics.median(v[c] for v in fw_us) for c in range(nc)]
+    st = B.ds4g_last_error(rws) or B.ds4g_last_error(fws)
+    if st:
+        raise RuntimeError(f"device status {st} after the timed region")
+    dev_s, e2e_s = max_over_ranks([dev_s, e2e_s], world, dev)
+    if rank != 0:
+        return None
+    tokens = T * nc * args.steps * world
+    hbm, kind = peaks()
+    fw_bytes = [u * EXPERT_BYTES_Q2 + SHARED_BYTES + 2 * T * H * 4 + 2 * T * K * 4 for u in distinct]
+    achieved = sum(fw_bytes) / (sum(fw_us) * 1e-6) / 1e9
+    line = {
+        "metric": METRIC, "value": round(tokens / dev_s, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dev_s / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp16x2-split activations x exact codes -> f32", "data": "synthetic",
+        "config": {"workload": B2_WORKLOAD, "tokens_per_call": T, "layer_copies": nc, "global_batch": T,
+                   "seq_len": 1, "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "no flush: 8 layer copies of 1.86 GB used in turn (>> 126 MB L2)",
+                   "distinct_experts_per_call": distinct,
+                   "achieved_hbm_gbs_block": round(step_bytes * args.steps / dev_s / 1e9, 1),
+                   "setup_s": round(setup_s, 1)},
+        "e2e": {"value": round(tokens / e2e_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(x_host.numel() * 4),
+                "d2h_bytes_per_step": int(y_host.numel() * 4)},
+        "roofline": {"bound": "hbm", "kernel": "ds4g_moe_forward at T=32 (all its launches)",
+                     "achieved": round(achieved, 1), "peak": hbm, "peak_kind": kind, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "bytes_per_launch": int(sum(fw_bytes) / nc),
+                     "launch_us": round(sum(fw_us) / nc, 2), "traffic": None},
+        "gpu_launches": (nkern * args.steps) if nkern is not None else None,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline("batched", args.cpu_size, 8)
+    return line
+
+
+# ------------------------------------------------- q2-q4 prefill workload
+Q4P_T, Q4P_CFG, Q4P_LAYERS = 4096, 4, 8
+Q4P_WORKLOAD = ("config4 mixed-precision prefill: T=4096 tokens through 8 MoE layers x 256 experts (layers 0-1 "
+                "IQ2_XXS gate/up + Q2_K down, layers 2-7 Q4_K gate/up/down), bf16 shared, fp32 router, Zipf(1.1) "
+                "router bias, rmsnorm between layers; a step = the whole 8-layer chain")
+
+
+def run_q2q4_prefill(args, rank, world, local_rank):
+    import torch
+    import bit_quantized_moe_bias_b300 as B
+    torch.cuda.set_device(local_rank)
+    dev = f"cuda:{local_rank}"
+    T, nl = Q4P_T, Q4P_LAYERS
+    t_setup = time.time()
+    layers = build_model(dev, nl, Q4P_CFG, q4_layers=Q4_LAYERS, zipf=True)
+    setup_s = time.time() - t_setup
+    x_host = torch.from_numpy(synth.hidden(SEED + rank, Q4P_CFG, T)).pin_memory()
+    y_host = torch.empty(T, H, dtype=torch.float32).pin_memory()
+    x = x_host.to(dev)
+    hb = [torch.empty(T, H, device=dev) for _ in range(2)]
+    out = torch.empty(T, H, device=dev)
+    ids = torch.empty(T, K, dtype=torch.int32, device=dev)
+    w = torch.empty(T, K, dtype=torch.float32, device=dev)
+    rws = B.workspace(B.ds4g_route_workspace(T), dev)
+    fws = B.workspace(B.ds4g_forward_workspace(T), dev)
+
+    def step(ev=None):
+        h = x
+        for l, (L, R, b) in enumerate(layers):
+            B.ds4g_moe_route(h, R, b, ids, w, rws)
+            if ev is not None:
+                ev[l][0].record()
+            dst = out if l == nl - 1 else hb[0]
+            B.ds4g_moe_gate_up(h, L.struct, ids, w, dst, fws)
+            if ev is not None:
+                ev[l][1].record()
+            B.ds4g_moe_down(h, L.struct, ids, w, dst, fws)
+            if l < nl - 1:
+                B.ds4g_rmsnorm(dst, hb[1])
+                h = hb[1]
+
+    for _ in range(max(args.warmup, 1)):
+        step()
+    torch.cuda.synchronize()
+    st = B.ds4g_last_error(rws) or B.ds4g_last_error(fws)
+    if st:
+        raise RuntimeError(f"device status {st} during warm-up")
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    evs = [[(mk(), mk()) for _ in range(nl)] for _ in range(args.steps)]
+    e0, e1 = mk(), mk()
+    _barrier(world)
+    with ClockSampler(local_rank) as clk:
+        e0.record()
+        for i in range(args.steps):
+            step(evs[i])
+        e1.record()
+        torch.cuda.synchronize()
+    _barrier(world)
+    dev_s = e0.elapsed_time(e1) / 1e3
+    gu_us = statistics.mean(sum(a.elapsed_time(b) for a, b in ev) for ev in evs) * 1e3
+    _barrier(world)
     t0 = time.perf_counter()
-    oracle.moe_forward(x, ids, w, gate, up, down, *sh, grid)
-    t = t_route + time.perf_counter() - t0
-    return {"value": round(ntok / t, 4), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"first {ntok} of the {PF_T} tokens (oracle route + forward, fp64, OpenMP over rows); "
-                      "synthetic weight generation not timed"}
+    for _ in range(args.steps):
+        x.copy_(x_host, non_blocking=True)
+        step()
+        y_host.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    _barrier(world)
+    st = B.ds4g_last_error(rws) or B.ds4g_last_error(fws)
+    if st:
+        raise RuntimeError(f"device status {st} after the timed region")
+    dev_s, e2e_s = max_over_ranks([dev_s, e2e_s], world, dev)
+    if rank != 0:
+        return None
+    tokens = T * args.steps * world
+    meas = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    peak, kind = (float(meas["bf16_tflops"]), "measured burst") if "bf16_tflops" in meas else (1800.0, "fallback")
+    gu_flop = nl * 2 * (K * T + T) * 2 * F * H
+    layer_flop = 2 * (K * T + T) * 3 * F * H + 2 * T * E * H
+    achieved = gu_flop / (gu_us * 1e-6) / 1e12
+    line = {
+        "metric": METRIC, "value": round(tokens / dev_s, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dev_s / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16/bf16 x f16/bf16 -> f32", "data": "synthetic",
+        "config": {"workload": Q4P_WORKLOAD, "tokens_per_step": T, "layers": nl, "q4_layers": Q4_LAYERS,
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "no flush: 25.8 GB of layer weights per step (>> 126 MB L2)",
+                   "achieved_tflops_block": round(nl * layer_flop / (dev_s / args.steps) / 1e12, 1),
+                   "setup_s": round(setup_s, 1)},
+        "e2e": {"value": round(tokens / e2e_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(x_host.numel() * 4),
+                "d2h_bytes_per_step": int(y_host.numel() * 4)},
+        "roofline": {"bound": "tensor", "kernel": "prefill_gemm_kernel (gate/up phase, incl. bucket + permute), "
+                                                  "8 layers", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": kind, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "flop_per_launch": gu_flop // nl, "launch_us": round(gu_us / nl, 2), "traffic": None},
+        "gpu_launches": (nl * 6 + (nl - 1)) * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline("q2q4-prefill", args.cpu_size, 2)
+    return line
+
+
+WORKLOADS = {"decode": WORKLOAD, "prefill": PF_WORKLOAD, "batched": B2_WORKLOAD, "q2q4-prefill": Q4P_WORKLOAD,
+             "decode-stream": WORKLOAD}
 
 
 # ------------------------------------------------------------- CPU oracle
+# The oracle (plain C, fp64 accumulation, OpenMP over output rows) timed on a
+# bounded sample of each workload.  Generating the synthetic weights is not
+# timed.  The GPU arm runs these samples in a fresh interpreter (the same
+# code path as --impl reference): in the GPU arm's own process the oracle's
+# OpenMP threads competed with torch's thread pool and ran about 4x slower.
 _CACHE = {}
 
 
@@ -595,29 +842,75 @@ def _cached(key, fn):
     return _CACHE[key]
 
 
+def _experts(cfg, layer, ids, gut=0, dt=1):
+    gate, up, down = [None] * E, [None] * E, [None] * E
+    for e in sorted(set(int(v) for v in np.asarray(ids).reshape(-1))):
+        gate[e], up[e], down[e] = _cached(("X", cfg, layer, e, gut),
+                                          lambda: synth.expert(SEED, cfg, layer, e, gut, dt))
+    return gate, up, down
+
+
 def oracle_sample(nlayers, nthreads=0):
-    """Oracle on 1 token through the first `nlayers` layers of the config-1
-    chain with `nthreads` OpenMP threads (0 = all cores); returns (seconds of
-    oracle compute, threads).  Generating the synthetic weights is not timed
-    (and is cached between samples)."""
+    """Decode (full-depth workload): 1 token through the first `nlayers`
+    layers of the chain.  Returns (seconds of oracle compute, tokens)."""
     import oracle
     x = synth.hidden(SEED, CFG, 1, layer=999, normalise=False)
     grid = synth.iq2_grid(SEED)
     t = 0.0
     for l in range(nlayers):
-        R, b, sh = _cached(("L", l), lambda: (synth.router(SEED, CFG, l), synth.bias_normal(SEED, CFG, l),
-                                              synth.shared(SEED, CFG, l)))
+        R, b, sh = _cached(("L", CFG, l), lambda: (synth.router(SEED, CFG, l), synth.bias_normal(SEED, CFG, l),
+                                                   synth.shared(SEED, CFG, l)))
         t0 = time.perf_counter()
         xn = oracle.rmsnorm(x)
         ids, w, _, _ = oracle.route(xn, R, b)
         t += time.perf_counter() - t0
-        gate, up, down = [None] * E, [None] * E, [None] * E
-        for e in ids[0]:
-            gate[e], up[e], down[e] = _cached(("X", l, int(e)), lambda: synth.expert(SEED, CFG, l, int(e)))
+        gate, up, down = _experts(CFG, l, ids)
         t0 = time.perf_counter()
         x = oracle.moe_forward(xn, ids, w, gate, up, down, *sh, grid, nthreads=nthreads)
         t += time.perf_counter() - t0
-    return t, (nthreads or os.cpu_count())
+    return t, 1
+
+
+def oracle_sample_layer(cfg, ntok, zipf, nthreads=0):
+    """One layer (prefill or batched decode): route + forward of the first
+    `ntok` tokens of the workload's batch.  Returns (seconds, tokens)."""
+    import oracle
+    x = synth.hidden(SEED, cfg, ntok)
+    R, b, sh = _cached(("L", cfg, 0), lambda: (synth.router(SEED, cfg, 0), (synth.bias_zipf if zipf else
+                                               synth.bias_normal)(SEED, cfg, 0), synth.shared(SEED, cfg, 0)))
+    grid = synth.iq2_grid(SEED)
+    t0 = time.perf_counter()
+    ids, w, _, _ = oracle.route(x, R, b)
+    t = time.perf_counter() - t0
+    gate, up, down = _experts(cfg, 0, ids)
+    t0 = time.perf_counter()
+    oracle.moe_forward(x, ids, w, gate, up, down, *sh, grid, nthreads=nthreads)
+    return t + time.perf_counter() - t0, ntok
+
+
+def oracle_sample_q2q4(ntok, nthreads=0):
+    """q2-q4 prefill chain: the first `ntok` tokens through all 8 layers
+    (route, forward, rmsnorm between layers).  Tokens are independent of one
+    another through the whole chain.  Returns (seconds, tokens)."""
+    import oracle
+    h = synth.hidden(SEED, Q4P_CFG, ntok)
+    grid = synth.iq2_grid(SEED)
+    t = 0.0
+    for l in range(Q4P_LAYERS):
+        q4 = l >= Q4P_LAYERS - Q4_LAYERS
+        gut, dt = (2, 2) if q4 else (0, 1)
+        R, b, sh = _cached(("L", Q4P_CFG, l), lambda: (synth.router(SEED, Q4P_CFG, l),
+                                                        synth.bias_zipf(SEED, Q4P_CFG, l),
+                                                        synth.shared(SEED, Q4P_CFG, l)))
+        t0 = time.perf_counter()
+        ids, w, _, _ = oracle.route(h, R, b)
+        t += time.perf_counter() - t0
+        gate, up, down = _experts(Q4P_CFG, l, ids, gut, dt)
+        t0 = time.perf_counter()
+        out = oracle.moe_forward(h, ids, w, gate, up, down, *sh, grid, gut, dt, nthreads=nthreads)
+        h = oracle.rmsnorm(out) if l + 1 < Q4P_LAYERS else out
+        t += time.perf_counter() - t0
+    return t, ntok
 
 
 def cpu_model():
@@ -632,37 +925,73 @@ def cpu_model():
     return platform.processor() or "unknown"
 
 
-def cpu_baseline(nlayers):
-    t, cores = oracle_sample(nlayers)
-    per_token = t * NLAYER / nlayers
-    t1, _ = oracle_sample(1, nthreads=1)          # the same oracle on one core: its first layer
-    return {"value": round(1.0 / per_token, 5), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "value_1thread": round(1.0 / (t1 * NLAYER), 5), "cpu_model": cpu_model(),
-            "sample": f"1 token through the first {nlayers} of {NLAYER} layers (oracle rmsnorm + route + "
-                      f"forward, fp64, OpenMP over rows), extrapolated linearly to {NLAYER} layers; "
-                      f"value_1thread: its first layer on one thread, extrapolated to {NLAYER}"}
+# per workload: (sample function of (size, nthreads), total tokens of one
+# GPU step's workload unit, description of a sample of `size`)
+def _sampler(workload, size):
+    if workload == "prefill":
+        return (lambda n: oracle_sample_layer(PF_CFG, size, False, n),
+                f"first {size} of the {PF_T} tokens of the chunk (oracle route + forward)")
+    if workload == "batched":
+        return (lambda n: oracle_sample_layer(B2_CFG, size, True, n),
+                f"first {size} of the {B2_T} tokens of the batch (oracle route + forward)")
+    if workload == "q2q4-prefill":
+        return (lambda n: oracle_sample_q2q4(size, n),
+                f"first {size} of the {Q4P_T} tokens through all {Q4P_LAYERS} layers (oracle route + forward, "
+                "rmsnorm between layers); tokens are independent through the chain")
+    nl = size
+    return (lambda n: (lambda r: (r[0] * NLAYER / nl, r[1]))(oracle_sample(nl, n)),
+            f"1 token through the first {nl} of {NLAYER} layers (oracle rmsnorm + route + forward), "
+            f"extrapolated linearly to {NLAYER} layers")
+
+
+def default_cpu_size(workload):
+    return {"prefill": 8, "batched": 32, "q2q4-prefill": 4}.get(workload, NLAYER)
 
 
 def run_reference(args):
-    tokens, secs = 0, 0.0
+    """The oracle on this host's cores, on a bounded sample of the workload
+    per step; value = sample tokens / oracle seconds (higher is better)."""
+    size = args.cpu_size or default_cpu_size(args.workload)
+    fn, desc = _sampler(args.workload, size)
     for _ in range(args.warmup):
-        oracle_sample(1)
-    cores = os.cpu_count()
+        fn(args.cpu_threads)
+    tokens, secs = 0, 0.0
     for _ in range(args.steps):
-        t, cores = oracle_sample(args.cpu_layers)
-        secs += t * NLAYER / args.cpu_layers
-        tokens += 1
+        t, n = fn(args.cpu_threads)
+        secs += t
+        tokens += n
     value = tokens / secs
+    cores = args.cpu_threads or os.cpu_count()
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "tokens/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "layers": NLAYER, "tokens_per_step": 1},
+        "config": {"workload": WORKLOADS[args.workload]},
         "cpu_baseline": {"value": round(value, 5), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"per step 1 token through {args.cpu_layers} of {NLAYER} layers, "
-                                   f"extrapolated to {NLAYER}"},
+                         "cpu_model": cpu_model(), "sample": f"per step: {desc}; fp64, OpenMP over output rows"},
         "e2e": {"value": round(value, 5), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+
+
+def cpu_baseline(workload, size=None, size_1thread=None):
+    """The oracle timed in a fresh interpreter (bench.py --impl reference):
+    all cores on `size`, and one thread on `size_1thread`."""
+    def sub(sz, threads):
+        cmd = [sys.executable, os.path.abspath(__file__), "--impl", "reference", "--workload", workload,
+               "--steps", "1", "--warmup", "0", "--cpu-threads", str(threads)]
+        if sz:
+            cmd += ["--cpu-size", str(sz)]
+        env = {k: v for k, v in os.environ.items() if k not in ("OMP_NUM_THREADS", "RANK", "WORLD_SIZE",
+                                                               "LOCAL_RANK")}
+        out = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=900, check=True).stdout
+        return json.loads(out.strip().splitlines()[-1])["cpu_baseline"]
+    full = sub(size, 0)
+    if size_1thread is not None:
+        one = sub(size_1thread, 1)
+        full["value_1thread"] = one["value"]
+        full["sample_1thread"] = one["sample"]
+    full["process"] = "fresh interpreter (bench.py --impl reference), no torch loaded"
+    return full
 
 
 def main():
@@ -674,14 +1003,17 @@ def main():
     ap.add_argument("--layers", type=int, default=NLAYER,
                     help="stacked layers (43 = the full-depth workload; fewer only for profiling)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-layers", type=int, default=43)
+    ap.add_argument("--cpu-size", type=int, default=0,
+                    help="oracle sample per step: layers (decode) or tokens (other workloads); 0 = default")
+    ap.add_argument("--cpu-threads", type=int, default=0, help="oracle OpenMP threads (0 = all cores)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["decode", "prefill", "decode-stream"], default="decode",
+    ap.add_argument("--workload", choices=list(WORKLOADS), default="decode",
                     help="decode = 43-layer full-depth decode (headline); prefill = T=2048 chunk, one layer; "
-                         "decode-stream = routed experts streamed from host memory through an HBM cache")
+                         "batched = T=32 tokens, one layer, Zipf routing; q2q4-prefill = T=4096 through 8 "
+                         "layers (2 q2, 6 q4), Zipf routing; decode-stream = routed experts streamed from host "
+                         "memory through an HBM cache")
     ap.add_argument("--stream-layers", type=int, default=4, help="decode-stream: layers (host memory 1.8 GB each)")
     ap.add_argument("--cache-slots", type=int, default=256, help="decode-stream: HBM cache slots (7.1 MB each)")
-    ap.add_argument("--cpu-tokens", type=int, default=8, help="prefill CPU-baseline sample size")
     ap.add_argument("--model", choices=["q2", "q2-q4"], default="q2",
                     help="decode model: q2 = every layer IQ2_XXS/Q2_K (headline); q2-q4 = last 6 layers Q4_K")
     ap.add_argument("--decode-path", choices=["fused", "layer", "split"], default="fused",
@@ -700,7 +1032,8 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
-    run = {"prefill": run_prefill, "decode-stream": run_stream}.get(args.workload, run_ours)
+    run = {"prefill": run_prefill, "decode-stream": run_stream, "batched": run_batched,
+           "q2q4-prefill": run_q2q4_prefill}.get(args.workload, run_ours)
     line = run(args, rank, world, local_rank)
     if line is not None:
         print(json.dumps(line), flush=True)

@@ -2,6 +2,7 @@
 // fixed dimensions, the packed device layout of the quantised blocks, the
 // workspace header, and small PTX wrappers (mma.sync, prmt, cache hints).
 #pragma once
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -91,6 +92,16 @@ size_t decode_workspace(int T);
 ds4g_status decode_forward(const float *hidden, int T, const ds4g_layer *L, const int32_t *ids, const float *w,
                            float *out, void *workspace, cudaStream_t st, int phases,
                            uint32_t *status_word = nullptr);
+
+// TMA tensor maps over a row-major [rows][cols] bf16 matrix, 128-byte
+// swizzle (tmap.cu).  tmap_bf16_2d: box of 64 columns x box_rows rows.
+// tmap_bf16_rowtile: box of tile_rows rows x (64 * tile_chunks) columns,
+// landing in shared memory as [tile_chunks][tile_rows][64] (one 128-byte line
+// per row of a 64-column chunk, so the swizzle rotates 16-byte units by row).
+// False if the encoder is unavailable or refuses the arguments.
+bool tmap_bf16_2d(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+bool tmap_bf16_rowtile(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t tile_rows,
+                       uint32_t tile_chunks);
 
 // An expert id is usable if it is in range and its packed matrices are
 // non-NULL and 16-byte aligned (a misaligned vector load would fault).

@@ -4,6 +4,8 @@
 // block on the driver's allocator, a plugin handed fixed buffers by its host
 // engine).  Its scratch is a file-scope device array instead of a caller
 // workspace.
+#include <atomic>
+
 #include "ds4g_internal.cuh"
 
 namespace ds4g {
@@ -16,20 +18,24 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes]
 
 // Device address of g_noalloc_scratch, looked up once per device.  In host
 // code the array's name is only a host-side stand-in, so kernels must be given
-// this address, never the symbol itself.
+// this address, never the symbol itself.  Host threads may race on the first
+// lookup of a device: both find the same address, and the atomic store makes
+// the cached value safe to read from any thread.  A cudaDeviceReset unloads
+// the module, so the cached address is stale afterwards (documented in the
+// header: the entry point is not supported after a reset).
 constexpr int kMaxDevices = 64;
-static void *g_scratch_addr[kMaxDevices];
+static std::atomic<void *> g_scratch_addr[kMaxDevices];
 
 static ds4g_status scratch_address(void **ptr) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return DS4G_ECUDA;
     if (dev < 0 || dev >= kMaxDevices) return DS4G_EUNSUPPORTED;
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
+    void *p = g_scratch_addr[dev].load(std::memory_order_acquire);
+    if (!p) {
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return DS4G_ECUDA;
-        g_scratch_addr[dev] = p;
+        g_scratch_addr[dev].store(p, std::memory_order_release);
     }
-    *ptr = g_scratch_addr[dev];
+    *ptr = p;
     return DS4G_OK;
 }
 
@@ -60,11 +66,13 @@ extern "C" ds4g_status ds4g_moe_forward_noalloc(const float *hidden, int T, cons
     const ds4g_status ar = scratch_address(&ws);
     if (ar != DS4G_OK) return ar;
     cudaStream_t st = (cudaStream_t)s;
-    // The array keeps whatever the previous call left.  The kernels' tile
-    // counters and the status word must start at zero, so clear the whole
-    // used range (partials and activations are fully rewritten before they
-    // are read).  cudaMemsetAsync allocates nothing.
-    if (cudaMemsetAsync(ws, 0, need, st) != cudaSuccess) return DS4G_ECUDA;
+    // The array keeps whatever the previous call left.  Only the status word
+    // and the kernels' tile counters must start at zero; all of them lie
+    // below kWsScratch (12 KB), and every other byte the kernels use is
+    // written before it is read.  The kernels put their counters back to
+    // zero, so the clear matters only after a call that a fault cut short;
+    // it is 12 KB, not the 4.9 MB in use.  cudaMemsetAsync allocates nothing.
+    if (cudaMemsetAsync(ws, 0, kWsScratch, st) != cudaSuccess) return DS4G_ECUDA;
     for (int t0 = 0; t0 < T; t0 += kDecodeMaxT) {
         const int n = T - t0 < kDecodeMaxT ? T - t0 : kDecodeMaxT;
         const ds4g_status rc = decode_forward(hidden + (size_t)t0 * kH, n, L, ids + (size_t)t0 * kK,

@@ -9,9 +9,13 @@
 //            tokens in order (rows 6T..7T-1, the shared expert's operand)
 //   gate/up  per (group, 128-row tile of G/U, chunk of <= 128 bucket rows):
 //            D_g = G_tile . xb_rows^T, D_u = U_tile . xb_rows^T in TMEM,
-//            epilogue h = silu(D_g) * D_u -> hb (bf16)
+//            epilogue h = silu(D_g) * D_u -> h32 (fp32)
+//   cast     per row of h32: routed rows -> fp16 of 2^-e h with one power of
+//            two 2^e per row (h can exceed the fp16 range on Q4_K layers), the
+//            shared rows -> bf16; -> hb, hscale
 //   down     per (group, 128-row tile of D, chunk): D = Dn_tile . hb_rows^T,
-//            epilogue y[slot] = w[slot] * D (fp32; weight 1 for the shared rows)
+//            epilogue y[slot] = w[slot] * 2^e[slot] * D (fp32; weight 1 and
+//            no scale for the shared rows)
 //   combine  out[t] = y[6T + t] + sum_{k=0..5} y[inv[t][k]]   (fixed order)
 //
 // Groups are the 256 routed experts plus the shared expert (group 256).  A
@@ -24,11 +28,11 @@
 //               read straight from HBM into registers (one block column
 //               prefetched ahead) and written as bf16 into the 128-byte
 //               swizzled shared-memory layout the tensor core reads.
-// The weights enter as the fp32 value of the block formula rounded to nearest
-// even, in fp16 for the routed gate/up (with fp16 activations) and in bf16
-// for the down projection (with bf16 h) — the same bits ds4g_dequantize gives
-// for bf16 — so the GEMM's only departures from fp32 are that operand
-// rounding and the accumulation order.  The shared expert is bf16 throughout.
+// The routed weights enter as the fp32 value of the block formula rounded to
+// nearest even in fp16, against fp16 activations (gate/up) and fp16 scaled h
+// (down), so the GEMM's only departures from fp32 are that operand rounding
+// and the accumulation order.  The shared expert is bf16 throughout (its
+// weights are bf16 in memory).
 //
 // Dequantisation without per-weight arithmetic: an IQ2_XXS sub-block has
 // only three magnitudes db*8, db*25, db*43 (the codebook's values), a Q2_K
@@ -67,7 +71,8 @@ struct PFArgs {
     const uint64_t *grid;
     const int32_t *perm;             // [6T]
     const float *w;                  // [T*6]
-    __nv_bfloat16 *hb;               // [7T][2048]
+    float *h32;                      // [7T][2048] h in fp32 (gate/up output; aliases y)
+    const float *hscale;             // [7T] 2^e of each row of hb (down phase)
     float *y;                        // [7T][4096]
     uint32_t *status;
 };
@@ -189,9 +194,10 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
-// Operand element of the GEMM: fp16 for the routed gate/up (activations are
-// RMS-normalised, |x| <= 64, and fp16 keeps 3 more bits of x than bf16),
-// bf16 elsewhere (h can exceed the fp16 range).
+// Operand element of the GEMM: fp16 for the routed experts (activations are
+// RMS-normalised, |x| <= 64, h enters scaled per row, and fp16 keeps 3 more
+// bits than bf16), bf16 for the shared expert's activations (its weights are
+// bf16 in memory, and both operands of one MMA have the same type).
 __device__ __forceinline__ uint32_t pack2(bool f16, float lo, float hi) {
     return f16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
 }
@@ -316,7 +322,7 @@ __device__ __forceinline__ void dq_q2k_sub(const PFSmem &sm, uint32_t W, uint32_
     const float dsc = __fmul_rn(d, (float)(scb & 15u));
     const float dm = __fmul_rn(dmin, (float)(scb >> 4));
     uint32_t rlo, rhi;
-    split4(false, __fmaf_rn(dsc, 0.0f, -dm), __fmaf_rn(dsc, 1.0f, -dm), __fmaf_rn(dsc, 2.0f, -dm),
+    split4(true, __fmaf_rn(dsc, 0.0f, -dm), __fmaf_rn(dsc, 1.0f, -dm), __fmaf_rn(dsc, 2.0f, -dm),
            __fmaf_rn(dsc, 3.0f, -dm), rlo, rhi);
     const uint2 s0 = sm.q2lut[16 * (W & 255u) + rep16], s1 = sm.q2lut[16 * ((W >> 8) & 255u) + rep16];
     const uint2 s2 = sm.q2lut[16 * ((W >> 16) & 255u) + rep16], s3 = sm.q2lut[16 * (W >> 24) + rep16];
@@ -519,8 +525,8 @@ __global__ void __launch_bounds__(kPFThreads, 1)
                     break;
                 }
                 tc::tc_fence_after();
-                // routed gate/up: fp16 operands; shared expert and down: bf16
-                const uint32_t idesc = tc::idesc_f16(kBM, t.npad, !(a.phase == 1 && !t.shared));
+                // routed experts: fp16 operands; shared expert: bf16
+                const uint32_t idesc = tc::idesc_f16(kBM, t.npad, t.shared);
                 const uint32_t dcol = tbase + (uint32_t)(ab * (a.phase == 1 ? 256 : 128));
                 bool ok = true;
                 for (int ks = 0; ks < nkb; ++ks, ++it) {
@@ -580,7 +586,7 @@ __global__ void __launch_bounds__(kPFThreads, 1)
                         const int n = c0 + j;
                         if (n < t.n) {
                             const float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
-                            a.hb[(size_t)(t.row0 + n) * kF + pos] = __float2bfloat16_rn(silu_f(gv) * uv);
+                            a.h32[(size_t)(t.row0 + n) * kF + pos] = silu_f(gv) * uv;
                         }
                     }
                 }
@@ -595,7 +601,7 @@ __global__ void __launch_bounds__(kPFThreads, 1)
                         const int n = c0 + j;
                         if (n < t.n) {
                             const int slot = t.row0 + n;
-                            const float sc = t.shared ? 1.0f : __ldg(a.w + a.perm[slot]);
+                            const float sc = t.shared ? 1.0f : __ldg(a.w + a.perm[slot]) * __ldg(a.hscale + slot);
                             a.y[(size_t)slot * kH + row] = sc * __uint_as_float(dv[j]);
                         }
                     }
@@ -674,7 +680,7 @@ __global__ void __launch_bounds__(kPFThreads, 1)
                             } else {
                                 const int j0 = 2 * ks, j1 = 2 * ks + 1;
                                 const uint4 q0 = cur.q[2 * (j0 & 3) + (j0 >> 2)], q1 = cur.q[2 * (j1 & 3) + (j1 >> 2)];
-                                dq_q4k_sub(false, cur, half ? j1 : j0, half ? q1 : q0, st, m, 4 * half);
+                                dq_q4k_sub(true, cur, half ? j1 : j0, half ? q1 : q0, st, m, 4 * half);
                             }
                         }
                         tc::fence_proxy_async_smem();
@@ -737,6 +743,60 @@ __global__ void __launch_bounds__(256) permute_cast_kernel(const float *__restri
     dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
+// Row r of h32 (2048 fp32 values, one CTA of 256 threads): routed rows
+// (r < 6T) -> hb = fp16 of 2^-e h, where 2^e puts the row's largest |h| in
+// [2^14, 2^15) (any finite h fits fp16 and keeps 11 significant bits), and
+// hscale[r] = 2^e; shared rows (r >= 6T) -> bf16 of h, hscale = 1.  The
+// routed rows past offsets[256] (entries with a bad id, which no GEMM task
+// writes or reads) become zeros.  A non-finite h is flagged.
+__global__ void __launch_bounds__(256) hcast_kernel(const float *__restrict__ h32, const int32_t *offsets, int T,
+                                                    uint16_t *__restrict__ hb, float *__restrict__ hscale,
+                                                    uint32_t *status) {
+    const int r = blockIdx.x;
+    const bool routed = r < kK * T;
+    if (routed && r >= offsets[kE]) {
+        *reinterpret_cast<uint4 *>(hb + (size_t)r * kF + 8 * threadIdx.x) = make_uint4(0, 0, 0, 0);
+        if (threadIdx.x == 0) hscale[r] = 1.0f;
+        return;
+    }
+    const float4 *src = reinterpret_cast<const float4 *>(h32 + (size_t)r * kF) + 2 * threadIdx.x;
+    const float4 v0 = __ldcs(src), v1 = __ldcs(src + 1);
+    const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) bad |= !(fabsf(v[i]) <= 3.4028235e38f);
+    if (bad) flag_status(status, DS4G_EDEVICE, 0xF16u);
+    float e2 = 1.0f;
+    if (routed) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        __shared__ float red[8];
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+        __syncthreads();
+        m = red[0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) m = fmaxf(m, red[i]);
+        // m < 2^E with E = biased exponent - 126; e = E - 15 (0 for m = 0)
+        const int E = (int)((__float_as_uint(m) >> 23) & 255u) - 126;
+        const int e = m > 0.f ? max(min(E - 15, 100), -100) : 0;
+        e2 = __uint_as_float((uint32_t)(127 + e) << 23);
+        const float inv = __uint_as_float((uint32_t)(127 - e) << 23);
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = pack_f16x2(v[2 * i] * inv, v[2 * i + 1] * inv);
+        *reinterpret_cast<uint4 *>(hb + (size_t)r * kF + 8 * threadIdx.x) = make_uint4(o[0], o[1], o[2], o[3]);
+    } else {
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+        *reinterpret_cast<uint4 *>(hb + (size_t)r * kF + 8 * threadIdx.x) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (threadIdx.x == 0) hscale[r] = e2;
+}
+
 // out[t] = y[6T + t] + sum_{k=0..5} y[inv[6t + k]]   (fixed order)
 __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ y, const int32_t *inv, int T,
                                                       float *__restrict__ out) {
@@ -765,7 +825,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
 
 // ------------------------------------------------------------------- host
 struct PFLayout {
-    size_t counts, offsets, perm, inv, xb, hb, y, total;
+    size_t counts, offsets, perm, inv, hscale, xb, hb, y, total;
 };
 
 static PFLayout pf_layout(int T) {
@@ -780,6 +840,8 @@ static PFLayout pf_layout(int T) {
     off += align_up(nslot * 4, 256);
     L.inv = off;
     off += align_up(nslot * 4, 256);
+    L.hscale = off;
+    off += align_up(nrow * 4, 256);
     L.xb = off;
     off += align_up(nrow * kH * 2, 1024);
     L.hb = off;
@@ -795,39 +857,12 @@ size_t prefill_workspace(int T) { return pf_layout(T).total; }
 ds4g_status bucket_launch(const int32_t *ids, int T, int32_t *counts, int32_t *offsets, int32_t *perm,
                           int32_t *inv, uint32_t *status, cudaStream_t st);
 
-static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-
-static bool encoder() {
-    if (g_encode) return true;
-    void *fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || !fn)
-        return false;
-    g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
-    return true;
-}
-
-// 2-D bf16 tensor map over a row-major [rows][cols] matrix; box = 64 columns
-// (128 bytes, the swizzle span) x box_rows rows, 128-byte swizzle.
-static bool map_bf16(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
-    const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {cols * 2};
-    const cuuint32_t box[2] = {64, box_rows};
-    const cuuint32_t es[2] = {1, 1};
-    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 static int g_pf_sms = 0;
 static bool g_pf_attr = false;
 
 // phases: 1 = bucket, permute and gate/up; 2 = down and combine; 3 = both.
 ds4g_status prefill_forward(const float *hidden, int T, const ds4g_layer *L, const int32_t *ids, const float *w,
                             float *out, void *workspace, cudaStream_t st, int phases) {
-    if (!encoder()) return DS4G_ECUDA;
     if (!g_pf_sms) {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess) return DS4G_ECUDA;
@@ -847,6 +882,7 @@ ds4g_status prefill_forward(const float *hidden, int T, const ds4g_layer *L, con
     int32_t *perm = (int32_t *)(ws + lay.perm), *inv = (int32_t *)(ws + lay.inv);
     __nv_bfloat16 *xb = (__nv_bfloat16 *)(ws + lay.xb), *hb = (__nv_bfloat16 *)(ws + lay.hb);
     float *y = (float *)(ws + lay.y);
+    float *hscale = (float *)(ws + lay.hscale);
     const int nrow = (kK + 1) * T;
 
     PFArgs a;
@@ -855,7 +891,8 @@ ds4g_status prefill_forward(const float *hidden, int T, const ds4g_layer *L, con
     a.grid = L->iq2_grid;
     a.perm = perm;
     a.w = w;
-    a.hb = hb;
+    a.h32 = y;        // gate/up output; consumed by the cast before the down phase writes y
+    a.hscale = hscale;
     a.y = y;
     a.status = status;
     if (phases & 1) {
@@ -865,8 +902,8 @@ ds4g_status prefill_forward(const float *hidden, int T, const ds4g_layer *L, con
         if (cudaGetLastError() != cudaSuccess) return DS4G_ECUDA;
         CUtensorMap mB[4], mG, mU;
         for (int i = 0; i < 4; ++i)
-            if (!map_bf16(&mB[i], xb, nrow, kH, 16u << i)) return DS4G_ECUDA;
-        if (!map_bf16(&mG, L->sh_gate, kF, kH, kBM) || !map_bf16(&mU, L->sh_up, kF, kH, kBM)) return DS4G_ECUDA;
+            if (!tmap_bf16_2d(&mB[i], xb, nrow, kH, 16u << i)) return DS4G_ECUDA;
+        if (!tmap_bf16_2d(&mG, L->sh_gate, kF, kH, kBM) || !tmap_bf16_2d(&mU, L->sh_up, kF, kH, kBM)) return DS4G_ECUDA;
         a.phase = 1;
         a.qt = L->gate_up_type;
         a.hb_q2perm = L->down_type == DS4G_Q2_K ? 1 : 0;
@@ -878,10 +915,12 @@ ds4g_status prefill_forward(const float *hidden, int T, const ds4g_layer *L, con
         if (cudaGetLastError() != cudaSuccess) return DS4G_ECUDA;
     }
     if (!(phases & 2)) return DS4G_OK;
+    hcast_kernel<<<nrow, 256, 0, st>>>(y, offsets, T, reinterpret_cast<uint16_t *>(hb), hscale, status);
+    if (cudaGetLastError() != cudaSuccess) return DS4G_ECUDA;
     CUtensorMap mB2[4], mD;
     for (int i = 0; i < 4; ++i)
-        if (!map_bf16(&mB2[i], hb, nrow, kF, 16u << i)) return DS4G_ECUDA;
-    if (!map_bf16(&mD, L->sh_down, kH, kF, kBM)) return DS4G_ECUDA;
+        if (!tmap_bf16_2d(&mB2[i], hb, nrow, kF, 16u << i)) return DS4G_ECUDA;
+    if (!tmap_bf16_2d(&mD, L->sh_down, kH, kF, kBM)) return DS4G_ECUDA;
     a.phase = 2;
     a.qt = L->down_type;
     a.hb_q2perm = 0;

@@ -318,18 +318,28 @@ ds4g_status ds4g_moe_decode_stack(const float *hidden, int n_layers, const float
  * engine hands it fixed input/output buffers and owns all other memory.
  * (The ds4 pages have no counterpart: their engine owns all its memory.)
  *
- * Same computation, arguments and checks as ds4g_moe_forward minus the
- * workspace; the caller still passes hidden, ids, w and out.  Scratch is a
- * library-owned device array of 5 MB (file scope, one per device that
- * loads the library, held until the process exits).  Limits and behaviour:
+ * Arguments and checks are those of ds4g_moe_forward minus the workspace;
+ * the caller still passes hidden, ids, w and out.  Whatever T, the call runs
+ * the per-slot decode kernels of ds4g_moe_forward on chunks of up to three
+ * tokens, so it returns, bit for bit, what ds4g_moe_forward returns when
+ * called on the same chunks one at a time.  For a whole batch of T >= 4
+ * tokens ds4g_moe_forward takes other kernels (the batched path from T = 4,
+ * the tensor-core prefill path from T = 64): their results agree with this
+ * call within the block's tolerance, not bit for bit, and they read each
+ * selected expert's weights once per batch, where this call reads them once
+ * per chunk.  Scratch is a library-owned device array of 5 MB (file scope,
+ * one per device that loads the library, held until the process exits).
+ * Limits and behaviour:
  *  - 1 <= T <= DS4G_NOALLOC_MAX_T, else DS4G_EINVAL (T < 1) or
  *    DS4G_ENOSPACE (T too large), returned before any CUDA call.
  *  - Allocates nothing: no cudaMalloc/cudaFree and no allocating library
- *    call.  Every call clears the used part of the array with
- *    cudaMemsetAsync on s, then runs the decode kernels on s.
+ *    call.  Every call clears the array's status word and tile counters
+ *    (12 KB) with cudaMemsetAsync on s, then runs the decode kernels on s.
  *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *    (cudaGetSymbolAddress) with that device current and keeps it for the
+ *    process; make that first call before any stream capture.  After a
+ *    cudaDeviceReset the kept address is stale: the call is not supported
+ *    on a device that has been reset.
  *  - All calls share the one array: calls that overlap on the GPU (other
  *    streams, other host threads) race and give wrong results.  Serialise
  *    them, e.g. on one stream.

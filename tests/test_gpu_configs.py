@@ -79,8 +79,9 @@ def test_q2q4_prefill_layers_T4096():
     before each layer the sampled tokens' rows are replaced by the oracle
     chain's hidden state, so the oracle and the library see the same input
     for the compared rows while the other 4096 - n rows keep the library's own
-    chain and so its bucket sizes (up to all 4096 tokens on one expert)."""
-    T, NL, NS = 4096, 8, 24
+    chain and so its bucket sizes (up to all 4096 tokens on one expert).
+    256 seeded tokens per layer are compared."""
+    T, NL, NS = 4096, 8, 256
     layers = [FullLayer(0, 4, l) if l < 2 else FullLayer(0, 4, l, synth.Q4_K, synth.Q4_K) for l in range(NL)]
     rng = np.random.default_rng(4)
     s = np.array(sorted(set(rng.choice(T, NS, replace=False).tolist()) | {0, T - 1}))

@@ -3,8 +3,9 @@ large batches) against the CPU oracle, through the C ABI.
 
 The path rounds activations and dequantised weights to bf16 and accumulates
 in fp32 on the tensor cores, so the statement's prefill bound applies:
-relative L2 error <= 1e-2 per token.  Tokens are independent given the
-routing, so at full size the oracle recomputes a seeded sample of tokens."""
+relative L2 error <= 1e-2 per token.  The uniform-routing cases compare
+every token, so every bucket-row position inside a 128-row chunk and every
+chunk is checked; the special cases compare a seeded sample."""
 import numpy as np
 import pytest
 
@@ -58,8 +59,7 @@ def test_prefill_matches_oracle(layer_q2, T):
     ids, w, _, _ = oracle.route(x, synth.router(0, 3), synth.bias_normal(0, 3))
     got, st = _forward(layer_q2, x, ids, w)
     assert st == 0
-    s = _sample(T, 10, T)
-    _check_rows(got[s], layer_q2.oracle(x[s], ids[s], w[s]))
+    _check_rows(got, layer_q2.oracle(x, ids, w))
 
 
 def test_prefill_big_buckets_and_duplicates(layer_q2):

@@ -67,7 +67,7 @@ def test_reference_arm_line_on_rank0(monkeypatch):
     for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
         monkeypatch.delenv(k, raising=False)
     monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference", "--steps", "1", "--warmup", "0",
-                                      "--cpu-layers", "1"])
+                                      "--cpu-size", "1"])
     buf = io.StringIO()
     with contextlib.redirect_stdout(buf):
         bench.main()
