@@ -5,12 +5,14 @@
 //
 // One persistent CTA per SM, 18 warps: a producer warp, a control warp and
 // four consumer groups of four warps.  The work is cut into jobs of five
-// kinds — router rows, shared gate/up row pairs, shared down 4-row groups,
-// routed gate/up (slot, 16-row tile), routed down (slot, 16-row tile) — each
-// kind dealt round-robin over the CTAs (alternating direction per kind, so
-// per-CTA bytes balance).  Producer lane q feeds group q's two-slot
-// shared-memory ring with contiguous bulk copies of about 16 KB (a bulk copy
-// has a fixed cost, so pieces are kept large); the four lanes claim the
+// kinds — router rows, shared gate/up (16-row tile, 1024-column quarter),
+// shared down (16-row tile, 512-column quarter), routed gate/up (slot, 16-row
+// tile), routed down (slot, 16-row tile) — each kind dealt round-robin over
+// the CTAs (alternating direction per kind, so per-CTA bytes balance).
+// Producer lane q feeds group q's two-slot shared-memory ring with pieces of
+// about 16 KB (a copy has a fixed cost, so pieces are kept large): contiguous
+// bulk copies for the router rows and the packed experts, one 3-D tensor copy
+// per 16-row x 512-column tile of the row-major bf16 shared expert; the four lanes claim the
 // CTA's jobs of each kind from shared cursors, so a group that finishes early
 // takes more, and each picks its next job by readiness: router rows first;
 // routed gate/up as soon as the expert ids are known, alternating with shared
@@ -28,12 +30,14 @@
 //    routed-down piece carries a copy of that h (fp16 hi/lo scaled by a power
 //    of two per 16 entries, the 16-column sums and the scales, written by the
 //    gate/up jobs) next to its weights, so no CTA-wide transition is needed;
-//  - shared h: complete when its 1024 row pairs are stored; the control warp
-//    then copies it once into the CTA (over the activation, which every job
-//    that reads it has finished by then);
-//  - out: the four shared-down and six routed-down jobs of a 16-row output
-//    tile store partials; the last of the ten (a per-tile counter) sums them
-//    in a fixed order.
+//  - shared h: the four column quarters of a shared gate/up tile store
+//    partial sums; the last of the four (a per-tile counter) adds them in a
+//    fixed order and stores h of the tile's 16 rows; once all 128 tiles are
+//    stored the control warp copies h once into the CTA (over the bf16
+//    activation, which every job that reads it has finished by then);
+//  - out: the four shared-down quarters and six routed-down jobs of a 16-row
+//    output tile store partials; the last of the ten (a per-tile counter)
+//    sums them in a fixed order.
 // Every wait is bounded (~1 s); a timeout records DS4G_ETIMEOUT.
 //
 // Chained layers (ds4g_moe_decode_stack) launch each layer after the first as
@@ -45,11 +49,13 @@
 // article §2.1) run as rmsnorm + route + the decode path of the forward; the
 // fused layer that follows one of them is launched in plain stream order.
 //
-// Arithmetic: router and shared expert in fp32 FMA (bf16 weights widen
-// exactly); routed experts on mma.sync with exact codes (IQ2 grid value or
-// Q2_K quant as an fp16 subnormal, sign from the sign table) against the
-// activation as an fp16 hi + lo pair (h: scaled per 16 entries); block,
-// sub-block and h scales applied in fp32 to each 32- or 16-column partial.  The IQ2_XXS grid values must lie in
+// Arithmetic: router in fp32 FMA against the activation's fp16 hi + lo pair;
+// shared expert on mma.sync bf16 (weights as stored) against the activation,
+// or the shared h, as a bf16 hi + lo pair; routed experts on mma.sync with
+// exact codes (IQ2 grid value or Q2_K quant as an fp16 subnormal, sign from
+// the sign table) against the activation as an fp16 hi + lo pair (h: scaled
+// per 16 entries); block, sub-block and h scales applied in fp32 to each 32-
+// or 16-column partial.  The IQ2_XXS grid values must lie in
 // {8, 25, 43} (the format's magnitudes): the grid table holds, per row, 8
 // nibble codes that select the value bytes with one byte permute.
 #include "ds4g_internal.cuh"
@@ -72,14 +78,14 @@ constexpr int kMix = 1;                          // routed gate/up jobs between 
 
 // Jobs per kind and their pieces:
 //   router rows                         1 piece (16 KB fp32)
-//   shared gate/up row pairs            2 pieces (gate rows, up rows: 16 KB each)
-//   shared down 4-row groups            1 piece (16 KB)
+//   shared gate/up (tile, quarter)      4 pieces (gate, gate, up, up: 16 rows x 512 columns, 16 KB each)
+//   shared down (tile, quarter)         1 piece (16 rows x 512 columns, 16 KB)
 //   routed gate/up (slot, 16-row tile)  2 pieces (gate, up: 16 tile-blocks each)
 //   routed down (slot, 16-row tile)     1 piece (8 Q2_K tile-blocks + that slot's h)
 constexpr int kNPhase = 5;
 constexpr int kJR = kE;
-constexpr int kJSG = kF / 2;
-constexpr int kJSD = kH / 4;
+constexpr int kJSG = (kF / 16) * 4;   // shared gate/up: 128 tiles x 4 column quarters
+constexpr int kJSD = (kH / 16) * 4;   // shared down: 256 tiles x 4 column quarters
 constexpr int kJRG = kK * (kF / 16);
 constexpr int kJRD = kK * (kH / 16);
 constexpr int kTileParts = 4 + kK;      // jobs contributing to one 16-row output tile
@@ -94,11 +100,12 @@ struct D1Desc {
 // the last CTA of every launch resets it).
 struct D1Sync {
     uint32_t router_done;  // router logits stored
-    uint32_t sgu_done;     // shared gate/up row pairs stored
+    uint32_t sgu_done;     // shared gate/up tiles whose h is stored
     uint32_t exit_count;
     uint32_t pad0[5];
     uint32_t rgu_done[8];  // per routed slot: gate/up 16-row tiles stored
     uint32_t tile_cnt[kH / 16];
+    uint32_t sgu_cnt[kF / 16];   // per shared gate/up tile: column quarters stored
 };
 
 struct D1Args {
@@ -119,8 +126,9 @@ struct D1Args {
     D1Sync *sync;
     float *logits;         // [256]
     uint8_t *hr;           // [6][kHSlot]: fp16 h hi [2048], lo [2048], 16-col sums [128], scales [128] (fp32)
-    float *h_s;            // [2048]
-    float *p_s;            // [4096] shared-expert output
+    __nv_bfloat16 *hsb;    // [2][kHLd] shared h as bf16 hi, lo
+    float *sgu_part;       // [128 tiles][4 quarters][32]: gate (16 rows), up (16 rows) partial sums
+    float *p_s;            // [4][4096] shared-expert output, per column quarter
     float *p_r;            // [6][4096] weighted routed outputs
 };
 
@@ -130,8 +138,12 @@ constexpr uint32_t kOffRing = 0;
 constexpr uint32_t kOffDesc = kOffRing + kD1Slots * kD1Slot;
 constexpr uint32_t kOffGtab = kOffDesc + kD1Slots * 16;
 constexpr uint32_t kOffStab = kOffGtab + 256 * kRep * 4;
-constexpr uint32_t kOffXn = kOffStab + 128 * kRep * 8;   // x fp32; later the shared h (fp32)
-constexpr uint32_t kOffXq = kOffXn + kH * 4;
+constexpr int kXLd = kH + 8;                     // bf16 hi/lo rows of x (16-byte pad: no bank conflict)
+constexpr int kHLd = kF + 8;                     // bf16 hi/lo rows of the shared h
+constexpr uint32_t kOffXb = kOffStab + 128 * kRep * 8;   // x fp32 on arrival; then x bf16 hi/lo; then shared h
+constexpr uint32_t kXbBytes = 2 * kXLd * 2;
+static_assert(kXbBytes >= kH * 4 && kXbBytes >= 2 * kHLd * 2, "activation area");
+constexpr uint32_t kOffXq = kOffXb + kXbBytes;
 constexpr uint32_t kOffRed = kOffXq + 2 * kH * 2;
 constexpr uint32_t kOffWk = kOffRed + kNGrp * 2 * 128 * 4;
 constexpr uint32_t kOffIds = kOffWk + 32;
@@ -142,16 +154,17 @@ constexpr uint32_t kOffFlags = kOffBar + (2 * kD1Slots + 2) * 8;
 constexpr uint32_t kOffJc = kOffFlags + 32;      // per kind: the CTA's next unclaimed job
 constexpr size_t kD1SmemBytes = kOffJc + 32;
 static_assert(kD1SmemBytes <= 232448, "shared memory");
-static_assert((kOffXn % 128) == 0 && (kOffEptr % 8) == 0 && (kOffBar % 8) == 0, "alignment");
+static_assert((kOffXb % 128) == 0 && (kOffXq % 16) == 0 && (kOffEptr % 8) == 0 && (kOffBar % 8) == 0, "alignment");
 
 struct D1Smem {
     uint8_t *ring;
     D1Desc *desc;
     uint32_t *gtab;        // [256][kRep] nibble codes of the grid row's 8 values
     uint2 *stab;           // [128][kRep] sign bytes (bit 7 of each byte) of the 8 values
-    float *xn;             // [4096] normalised activation (router, shared gate/up)
-    float *hs;             // [2048] shared h (same memory as xn, once xn is dead)
-    __half *xq;            // [2][4096] activation hi, lo
+    float *xraw;           // [4096] input activation as it arrives (fp32)
+    __nv_bfloat16 *xb;     // [2][kXLd] normalised activation, bf16 hi, lo (shared gate/up), over xraw
+    __nv_bfloat16 *hs;     // [2][kHLd] shared h, bf16 hi, lo (same memory, once xb is dead)
+    __half *xq;            // [2][4096] normalised activation, fp16 hi, lo (router, routed gate/up)
     float *red;            // [4 groups][2][128]
     float *wk;             // [6]
     int *ids_s;            // [6]
@@ -170,8 +183,9 @@ __device__ __forceinline__ D1Smem d1_smem() {
     s.desc = reinterpret_cast<D1Desc *>(d1_raw + kOffDesc);
     s.gtab = reinterpret_cast<uint32_t *>(d1_raw + kOffGtab);
     s.stab = reinterpret_cast<uint2 *>(d1_raw + kOffStab);
-    s.xn = reinterpret_cast<float *>(d1_raw + kOffXn);
-    s.hs = s.xn;
+    s.xraw = reinterpret_cast<float *>(d1_raw + kOffXb);
+    s.xb = reinterpret_cast<__nv_bfloat16 *>(d1_raw + kOffXb);
+    s.hs = s.xb;
     s.xq = reinterpret_cast<__half *>(d1_raw + kOffXq);
     s.red = reinterpret_cast<float *>(d1_raw + kOffRed);
     s.wk = reinterpret_cast<float *>(d1_raw + kOffWk);
@@ -266,40 +280,6 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// Warp totals of two per-lane values: lanes 0-15 end with the total of a0,
-// lanes 16-31 with the total of a1.
-__device__ __forceinline__ float warp_sum2(float a0, float a1, int lane) {
-    const bool up = lane & 16;
-    float m = up ? a1 : a0;
-    m += __shfl_xor_sync(0xffffffffu, up ? a0 : a1, 16);
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) m += __shfl_xor_sync(0xffffffffu, m, o);
-    return m;
-}
-// Warp totals of four per-lane values: lanes 8r .. 8r+7 end with the total of a_r.
-__device__ __forceinline__ float warp_sum4(float a0, float a1, float a2, float a3, int lane) {
-    const bool up = lane & 16, mid = lane & 8;
-    float k0 = up ? a2 : a0, k1 = up ? a3 : a1;
-    k0 += __shfl_xor_sync(0xffffffffu, up ? a0 : a2, 16);
-    k1 += __shfl_xor_sync(0xffffffffu, up ? a1 : a3, 16);
-    float m = mid ? k1 : k0;
-    m += __shfl_xor_sync(0xffffffffu, mid ? k0 : k1, 8);
-#pragma unroll
-    for (int o = 4; o > 0; o >>= 1) m += __shfl_xor_sync(0xffffffffu, m, o);
-    return m;
-}
-
-// bf16 x 8 (one uint4) dotted with 8 fp32 values
-__device__ __forceinline__ float dot8_bf16(uint4 wv, const float *xv, float acc) {
-    const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        acc = fmaf(__uint_as_float(wd[i] << 16), xv[2 * i], acc);
-        acc = fmaf(__uint_as_float(wd[i] & 0xffff0000u), xv[2 * i + 1], acc);
-    }
-    return acc;
-}
-
 // 16-byte shared-memory load by the lanes where `pred` holds; zeros elsewhere
 // (the others issue no access).
 __device__ __forceinline__ uint4 lds128_if(const void *p, bool pred) {
@@ -322,43 +302,67 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 }
 
 // ------------------------------------------------------ piece consumers
-// A router row (4096 fp32) against xn: warp wq takes columns [1024 wq, +1024);
-// returns this lane's partial.
+// A router row (4096 fp32) against the activation x = hi + lo (fp16 pair):
+// warp wq takes columns [1024 wq, +1024); returns this lane's partial.
 __device__ __forceinline__ float router_row(const D1Smem &sm, const uint8_t *slot, int wq, int lane) {
     const float4 *r = reinterpret_cast<const float4 *>(slot) + 256 * wq + lane;
-    const float4 *x = reinterpret_cast<const float4 *>(sm.xn) + 256 * wq + lane;
+    const uint2 *xh = reinterpret_cast<const uint2 *>(sm.xq) + 256 * wq + lane;
+    const uint2 *xl = reinterpret_cast<const uint2 *>(sm.xq + kH) + 256 * wq + lane;
     float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const float4 rv = r[32 * i], xv = x[32 * i];
+        const float4 rv = r[32 * i];
+        const uint2 h = xh[32 * i], l = xl[32 * i];
+        const float2 h01 = __half22float2(*reinterpret_cast<const __half2 *>(&h.x));
+        const float2 h23 = __half22float2(*reinterpret_cast<const __half2 *>(&h.y));
+        const float2 l01 = __half22float2(*reinterpret_cast<const __half2 *>(&l.x));
+        const float2 l23 = __half22float2(*reinterpret_cast<const __half2 *>(&l.y));
         float &acc = (i & 1) ? acc1 : acc0;
-        acc = fmaf(rv.x, xv.x, acc);
-        acc = fmaf(rv.y, xv.y, acc);
-        acc = fmaf(rv.z, xv.z, acc);
-        acc = fmaf(rv.w, xv.w, acc);
+        acc = fmaf(rv.x, h01.x + l01.x, acc);
+        acc = fmaf(rv.y, h01.y + l01.y, acc);
+        acc = fmaf(rv.z, h23.x + l23.x, acc);
+        acc = fmaf(rv.w, h23.y + l23.y, acc);
     }
     return acc0 + acc1;
 }
 
-// Rows w and w + ld (bf16, smem) against v (fp32, smem), 8 columns per step
-// at 8 * (lane + 32 i): this lane's partials.  Each v load serves both rows.
-template <int kSteps>
-__device__ __forceinline__ void bf16_rows2(const __nv_bfloat16 *w, int ld, const float *v, int lane, float &s0,
-                                           float &s1) {
-    float a0 = 0.f, a1 = 0.f;
+// First 1024-byte-aligned byte of a ring slot: where a tensor copy with the
+// 128-byte swizzle lands (the swizzle pattern repeats every 1024 bytes).
+__device__ __forceinline__ uint8_t *slot_al1024(uint8_t *slot) {
+    return slot + ((1024u - (tc::smem_u32(slot) & 1023u)) & 1023u);
+}
+
+// A 16-row x 512-column bf16 piece as the row-tile tensor map lands it:
+// [8 chunks][16 rows][64 columns], each row of a chunk one 128-byte line whose
+// 16-byte units are rotated by (row & 7).  Warp wq multiplies chunks 2wq and
+// 2wq + 1 by the vector v (bf16 hi at v, lo at v + vld; entries col0 + 64c ..)
+// on mma.sync.  Inside a chunk the k order is permuted so that lane t reads 16
+// contiguous columns (16t .. 16t + 15; k-slice s takes 16t + 4s .. +3), the
+// same permutation on both operands.  B holds v hi in column 0 and v lo in
+// column 1 (lanes with g < 2 load them, the others hold zeros), so c
+// accumulates, in lanes t == 0: c[0] + c[1] = row g, c[2] + c[3] = row g + 8.
+__device__ __forceinline__ void bf16_piece_mma(const uint8_t *piece, const __nv_bfloat16 *v, int vld, int col0,
+                                               int wq, int lane, float (&c)[4]) {
+    const int g = lane >> 2, t = lane & 3;
+    const __nv_bfloat16 *vb = v + (g & 1) * vld + col0 + 16 * t;
 #pragma unroll
-    for (int i = 0; i < kSteps; ++i) {
-        const int c = 8 * (lane + 32 * i);
-        const uint4 w0 = *reinterpret_cast<const uint4 *>(w + c);
-        const uint4 w1 = *reinterpret_cast<const uint4 *>(w + ld + c);
-        float xv[8];
-        *reinterpret_cast<float4 *>(xv) = *reinterpret_cast<const float4 *>(v + c);
-        *reinterpret_cast<float4 *>(xv + 4) = *reinterpret_cast<const float4 *>(v + c + 4);
-        a0 = dot8_bf16(w0, xv, a0);
-        a1 = dot8_bf16(w1, xv, a1);
+    for (int cc = 0; cc < 2; ++cc) {
+        const int ch = 2 * wq + cc;
+        const uint8_t *la = piece + (ch * 16 + g) * 128;
+        const uint8_t *lb = la + 8 * 128;
+        const uint4 a0 = *reinterpret_cast<const uint4 *>(la + (((2 * t) ^ g) << 4));
+        const uint4 a1 = *reinterpret_cast<const uint4 *>(la + (((2 * t + 1) ^ g) << 4));
+        const uint4 b0 = *reinterpret_cast<const uint4 *>(lb + (((2 * t) ^ g) << 4));
+        const uint4 b1 = *reinterpret_cast<const uint4 *>(lb + (((2 * t + 1) ^ g) << 4));
+        const uint4 x0 = lds128_if(vb + 64 * ch, g < 2);
+        const uint4 x1 = lds128_if(vb + 64 * ch + 8, g < 2);
+        const uint32_t ra[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const uint32_t rb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        const uint32_t rx[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+        for (int sl = 0; sl < 4; ++sl)
+            mma_bf16(c, ra[2 * sl], rb[2 * sl], ra[2 * sl + 1], rb[2 * sl + 1], rx[2 * sl], rx[2 * sl + 1]);
     }
-    s0 = a0;
-    s1 = a1;
 }
 
 __device__ __forceinline__ uint32_t bfe7(uint32_t v, uint32_t pos) {
@@ -500,18 +504,19 @@ __device__ __forceinline__ int phase_jobs(int p) {
     return p == 0 ? kJR : p == 1 ? kJSG : p == 2 ? kJSD : p == 3 ? kJRG : kJRD;
 }
 __device__ __forceinline__ int phase_off(int p, int c, int G) { return (p & 1) ? (G - 1 - c) : c; }
-__device__ __forceinline__ int phase_pieces(int p) { return (p == 1 || p == 3) ? 2 : 1; }
+__device__ __forceinline__ int phase_pieces(int p) { return p == 1 ? 4 : p == 3 ? 2 : 1; }
 
 // If this warp's counted job was the last of its 16-row output tile (the
 // counter returned kTileParts - 1), sum the tile's partials in a fixed order:
-// shared expert, then routed experts k = 0..5.
+// the shared expert's four column quarters, then routed experts k = 0..5.
 __device__ __forceinline__ void finish_tile(const D1Args &a, int tile, uint32_t old_lane0, int lane) {
     if (tile < 0) return;
     const uint32_t old = __shfl_sync(0xffffffffu, old_lane0, 0);
     if (old != kTileParts - 1) return;
     if (lane < 16) {
         const int row = 16 * tile + lane;
-        float v = __ldcg(a.p_s + row);
+        float v = (__ldcg(a.p_s + row) + __ldcg(a.p_s + kH + row)) +
+                  (__ldcg(a.p_s + 2 * kH + row) + __ldcg(a.p_s + 3 * kH + row));
 #pragma unroll
         for (int k = 0; k < kK; ++k) v += __ldcg(a.p_r + (size_t)k * kH + row);
         a.out[row] = v;
@@ -550,7 +555,7 @@ __device__ __forceinline__ void d1_control(const D1Args &a, const D1Smem &sm, in
     if (a.pdl) asm volatile("griddepcontrol.wait;" ::: "memory");
     if (lane == 0) {
         tc::mbar_arrive_expect_tx(sm.xbar, kH * 4);
-        bulk_load(sm.xn, a.x, kH * 4, sm.xbar);
+        bulk_load(sm.xraw, a.x, kH * 4, sm.xbar);
     }
     bool ok = true;
     if (lane == 0) ok = spin_geq(&a.sync->router_done, (uint32_t)kJR, abort_flag);
@@ -624,16 +629,17 @@ __device__ __forceinline__ void d1_control(const D1Args &a, const D1Smem &sm, in
     // readiness: lane 0 the shared h, lanes 1..6 routed slots 0..5
     bool pending = lane <= kK;
     const uint32_t *ctr = lane == 0 ? &a.sync->sgu_done : &a.sync->rgu_done[(lane >= 1 && lane <= kK) ? lane - 1 : 0];
-    const uint32_t target = lane == 0 ? (uint32_t)kJSG : (uint32_t)(kF / 16);
+    const uint32_t target = (uint32_t)(kF / 16);   // shared gate/up tiles, or one slot's routed tiles
     const long long t0 = clock64();
     while (__any_sync(0xffffffffu, pending)) {
         if (pending && ld_acquire(ctr) >= target) {
             pending = false;
             if (lane == 0) {
-                // every job that reads xn has finished: the shared h may overwrite it
+                // every job that reads the bf16 activation has finished: the
+                // shared h may overwrite it
                 fence_proxy_async_global();
-                tc::mbar_arrive_expect_tx(sm.hsbar, kF * 4);
-                bulk_load(sm.hs, a.h_s, kF * 4, sm.hsbar);
+                tc::mbar_arrive_expect_tx(sm.hsbar, 2 * kHLd * 2);
+                bulk_load(sm.hs, a.hsb, 2 * kHLd * 2, sm.hsbar);
                 __threadfence_block();
                 *reinterpret_cast<volatile int *>(&sm.flags[2]) = 1;
             } else {
@@ -651,8 +657,11 @@ __device__ __forceinline__ void d1_control(const D1Args &a, const D1Smem &sm, in
 }
 
 // ------------------------------------------------------------ kernel
-__global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
+__global__ void __launch_bounds__(kD1Threads, 1)
+    decode_t1_kernel(const __grid_constant__ CUtensorMap tmSG, const __grid_constant__ CUtensorMap tmSU,
+                     const __grid_constant__ CUtensorMap tmSD, D1Args a) {
     const D1Smem sm = d1_smem();
+    const CUtensorMap *tm_sg = &tmSG, *tm_su = &tmSU, *tm_sd = &tmSD;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, c = blockIdx.x;
     volatile int *abort_flag = sm.flags;
@@ -664,6 +673,9 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
         }
         tc::mbar_init(sm.xbar, 1);
         tc::mbar_init(sm.hsbar, 1);
+        tc::prefetch_tmap(tm_sg);
+        tc::prefetch_tmap(tm_su);
+        tc::prefetch_tmap(tm_sd);
         for (int i = 0; i < 8; ++i) sm.flags[i] = 0;
         for (int i = 0; i < 8; ++i) sm.jc[i] = 0;
         tc::fence_mbar_init();
@@ -686,7 +698,7 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
             }
             volatile int *jc = sm.jc;
             uint32_t itq = 0, seen = 0;
-            int pend_p = -1, pend_j = 0, turn = 0;
+            int pend_p = -1, pend_j = 0, pend_pc = 0, turn = 0;
             int held = -1;   // a claimed routed-down job whose slot's h is not complete yet
             long long t_idle = clock64();
             while (true) {
@@ -696,10 +708,10 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
                 int p = -1, j = 0, pc = 0;
                 if (!stalled) {
                     if (pend_p >= 0) {
-                        // second piece of a two-piece job
+                        // next piece of a job of several pieces
                         p = pend_p;
                         j = pend_j;
-                        pc = 1;
+                        pc = pend_pc;
                     } else {
                         const int ids = *reinterpret_cast<volatile int *>(&sm.flags[1]);
                         const int hs_ok = *reinterpret_cast<volatile int *>(&sm.flags[2]);
@@ -773,19 +785,26 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
                 d.piece = pc;
                 d.e = 0;
                 const void *src = nullptr, *src2 = nullptr;
+                const CUtensorMap *tmap = nullptr;   // shared-expert pieces: one 3-D tensor copy
+                int trow = 0, tchunk = 0;
                 uint32_t bytes = 0;
                 if (p == 0) {
                     d.kind = PK_ROUTER;
                     src = a.router + (size_t)j * kH;
                     bytes = kH * 4;
                 } else if (p == 1) {
+                    // 16 rows x 512 columns of gate (pieces 0, 1) or up (2, 3)
                     d.kind = PK_SGU;
-                    src = (pc ? a.sh_up : a.sh_gate) + (size_t)(2 * j) * kH;
-                    bytes = 2 * kH * 2;
+                    tmap = pc < 2 ? tm_sg : tm_su;
+                    trow = 16 * (j >> 2);
+                    tchunk = 16 * (j & 3) + 8 * (pc & 1);
+                    bytes = 16 * 512 * 2;
                 } else if (p == 2) {
                     d.kind = PK_SDN;
-                    src = a.sh_down + (size_t)(4 * j) * kF;
-                    bytes = 4 * kF * 2;
+                    tmap = tm_sd;
+                    trow = 16 * (j >> 2);
+                    tchunk = 8 * (j & 3);
+                    bytes = 16 * 512 * 2;
                 } else if (p == 3) {
                     d.kind = PK_RGU;
                     const int k = j / (kF / 16), tile = j % (kF / 16);
@@ -813,7 +832,10 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
                     }
                 }
                 sm.desc[s] = d;
-                if (bytes) {
+                if (tmap) {
+                    tc::mbar_arrive_expect_tx(&sm.full[s], bytes);
+                    tc::tma_load_3d(slot_al1024(dst), tmap, 0, trow, tchunk, &sm.full[s]);
+                } else if (bytes) {
                     tc::mbar_arrive_expect_tx(&sm.full[s], bytes + (src2 ? (uint32_t)kHSlot : 0u));
                     bulk_load(dst, src, bytes, &sm.full[s]);
                     if (src2) bulk_load(dst + kRdnW, src2, kHSlot, &sm.full[s]);
@@ -821,8 +843,9 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
                     tc::mbar_arrive(&sm.full[s]);
                 }
                 ++itq;
-                pend_p = (phase_pieces(p) == 2 && pc == 0) ? p : -1;
+                pend_p = pc + 1 < phase_pieces(p) ? p : -1;
                 pend_j = j;
+                pend_pc = pc + 1;
                 t_idle = clock64();
             }
             // The last piece issued into each of the group's slots has landed
@@ -879,7 +902,7 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
         if (!d1_wait(sm.xbar, 0, abort_flag)) d1_abort(a, sm.flags, 0x20u);
         float xv[8], ss = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) xv[i] = sm.xn[ct + 512 * i];
+        for (int i = 0; i < 8; ++i) xv[i] = sm.xraw[ct + 512 * i];
 #pragma unroll
         for (int i = 0; i < 8; ++i) ss = fmaf(xv[i], xv[i], ss);
         ss = warp_sum(ss);
@@ -893,16 +916,19 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
         for (int i = 0; i < 8; ++i) {
             const float v = xv[i] * r;
             if (!(fabsf(v) < 65504.f)) flag_status(a.status, DS4G_EDEVICE, 0xF16u);
-            sm.xn[ct + 512 * i] = v;
             __half hi, lo;
             split_f16(v, hi, lo);
             sm.xq[ct + 512 * i] = hi;
             sm.xq[kH + ct + 512 * i] = lo;
+            __nv_bfloat16 bh, bl;
+            split_bf16(v, bh, bl);
+            sm.xb[ct + 512 * i] = bh;   // over xraw: every thread read its values before the barrier above
+            sm.xb[kXLd + ct + 512 * i] = bl;
         }
         asm volatile("bar.sync 1, %0;" ::"n"(kD1Cons * 32));
 
         float rg0 = 0.f, rg1 = 0.f, ru0 = 0.f, ru1 = 0.f; // routed gate/up partials, rows g, g+8
-        float sg0 = 0.f, sg1 = 0.f;                       // shared gate partials, rows 2j, 2j+1
+        float cg[4] = {0.f, 0.f, 0.f, 0.f}, cu[4] = {0.f, 0.f, 0.f, 0.f};   // shared gate/up accumulators
         int pend_tile = -1;                               // tile counted by this warp, not yet examined
         uint32_t pend_old = 0u;
         bool hs_ok = false;
@@ -931,18 +957,21 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
                 if (lane == 0) red[wq] = v;
                 last = true;
             } else if (d.kind == PK_SGU) {
-                // gate (piece 0) or up (piece 1) rows 2j, 2j+1; warp wq: columns [1024 wq, +1024)
-                float a0, a1;
-                bf16_rows2<4>(reinterpret_cast<const __nv_bfloat16 *>(slot) + 1024 * wq, kH, sm.xn + 1024 * wq,
-                              lane, a0, a1);
+                // pieces 0, 1: gate rows of the tile, columns 1024 kq + 512 piece;
+                // pieces 2, 3: up rows, same columns
                 if (d.piece == 0) {
-                    sg0 = a0;
-                    sg1 = a1;
-                } else {
-                    const float gsum = warp_sum2(sg0, sg1, lane), usum = warp_sum2(a0, a1, lane);
-                    if ((lane & 15) == 0) {
-                        red[2 * wq + (lane >> 4)] = gsum;
-                        red[8 + 2 * wq + (lane >> 4)] = usum;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) cg[i] = cu[i] = 0.f;
+                }
+                const int col0 = 1024 * (d.job & 3) + 512 * (d.piece & 1);
+                if (d.piece < 2) bf16_piece_mma(slot_al1024(const_cast<uint8_t *>(slot)), sm.xb, kXLd, col0, wq, lane, cg);
+                else bf16_piece_mma(slot_al1024(const_cast<uint8_t *>(slot)), sm.xb, kXLd, col0, wq, lane, cu);
+                if (d.piece == 3) {
+                    if ((lane & 3) == 0) {
+                        red[wq * 32 + (lane >> 2)] = cg[0] + cg[1];
+                        red[wq * 32 + 8 + (lane >> 2)] = cg[2] + cg[3];
+                        red[wq * 32 + 16 + (lane >> 2)] = cu[0] + cu[1];
+                        red[wq * 32 + 24 + (lane >> 2)] = cu[2] + cu[3];
                     }
                     last = true;
                 }
@@ -970,14 +999,13 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
                     last = true;
                 }
             } else if (d.kind == PK_SDN) {
-                // shared down rows 4j .. 4j+3; warp wq: columns [512 wq, +512) of all four
-                const __nv_bfloat16 *w = reinterpret_cast<const __nv_bfloat16 *>(slot) + 512 * wq;
-                const float *hv = sm.hs + 512 * wq;
-                float a0, a1, a2, a3;
-                bf16_rows2<2>(w, kF, hv, lane, a0, a1);
-                bf16_rows2<2>(w + 2 * kF, kF, hv, lane, a2, a3);
-                const float v = warp_sum4(a0, a1, a2, a3, lane);
-                if ((lane & 7) == 0) red[4 * wq + (lane >> 3)] = v;
+                // shared down: 16 rows of the output tile, columns 512 kq .. +512 of h
+                float c[4] = {0.f, 0.f, 0.f, 0.f};
+                bf16_piece_mma(slot_al1024(const_cast<uint8_t *>(slot)), sm.hs, kHLd, 512 * (d.job & 3), wq, lane, c);
+                if ((lane & 3) == 0) {
+                    red[wq * 16 + (lane >> 2)] = c[0] + c[1];
+                    red[wq * 16 + 8 + (lane >> 2)] = c[2] + c[3];
+                }
                 last = true;
             } else {  // PK_RDN: eight Q2_K tile-blocks of one expert; warp wq: tile-blocks 2wq, 2wq+1
                 float s0 = 0.f, s1 = 0.f;
@@ -1013,13 +1041,35 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
                         red_add_release(&a.sync->router_done, 1u);
                     }
                 } else if (d.kind == PK_SGU) {
-                    if (lane < 2) {
-                        const float gs = (red[lane] + red[2 + lane]) + (red[4 + lane] + red[6 + lane]);
-                        const float us = (red[8 + lane] + red[10 + lane]) + (red[12 + lane] + red[14 + lane]);
-                        a.h_s[2 * d.job + lane] = silu_f(gs) * us;
-                    }
+                    // partial sums of this column quarter (16 gate rows, 16 up rows);
+                    // the last of the tile's four quarters adds them in order and
+                    // stores h of the 16 rows as bf16 hi, lo
+                    const int rt = d.job >> 2, kq = d.job & 3;
+                    const float v = (red[lane] + red[32 + lane]) + (red[64 + lane] + red[96 + lane]);
+                    a.sgu_part[(size_t)(rt * 4 + kq) * 32 + lane] = v;
                     __syncwarp();
-                    if (lane == 0) red_add_release(&a.sync->sgu_done, 1u);
+                    uint32_t old = 0u;
+                    if (lane == 0) old = atom_add_acq_rel(&a.sync->sgu_cnt[rt], 1u);
+                    old = __shfl_sync(0xffffffffu, old, 0);
+                    __syncwarp();   // the other lanes' reads below follow lane 0's acquire
+                    if (old == 3u) {
+                        if (lane < 16) {
+                            const float *pp = a.sgu_part + (size_t)rt * 128;
+                            const float gs = (__ldcg(pp + lane) + __ldcg(pp + 32 + lane)) +
+                                             (__ldcg(pp + 64 + lane) + __ldcg(pp + 96 + lane));
+                            const float us = (__ldcg(pp + 16 + lane) + __ldcg(pp + 48 + lane)) +
+                                             (__ldcg(pp + 80 + lane) + __ldcg(pp + 112 + lane));
+                            __nv_bfloat16 hi, lo;
+                            split_bf16(silu_f(gs) * us, hi, lo);
+                            a.hsb[16 * rt + lane] = hi;
+                            a.hsb[kHLd + 16 * rt + lane] = lo;
+                        }
+                        __syncwarp();
+                        if (lane == 0) {
+                            a.sync->sgu_cnt[rt] = 0u;   // all four quarters arrived: ready for the next launch
+                            red_add_release(&a.sync->sgu_done, 1u);
+                        }
+                    }
                 } else if (d.kind == PK_RGU) {
                     // h of 16 rows of slot k: fp16 hi/lo of 2^-e h (one power of two
                     // per 16 entries, so any finite h fits), the 16-column sum of h
@@ -1056,9 +1106,11 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
                     __syncwarp();
                     if (lane == 0) red_add_release(&a.sync->rgu_done[k], 1u);
                 } else if (d.kind == PK_SDN) {
-                    if (lane < 4)
-                        a.p_s[4 * d.job + lane] = (red[lane] + red[4 + lane]) + (red[8 + lane] + red[12 + lane]);
-                    tile = (4 * d.job) / 16;
+                    const int ot = d.job >> 2, kq = d.job & 3;
+                    if (lane < 16)
+                        a.p_s[(size_t)kq * kH + 16 * ot + lane] =
+                            (red[lane] + red[16 + lane]) + (red[32 + lane] + red[48 + lane]);
+                    tile = ot;
                 } else {  // routed down partial of one expert, weighted
                     const int k = d.job / (kH / 16), tl = d.job % (kH / 16);
                     if (lane < 16) {
@@ -1102,7 +1154,7 @@ __global__ void __launch_bounds__(kD1Threads, 1) decode_t1_kernel(D1Args a) {
 
 // ------------------------------------------------------------------ host
 struct D1Layout {
-    size_t sync, logits, hr, h_s, p_s, p_r, total;
+    size_t sync, logits, hr, hsb, sgu_part, p_s, p_r, total;
 };
 static_assert(sizeof(D1Sync) <= kWsD1SyncBytes, "coordination block exceeds its area");
 static D1Layout d1_layout() {
@@ -1113,10 +1165,12 @@ static D1Layout d1_layout() {
     off += align_up(kE * 4, 256);
     L.hr = off;
     off += align_up((size_t)kK * kHSlot, 256);
-    L.h_s = off;
-    off += align_up((size_t)kF * 4, 256);
+    L.hsb = off;
+    off += align_up((size_t)2 * kHLd * 2, 256);
+    L.sgu_part = off;
+    off += align_up((size_t)(kF / 16) * 4 * 32 * 4, 256);
     L.p_s = off;
-    off += align_up((size_t)kH * 4, 256);
+    off += align_up((size_t)4 * kH * 4, 256);
     L.p_r = off;
     off += align_up((size_t)kK * kH * 4, 256);
     L.total = off;
@@ -1254,7 +1308,8 @@ static D1Args d1_args(const float *hidden, int normalize, const float *router, c
     a.sync = (D1Sync *)(ws + lay.sync);
     a.logits = (float *)(ws + lay.logits);
     a.hr = ws + lay.hr;
-    a.h_s = (float *)(ws + lay.h_s);
+    a.hsb = (__nv_bfloat16 *)(ws + lay.hsb);
+    a.sgu_part = (float *)(ws + lay.sgu_part);
     a.p_s = (float *)(ws + lay.p_s);
     a.p_r = (float *)(ws + lay.p_r);
     return a;
@@ -1275,7 +1330,12 @@ static ds4g_status d1_launch(const D1Args &a, cudaStream_t s, bool pdl) {
     cfg.numAttrs = pdl ? 1 : 0;
     D1Args b = a;
     b.pdl = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, decode_t1_kernel, b) == cudaSuccess ? DS4G_OK : DS4G_ECUDA;
+    // shared-expert pieces: 16 rows x 512 columns (8 chunks of 64) per tensor copy
+    CUtensorMap mg, mu, md;
+    if (!tmap_bf16_rowtile(&mg, a.sh_gate, kF, kH, 16, 8) || !tmap_bf16_rowtile(&mu, a.sh_up, kF, kH, 16, 8) ||
+        !tmap_bf16_rowtile(&md, a.sh_down, kH, kF, 16, 8))
+        return DS4G_ECUDA;
+    return cudaLaunchKernelEx(&cfg, decode_t1_kernel, mg, mu, md, b) == cudaSuccess ? DS4G_OK : DS4G_ECUDA;
 }
 
 }  // namespace ds4g

@@ -62,7 +62,7 @@ constexpr size_t kWsHeader = 256;
 // counters at zero, and no path writes scratch below kWsScratch, so one
 // zeroed workspace serves any sequence of calls and token counts.
 constexpr size_t kWsD1Sync = kWsHeader;                      // decode1.cu coordination block
-constexpr size_t kWsD1SyncBytes = 1280;
+constexpr size_t kWsD1SyncBytes = 2048;
 constexpr size_t kWsDecCnt = kWsD1Sync + kWsD1SyncBytes;     // decode.cu tile counters
 constexpr size_t kWsDecCntBytes = 10752;
 constexpr size_t kWsScratch = kWsDecCnt + kWsDecCntBytes;    // first byte of any path's scratch
