@@ -76,6 +76,7 @@ def lib():
             "ds4g_moe_decode_stack": ([vp, i, C.POINTER(vp), C.POINTER(vp), C.POINTER(ds4g_layer), vp, vp, vp, vp,
                                        vp, sz, vp], i),
             "ds4g_moe_forward_noalloc": ([vp, i, C.POINTER(ds4g_layer), vp, vp, vp, vp], i),
+            "ds4g_test_force_timeout": ([i], None),
             "ds4g_expert_cache_pool_bytes": ([i, i, i], sz),
             "ds4g_expert_cache_create": ([i, i, i, i, vp, sz, C.POINTER(vp)], i),
             "ds4g_expert_cache_destroy": ([vp], i),
@@ -255,6 +256,12 @@ def ds4g_moe_forward_noalloc(hidden, layer: ds4g_layer, ids, w, out, stream=None
     _check("ds4g_moe_forward_noalloc",
            lib().ds4g_moe_forward_noalloc(_ptr(hidden), T, C.byref(layer), _ptr(ids), _ptr(w), _ptr(out),
                                           _stream(stream)))
+
+
+def ds4g_test_force_timeout(on: bool):
+    """Test hook: while on, fused layer launches wait for logits that never
+    arrive and give up after ~130 us with DS4G_ETIMEOUT."""
+    lib().ds4g_test_force_timeout(1 if on else 0)
 
 
 class HostExperts:

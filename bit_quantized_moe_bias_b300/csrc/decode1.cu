@@ -112,6 +112,8 @@ struct D1Args {
     const float *x;
     int normalize;
     int pdl;
+    uint32_t router_extra;  // 0; 1 only under the test hook (waits for a router row that does not exist)
+    long long router_limit; // clock cycles the control warp waits for the router logits
     const float *router;   // [256][4096]
     const float *bias;     // [256]
     int32_t *ids;          // [6] out
@@ -233,14 +235,15 @@ __device__ __forceinline__ void red_add_release(uint32_t *p, uint32_t v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Bounded spin until *p >= target.  Returns false on timeout or abort.
-__device__ __noinline__ bool spin_geq(const uint32_t *p, uint32_t target, volatile int *abort_flag) {
+// Bounded spin until *p >= target.  Returns false after `limit` clock
+// cycles or on abort.
+__device__ __noinline__ bool spin_geq(const uint32_t *p, uint32_t target, volatile int *abort_flag, long long limit) {
     const long long t0 = clock64();
     while (true) {
         for (int i = 0; i < 32; ++i)
             if (ld_acquire(p) >= target) return true;
         if (*abort_flag) return false;
-        if (clock64() - t0 > (2ll << 30)) return false;  // ~1 s
+        if (clock64() - t0 > limit) return false;
         __nanosleep(64);
     }
 }
@@ -558,7 +561,7 @@ __device__ __forceinline__ void d1_control(const D1Args &a, const D1Smem &sm, in
         bulk_load(sm.xraw, a.x, kH * 4, sm.xbar);
     }
     bool ok = true;
-    if (lane == 0) ok = spin_geq(&a.sync->router_done, (uint32_t)kJR, abort_flag);
+    if (lane == 0) ok = spin_geq(&a.sync->router_done, (uint32_t)kJR + a.router_extra, abort_flag, a.router_limit);
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     __syncwarp();
     if (!ok) {
@@ -927,8 +930,9 @@ __global__ void __launch_bounds__(kD1Threads, 1)
         }
         asm volatile("bar.sync 1, %0;" ::"n"(kD1Cons * 32));
 
-        float rg0 = 0.f, rg1 = 0.f, ru0 = 0.f, ru1 = 0.f; // routed gate/up partials, rows g, g+8
-        float cg[4] = {0.f, 0.f, 0.f, 0.f}, cu[4] = {0.f, 0.f, 0.f, 0.f};   // shared gate/up accumulators
+        // accumulator of a gate/up job across its pieces: routed (gate rows g, g+8,
+        // up rows g, g+8) or shared (the mma accumulator of gate, then of up)
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
         int pend_tile = -1;                               // tile counted by this warp, not yet examined
         uint32_t pend_old = 0u;
         bool hs_ok = false;
@@ -959,42 +963,41 @@ __global__ void __launch_bounds__(kD1Threads, 1)
             } else if (d.kind == PK_SGU) {
                 // pieces 0, 1: gate rows of the tile, columns 1024 kq + 512 piece;
                 // pieces 2, 3: up rows, same columns
-                if (d.piece == 0) {
+                if (d.piece == 0 || d.piece == 2) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) cg[i] = cu[i] = 0.f;
+                    for (int i = 0; i < 4; ++i) acc[i] = 0.f;
                 }
                 const int col0 = 1024 * (d.job & 3) + 512 * (d.piece & 1);
-                if (d.piece < 2) bf16_piece_mma(slot_al1024(const_cast<uint8_t *>(slot)), sm.xb, kXLd, col0, wq, lane, cg);
-                else bf16_piece_mma(slot_al1024(const_cast<uint8_t *>(slot)), sm.xb, kXLd, col0, wq, lane, cu);
-                if (d.piece == 3) {
+                bf16_piece_mma(slot_al1024(const_cast<uint8_t *>(slot)), sm.xb, kXLd, col0, wq, lane, acc);
+                if (d.piece & 1) {
+                    // gate rows after piece 1, up rows after piece 3
+                    const int o = wq * 32 + (d.piece == 3 ? 16 : 0);
                     if ((lane & 3) == 0) {
-                        red[wq * 32 + (lane >> 2)] = cg[0] + cg[1];
-                        red[wq * 32 + 8 + (lane >> 2)] = cg[2] + cg[3];
-                        red[wq * 32 + 16 + (lane >> 2)] = cu[0] + cu[1];
-                        red[wq * 32 + 24 + (lane >> 2)] = cu[2] + cu[3];
+                        red[o + (lane >> 2)] = acc[0] + acc[1];
+                        red[o + 8 + (lane >> 2)] = acc[2] + acc[3];
                     }
-                    last = true;
+                    last = d.piece == 3;
                 }
             } else if (d.kind == PK_RGU) {
-                if (d.piece == 0) rg0 = rg1 = ru0 = ru1 = 0.f;
+                if (d.piece == 0) acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
                 if (d.e >= 0) {
                     float t0, t1, t2, t3;
                     iq2_tileblock2(sm, slot + (size_t)(4 * wq) * kTB_IQ2, 4 * wq, lane, t0, t1);
                     iq2_tileblock2(sm, slot + (size_t)(4 * wq + 2) * kTB_IQ2, 4 * wq + 2, lane, t2, t3);
                     if (d.piece) {
-                        ru0 += t0 + t2;
-                        ru1 += t1 + t3;
+                        acc[2] += t0 + t2;
+                        acc[3] += t1 + t3;
                     } else {
-                        rg0 += t0 + t2;
-                        rg1 += t1 + t3;
+                        acc[0] += t0 + t2;
+                        acc[1] += t1 + t3;
                     }
                 }
                 if (d.piece == 1) {
                     if ((lane & 3) == 0) {
-                        red[wq * 16 + (lane >> 2)] = rg0;
-                        red[wq * 16 + (lane >> 2) + 8] = rg1;
-                        red[64 + wq * 16 + (lane >> 2)] = ru0;
-                        red[64 + wq * 16 + (lane >> 2) + 8] = ru1;
+                        red[wq * 16 + (lane >> 2)] = acc[0];
+                        red[wq * 16 + (lane >> 2) + 8] = acc[1];
+                        red[64 + wq * 16 + (lane >> 2)] = acc[2];
+                        red[64 + wq * 16 + (lane >> 2) + 8] = acc[3];
                     }
                     last = true;
                 }
@@ -1144,6 +1147,7 @@ __global__ void __launch_bounds__(kD1Threads, 1)
             // every CTA has finished: reset the coordination block for the next launch
             a.sync->router_done = 0;
             a.sync->sgu_done = 0;
+            for (int t = 0; t < kF / 16; ++t) a.sync->sgu_cnt[t] = 0;   // already zero unless a launch gave up
             for (int k = 0; k < 8; ++k) a.sync->rgu_done[k] = 0;
             for (int t = 0; t < kH / 16; ++t) a.sync->tile_cnt[t] = 0;   // already zero unless a launch gave up
             __threadfence();
@@ -1209,6 +1213,7 @@ static bool d1_fused(const ds4g_layer *L) {
 
 static int g_d1_sms = 0;
 static bool g_d1_attr = false;
+static int g_d1_force_timeout = 0;   // test hook (ds4g_test_force_timeout)
 
 // Host checks shared by the single-layer and the stacked entry points.
 static ds4g_status d1_check(const float *hidden, const float *router, const float *bias, const ds4g_layer *L,
@@ -1292,6 +1297,10 @@ static D1Args d1_args(const float *hidden, int normalize, const float *router, c
     a.x = hidden;
     a.normalize = normalize ? 1 : 0;
     a.pdl = 0;
+    // under the test hook the control warp waits for one router row more
+    // than exists and gives up after ~130 us (2^18 cycles) instead of ~1 s
+    a.router_extra = g_d1_force_timeout ? 1u : 0u;
+    a.router_limit = g_d1_force_timeout ? (1ll << 18) : (2ll << 30);
     a.router = router;
     a.bias = bias;
     a.ids = ids;
@@ -1343,6 +1352,8 @@ static ds4g_status d1_launch(const D1Args &a, cudaStream_t s, bool pdl) {
 using namespace ds4g;
 
 extern "C" size_t ds4g_layer_decode_workspace(void) { return d1_layout().total; }
+
+extern "C" void ds4g_test_force_timeout(int on) { g_d1_force_timeout = on ? 1 : 0; }
 
 extern "C" size_t ds4g_decode_stack_workspace(void) { return stack_layout().total; }
 

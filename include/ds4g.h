@@ -311,6 +311,18 @@ ds4g_status ds4g_moe_decode_stack(const float *hidden, int n_layers, const float
                                   void *workspace, size_t ws_bytes, ds4g_stream_t s);
 
 /* ------------------------------------------------------------------------
+ * Test hook of the bounded waits (no counterpart in the pages: it exists to
+ * exercise DS4G_ETIMEOUT without hanging or faulting a GPU).  While on != 0,
+ * every launch of the fused layer kernel (ds4g_moe_layer_decode and the
+ * IQ2_XXS/Q2_K layers of ds4g_moe_decode_stack) makes its control warps wait
+ * for one router row more than the layer has, giving up after about 130 us:
+ * the launch aborts, drains its copies, records DS4G_ETIMEOUT in the
+ * workspace and leaves it usable.  Process-wide, host-side only;
+ * turn it off (0) to run normally.  Not for production use.
+ * ------------------------------------------------------------------------ */
+void ds4g_test_force_timeout(int on);
+
+/* ------------------------------------------------------------------------
  * ds4g_moe_forward without a workspace, for callers that cannot allocate
  * device memory: code running inside an allocator or memory-pool callback
  * (where calling cudaMalloc would re-enter the allocator), a real-time loop

@@ -224,3 +224,28 @@ def test_layer_decode_h_beyond_fp16_range():
     assert st == 0
     check_route(ids[None], w[None], ids_r, w_r, keys, margin)
     assert_close_fwd(out[None], oracle_forward(x, ids[None], w[None], hx, shared, grid))
+
+
+def test_layer_decode_bounded_wait_times_out_and_recovers():
+    """The control warps' wait for the router logits is bounded: under the test
+    hook they wait for a router row that does not exist, give up after ~130 us, abort
+    the launch (every CTA drains its copies) and record DS4G_ETIMEOUT; the
+    same workspace then gives the normal result, bit for bit equal to a
+    fresh workspace's."""
+    x = synth.hidden(9, 1, 1)
+    R, b = synth.router(9, 1), synth.bias_normal(9, 1)
+    ids_r, w_r, keys, margin = oracle.route(x, R, b)
+    L, hx, shared, grid = device_layer(9, 1, 0, ids_r.reshape(-1))
+    ws = B.workspace(B.ds4g_layer_decode_workspace())
+    B.ds4g_test_force_timeout(True)
+    try:
+        _, _, _, st = _run(x[0], R, b, L, ws, normalize=False)
+    finally:
+        B.ds4g_test_force_timeout(False)
+    assert st == 6                                    # DS4G_ETIMEOUT
+    ids, w, out, st = _run(x[0], R, b, L, ws, normalize=False)
+    assert st == 0
+    fresh = _run(x[0], R, b, L, B.workspace(B.ds4g_layer_decode_workspace()), normalize=False)
+    assert fresh[3] == 0 and np.array_equal(out, fresh[2]) and np.array_equal(ids, fresh[0])
+    check_route(ids[None], w[None], ids_r, w_r, keys, margin)
+    assert_close_fwd(out[None], oracle_forward(x, ids[None], w[None], hx, shared, grid))
