@@ -612,7 +612,7 @@ def run_batched(args, rank, world, local_rank):
     import bit_quantized_moe_bias_b300 as B
     torch.cuda.set_device(local_rank)
     dev = f"cuda:{local_rank}"
-    T, nc = B2_T, B2_COPIES
+    T, nc = B2_T, args.batched_copies
     t_setup = time.time()
     layers = build_model(dev, nc, B2_CFG, zipf=True)
     setup_s = time.time() - t_setup
@@ -697,7 +697,8 @@ def run_batched(args, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dev_s / args.steps * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp16x2-split activations x exact codes -> f32", "data": "synthetic",
-        "config": {"workload": B2_WORKLOAD, "tokens_per_call": T, "layer_copies": nc, "global_batch": T,
+        "config": {"workload": B2_WORKLOAD if nc == B2_COPIES else B2_WORKLOAD.replace("8 independent", f"{nc} independent"),
+                   "tokens_per_call": T, "layer_copies": nc, "global_batch": T,
                    "seq_len": 1, "parallelism": "replicas" if world > 1 else "single",
                    "l2": "no flush: 8 layer copies of 1.86 GB used in turn (>> 126 MB L2)",
                    "distinct_experts_per_call": distinct,
@@ -1014,6 +1015,8 @@ def main():
                          "memory through an HBM cache")
     ap.add_argument("--stream-layers", type=int, default=4, help="decode-stream: layers (host memory 1.8 GB each)")
     ap.add_argument("--cache-slots", type=int, default=256, help="decode-stream: HBM cache slots (7.1 MB each)")
+    ap.add_argument("--batched-copies", type=int, default=B2_COPIES,
+                    help="batched: layer copies used in turn (8 keeps every call cold in L2; fewer only for profiling)")
     ap.add_argument("--model", choices=["q2", "q2-q4"], default="q2",
                     help="decode model: q2 = every layer IQ2_XXS/Q2_K (headline); q2-q4 = last 6 layers Q4_K")
     ap.add_argument("--decode-path", choices=["fused", "layer", "split"], default="fused",

@@ -57,7 +57,10 @@ extern "C" const char *ds4g_status_str(ds4g_status s) {
 extern "C" size_t ds4g_forward_workspace(int T) {
     if (T < 1) return 0;
     if (T >= kPrefillMinT) return prefill_workspace(T);
-    return decode_workspace(T < kDecodeMaxT ? T : kDecodeMaxT);
+    const size_t dec = decode_workspace(T < kDecodeMaxT ? T : kDecodeMaxT);
+    if (T <= kDecodeMaxT) return dec;
+    const size_t bat = batch_workspace(T);   // IQ2_XXS/Q2_K layers; Q4_K layers take the decode path
+    return bat > dec ? bat : dec;
 }
 
 static bool types_ok(const ds4g_layer *L) {
@@ -92,6 +95,8 @@ static ds4g_status run_forward(const float *hidden, int T, const ds4g_layer *L, 
         if ((long long)T * (kK + 1) * kH * 4 > (1ll << 40)) return DS4G_EUNSUPPORTED;
         return prefill_forward(hidden, T, L, ids, w, out, workspace, st, phases);
     }
+    if (T > kDecodeMaxT && phases == 3 && L->gate_up_type == DS4G_IQ2_XXS)
+        return batch_forward(hidden, T, L, ids, w, out, workspace, st);   // experts grouped: read once per chunk
     for (int t0 = 0; t0 < T; t0 += kDecodeMaxT) {
         const int n = T - t0 < kDecodeMaxT ? T - t0 : kDecodeMaxT;
         const ds4g_status rc = decode_forward(hidden + (size_t)t0 * kH, n, L, ids + (size_t)t0 * kK,

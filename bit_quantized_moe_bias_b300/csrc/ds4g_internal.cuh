@@ -93,6 +93,13 @@ ds4g_status decode_forward(const float *hidden, int T, const ds4g_layer *L, cons
                            float *out, void *workspace, cudaStream_t st, int phases,
                            uint32_t *status_word = nullptr);
 
+// Batched decode path (batch.cu, 4 <= T < 64, IQ2_XXS gate/up and Q2_K
+// down): the batch's slots grouped by expert, each selected expert read once
+// per (up to 32-token) chunk.
+size_t batch_workspace(int T);
+ds4g_status batch_forward(const float *hidden, int T, const ds4g_layer *L, const int32_t *ids, const float *w,
+                          float *out, void *workspace, cudaStream_t st);
+
 // TMA tensor maps over a row-major [rows][cols] bf16 matrix, 128-byte
 // swizzle (tmap.cu).  tmap_bf16_2d: box of 64 columns x box_rows rows.
 // tmap_bf16_rowtile: box of tile_rows rows x (64 * tile_chunks) columns,

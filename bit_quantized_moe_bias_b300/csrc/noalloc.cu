@@ -68,10 +68,10 @@ extern "C" ds4g_status ds4g_moe_forward_noalloc(const float *hidden, int T, cons
     cudaStream_t st = (cudaStream_t)s;
     // The array keeps whatever the previous call left.  Only the status word
     // and the kernels' tile counters must start at zero; all of them lie
-    // below kWsScratch (12 KB), and every other byte the kernels use is
+    // below kWsScratch (13 KB), and every other byte the kernels use is
     // written before it is read.  The kernels put their counters back to
     // zero, so the clear matters only after a call that a fault cut short;
-    // it is 12 KB, not the 4.9 MB in use.  cudaMemsetAsync allocates nothing.
+    // it is 13 KB, not the 4.9 MB in use.  cudaMemsetAsync allocates nothing.
     if (cudaMemsetAsync(ws, 0, kWsScratch, st) != cudaSuccess) return DS4G_ECUDA;
     for (int t0 = 0; t0 < T; t0 += kDecodeMaxT) {
         const int n = T - t0 < kDecodeMaxT ? T - t0 : kDecodeMaxT;

@@ -5,8 +5,8 @@
 // renormalised to sum 1.
 //
 // One launch for any T:
-//   small T (<= 8): CTA (expert group of 8, k-quarter); each warp streams one
-//     router row quarter once and dots it with all T tokens;
+//   small T (<= 64): CTA (expert group of 8, k-quarter); each warp streams one
+//     router row quarter once and dots it with all T tokens (4 at a time);
 //   large T: 32-token x 64-expert fp32 SIMT tiles over the full K.
 // Partial logits go to the workspace; the last CTA to finish a token range
 // (atomic ticket, no waiting) sums them in a fixed order and runs the top-k,
@@ -17,7 +17,7 @@
 
 namespace ds4g {
 
-constexpr int kRouteSmallT = 8;
+constexpr int kRouteSmallT = 64;
 constexpr int kRouteKS = 4;   // k-splits on the small-T path
 constexpr int kTileT = 32, kTileE = 64, kTileK = 32;
 
@@ -101,20 +101,29 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteArgs a) {
 #pragma unroll
     for (int i = 0; i < 8; ++i)
         r[i] = __ldcs(reinterpret_cast<const float4 *>(a.R + (size_t)e * kH + k0 + 4 * lane + 128 * i));
-    for (int t = 0; t < a.T; ++t) {
-        const float *xr = a.x + (size_t)t * kH + k0;
-        float acc = 0.f;
+    for (int t0 = 0; t0 < a.T; t0 += 4) {
+        // four tokens at a time: their activation loads are in flight together
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float4 xv = *reinterpret_cast<const float4 *>(xr + 4 * lane + 128 * i);
-            acc = fmaf(r[i].x, xv.x, acc);
-            acc = fmaf(r[i].y, xv.y, acc);
-            acc = fmaf(r[i].z, xv.z, acc);
-            acc = fmaf(r[i].w, xv.w, acc);
+        for (int u = 0; u < 4; ++u) {
+            if (t0 + u >= a.T) break;
+            const float *xr = a.x + (size_t)(t0 + u) * kH + k0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 xv = __ldg(reinterpret_cast<const float4 *>(xr + 4 * lane + 128 * i));
+                acc[u] = fmaf(r[i].x, xv.x, acc[u]);
+                acc[u] = fmaf(r[i].y, xv.y, acc[u]);
+                acc[u] = fmaf(r[i].z, xv.z, acc[u]);
+                acc[u] = fmaf(r[i].w, xv.w, acc[u]);
+            }
         }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (lane == 0) a.part[((size_t)ks * a.T + t) * kE + e] = acc;
+        for (int u = 0; u < 4; ++u) {
+            float v = acc[u];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+            if (lane == 0 && t0 + u < a.T) a.part[((size_t)ks * a.T + t0 + u) * kE + e] = v;
+        }
     }
     __threadfence();  // every writer publishes its partials before the ticket
     __shared__ uint32_t last;
@@ -126,15 +135,18 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteArgs a) {
     __syncthreads();
     if (!last) return;
     __threadfence();
-    __shared__ float lg[kRouteSmallT][kE];
-    for (int i = threadIdx.x; i < a.T * kE; i += blockDim.x) {
-        const int t = i / kE, ee = i % kE;
-        float v = 0.f;
-        for (int s = 0; s < kRouteKS; ++s) v += __ldcg(a.part + ((size_t)s * a.T + t) * kE + ee);
-        lg[t][ee] = v;
+    // one warp per token: its logits (sum of the k-quarters in order), top-6
+    __shared__ float lg[8][kE];
+    for (int t = warp; t < a.T; t += 8) {
+        for (int ee = lane; ee < kE; ee += 32) {
+            float v = 0.f;
+            for (int s = 0; s < kRouteKS; ++s) v += __ldcg(a.part + ((size_t)s * a.T + t) * kE + ee);
+            lg[warp][ee] = v;
+        }
+        __syncwarp();
+        topk_warp(a, t, lg[warp]);
+        __syncwarp();
     }
-    __syncthreads();
-    if (warp < a.T) topk_warp(a, warp, lg[warp]);
     if (threadIdx.x == 0) *a.cnt = 0u;
 }
 

@@ -204,18 +204,24 @@ typedef struct {
  *   out[t] = s + sum_{k=0..5} w[t][k] * y_k     (fixed k order, no atomics)
  * hidden [T][4096] f32 dev, ids [T][6] int32 dev, w [T][6] f32 dev,
  * out [T][4096] f32 dev.  A repeated id within a token is legal (both terms
- * are summed).  Two paths, chosen by T:
- *  - T < 64 (decode): per-slot dequant-in-register GEMV, processed in chunks
- *    of 3 tokens.  Codes enter the tensor cores exactly; activations as an
- *    fp16 hi+lo pair (|x| < 65504 required, else DS4G_EDEVICE); h as an
- *    fp16 hi+lo pair scaled by a power of two per 16 entries (any finite h;
- *    inf/NaN is DS4G_EDEVICE); fp32 accumulation.  Expected error ~1e-5
- *    relative.
+ * are summed).  Three paths, chosen by T:
+ *  - T <= 3, and Q4_K layers up to T = 63 (decode): per-slot
+ *    dequant-in-register GEMV, processed in chunks of 3 tokens.  Codes enter
+ *    the tensor cores exactly; activations as an fp16 hi+lo pair
+ *    (|x| < 65504 required, else DS4G_EDEVICE); h as an fp16 hi+lo pair
+ *    scaled by a power of two per 16 entries (any finite h; inf/NaN is
+ *    DS4G_EDEVICE); fp32 accumulation.  Expected error ~1e-5 relative.
+ *  - 4 <= T < 64 with IQ2_XXS/Q2_K layers (batched decode): the slots
+ *    grouped by expert, each selected expert's weights read once per chunk
+ *    of up to 32 tokens and applied to all of its tokens.  Same arithmetic as
+ *    the per-slot path except that h enters the down projection as fp16 of
+ *    2^-e h without a lo part, and the shared expert's bf16 weights as fp16.
+ *    Expected error ~1e-4 relative.
  *  - T >= 64 (chunked prefill, large batches): tokens bucketed by expert,
- *    grouped tcgen05 GEMM.  Weights are the fp32 block formula rounded to
- *    nearest even: fp16 with fp16 activations for the routed gate/up
- *    (|x| < 65504 required, else DS4G_EDEVICE), bf16 with bf16 h for the
- *    down projection, bf16 throughout for the shared expert; fp32
+ *    grouped tcgen05 GEMM.  Routed weights are the fp32 block formula
+ *    rounded to nearest even in fp16, against fp16 activations (gate/up;
+ *    |x| < 65504 required, else DS4G_EDEVICE) and fp16 h scaled by a power
+ *    of two per row (down); bf16 throughout for the shared expert; fp32
  *    accumulation.  Expected error ~1e-3 relative L2 per token.
  * workspace dev >= ds4g_forward_workspace(T) bytes (about 200 KB per token
  * on the prefill path), zeroed once before first use; one call at a time.
@@ -335,8 +341,9 @@ void ds4g_test_force_timeout(int on);
  * the per-slot decode kernels of ds4g_moe_forward on chunks of up to three
  * tokens, so it returns, bit for bit, what ds4g_moe_forward returns when
  * called on the same chunks one at a time.  For a whole batch of T >= 4
- * tokens ds4g_moe_forward takes other kernels (the batched path from T = 4,
- * the tensor-core prefill path from T = 64): their results agree with this
+ * tokens ds4g_moe_forward takes other kernels (the batched path from T = 4
+ * for IQ2_XXS/Q2_K layers, the tensor-core prefill path from T = 64): their
+ * results agree with this
  * call within the block's tolerance, not bit for bit, and they read each
  * selected expert's weights once per batch, where this call reads them once
  * per chunk.  Scratch is a library-owned device array of 5 MB (file scope,
@@ -346,7 +353,7 @@ void ds4g_test_force_timeout(int on);
  *    DS4G_ENOSPACE (T too large), returned before any CUDA call.
  *  - Allocates nothing: no cudaMalloc/cudaFree and no allocating library
  *    call.  Every call clears the array's status word and tile counters
- *    (12 KB) with cudaMemsetAsync on s, then runs the decode kernels on s.
+ *    (13 KB) with cudaMemsetAsync on s, then runs the decode kernels on s.
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current and keeps it for the
  *    process; make that first call before any stream capture.  After a

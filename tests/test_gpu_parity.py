@@ -163,8 +163,11 @@ def _forward_gpu(x, ids, w, L, phased=False):
     return out.cpu().numpy(), st
 
 
-@pytest.mark.parametrize("T", [1, 2, 3, 5])
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 32, 33, 63])
 def test_forward_decode_q2(T):
+    """T <= 3: the per-slot decode kernels; 4 <= T < 64: the batched path
+    (slots grouped by expert, chunks of up to 32 tokens: 33 and 63 end in a
+    ragged chunk)."""
     x = synth.hidden(0, 0, T)
     ids, w, _, _ = oracle.route(x, synth.router(0, 0), synth.bias_normal(0, 0))
     L, hx, shared, grid = device_layer(0, 0, 0, ids.reshape(-1))
@@ -194,6 +197,31 @@ def test_forward_duplicate_ids_and_shared_experts():
     got, st = _forward_gpu(x, ids, w, L)
     assert st == 0
     assert_close_fwd(got, oracle_forward(x, ids, w, hx, shared, grid))
+
+
+def test_forward_batched_duplicates_flags_and_determinism():
+    """The batched path (T = 8): a repeated id within a token is summed twice,
+    tokens share experts, and the result is bit for bit repeatable; an expert
+    whose matrices are missing, or an id out of range, is flagged and the
+    other tokens are still correct."""
+    T = 8
+    x = synth.hidden(2, 0, T)
+    ids = np.array([[5, 5, 9, 9, 9, 12], [12, 5, 77, 1, 2, 3], [5, 5, 5, 5, 5, 5], [1, 2, 3, 4, 5, 6],
+                    [200, 5, 9, 77, 12, 1], [6, 6, 6, 5, 5, 5], [9, 12, 77, 200, 3, 2], [1, 1, 2, 2, 3, 3]],
+                   np.int32)
+    w = np.array([[0.3, 0.2, 0.1, 0.1, 0.1, 0.2]] * T, np.float32)
+    L, hx, shared, grid = device_layer(2, 0, 0, ids.reshape(-1))
+    a, st = _forward_gpu(x, ids, w, L)
+    assert st == 0
+    b, st = _forward_gpu(x, ids, w, L)
+    assert st == 0 and np.array_equal(a, b)
+    assert_close_fwd(a, oracle_forward(x, ids, w, hx, shared, grid))
+    bad = ids.copy()
+    bad[3, 4] = 999                                            # token 3: an id out of range
+    got, st = _forward_gpu(x, bad, w, L)
+    assert st == 7
+    ok = [t for t in range(T) if t != 3]
+    assert_close_fwd(got[ok], oracle_forward(x[ok], ids[ok], w[ok], hx, shared, grid))
 
 
 def test_forward_flags_missing_expert():
