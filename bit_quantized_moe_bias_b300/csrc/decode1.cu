@@ -74,13 +74,15 @@ static_assert(kD1Slot >= 16 * kTB_IQ2 && kD1Slot >= 4 * kH && (kD1Slot % 128) ==
 constexpr int kSlotsPerGrp = 2;                  // one piece in flight while one is computed
 constexpr int kD1Slots = kNGrp * kSlotsPerGrp;   // 8
 constexpr int kRep = 16;                         // table replicas: one per lane of a half-warp
-constexpr int kMix = 1;                          // routed gate/up jobs between two shared gate/up jobs
+constexpr int kMix = 1;                          // routed gate/up pieces between two shared gate/up jobs
 
 // Jobs per kind and their pieces:
 //   router rows                         1 piece (16 KB fp32)
 //   shared gate/up (tile, quarter)      4 pieces (gate, gate, up, up: 16 rows x 512 columns, 16 KB each)
 //   shared down (tile, quarter)         1 piece (16 rows x 512 columns, 16 KB)
-//   routed gate/up (slot, 16-row tile)  2 pieces (gate, up: 16 tile-blocks each)
+//   routed gate/up (slot, 16-row tile)  4 pieces (gate, up x column half: 8 tile-blocks each);
+//                                       the CTA's groups take its pieces one at a time, and
+//                                       the last of a job's four adds them (shared memory)
 //   routed down (slot, 16-row tile)     1 piece (8 Q2_K tile-blocks + that slot's h)
 constexpr int kNPhase = 5;
 constexpr int kJR = kE;
@@ -89,6 +91,12 @@ constexpr int kJSD = (kH / 16) * 4;   // shared down: 256 tiles x 4 column quart
 constexpr int kJRG = kK * (kF / 16);
 constexpr int kJRD = kK * (kH / 16);
 constexpr int kTileParts = 4 + kK;      // jobs contributing to one 16-row output tile
+constexpr int kRgLocal = 8;             // routed gate/up jobs one CTA may hold (grid >= 96 CTAs)
+constexpr int kRgSplit = 2;                 // column parts of a routed gate/up piece (1 or 2)
+constexpr int kRgP = 2 * kRgSplit;          // pieces per routed gate/up job: gate, up x column part
+constexpr int kRgTB = 16 / kRgSplit;        // tile-blocks per piece
+static_assert(kRgSplit == 1 || kRgSplit == 2, "routed gate/up split");
+static_assert((kJRG + kRgLocal - 1) / kRgLocal <= 96, "grid bound of the local join");
 
 enum : int { PK_END = 0, PK_ROUTER, PK_SGU, PK_RGU, PK_SDN, PK_RDN };
 
@@ -154,7 +162,9 @@ constexpr uint32_t kOffCred = kOffEptr + 160;
 constexpr uint32_t kOffBar = kOffCred + 64;
 constexpr uint32_t kOffFlags = kOffBar + (2 * kD1Slots + 2) * 8;
 constexpr uint32_t kOffJc = kOffFlags + 32;      // per kind: the CTA's next unclaimed job
-constexpr size_t kD1SmemBytes = kOffJc + 32;
+constexpr uint32_t kOffRgs = kOffJc + 32;       // [kRgLocal][4 pieces][16 rows] routed gate/up partials
+constexpr uint32_t kOffRgc = kOffRgs + kRgLocal * 4 * 16 * 4;   // [kRgLocal] pieces arrived
+constexpr size_t kD1SmemBytes = kOffRgc + kRgLocal * 4;
 static_assert(kD1SmemBytes <= 232448, "shared memory");
 static_assert((kOffXb % 128) == 0 && (kOffXq % 16) == 0 && (kOffEptr % 8) == 0 && (kOffBar % 8) == 0, "alignment");
 
@@ -175,6 +185,8 @@ struct D1Smem {
     uint64_t *full, *empty, *xbar, *hsbar;
     int *flags;            // [0] abort, [1] ids known, [2] shared h requested, [3] routed slots ready (mask)
     int *jc;               // [5] per job kind: the CTA's next unclaimed local job index
+    float *rgs;            // [kRgLocal][4][16] routed gate/up piece sums of the CTA's jobs
+    int *rgc;              // [kRgLocal] pieces of each such job summed so far
 };
 
 extern __shared__ __align__(1024) uint8_t d1_raw[];
@@ -200,6 +212,8 @@ __device__ __forceinline__ D1Smem d1_smem() {
     s.hsbar = s.xbar + 1;
     s.flags = reinterpret_cast<int *>(d1_raw + kOffFlags);
     s.jc = reinterpret_cast<int *>(d1_raw + kOffJc);
+    s.rgs = reinterpret_cast<float *>(d1_raw + kOffRgs);
+    s.rgc = reinterpret_cast<int *>(d1_raw + kOffRgc);
     return s;
 }
 
@@ -391,12 +405,17 @@ __device__ __forceinline__ void iq2_tileblock2(const D1Smem &sm, const uint8_t *
     float d4g[2], d4h[2];
     const bool act = (g >> 1) == t;
     const __half *xb = sm.xq + (g & 1) * kH + 256 * b0 + 32 * t;
+    uint32_t ddr[2];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
         const uint8_t *tbu = tb + u * kTB_IQ2;
         qa[u] = *reinterpret_cast<const uint4 *>(tbu + 16 * lane);
         qb[u] = *reinterpret_cast<const uint4 *>(tbu + 512 + 16 * lane);
-        const uint32_t dd = *reinterpret_cast<const uint32_t *>(tbu + 1024 + 4 * g);
+        ddr[u] = *reinterpret_cast<const uint32_t *>(tbu + 1024 + 4 * g);
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const uint32_t dd = ddr[u];
         d4g[u] = __half2float(__ushort_as_half((unsigned short)(dd & 0xffffu))) * 4194304.0f;
         d4h[u] = __half2float(__ushort_as_half((unsigned short)(dd >> 16))) * 4194304.0f;
     }
@@ -507,7 +526,9 @@ __device__ __forceinline__ int phase_jobs(int p) {
     return p == 0 ? kJR : p == 1 ? kJSG : p == 2 ? kJSD : p == 3 ? kJRG : kJRD;
 }
 __device__ __forceinline__ int phase_off(int p, int c, int G) { return (p & 1) ? (G - 1 - c) : c; }
-__device__ __forceinline__ int phase_pieces(int p) { return p == 1 ? 4 : p == 3 ? 2 : 1; }
+__device__ __forceinline__ int phase_pieces(int p) { return p == 1 ? 4 : 1; }
+// Routed gate/up claims are pieces: claim i is piece i & 3 of the CTA's job i >> 2.
+__device__ __forceinline__ int claim_units(int p) { return p == 3 ? kRgP : 1; }
 
 // If this warp's counted job was the last of its 16-row output tile (the
 // counter returned kTileParts - 1), sum the tile's partials in a fixed order:
@@ -681,6 +702,7 @@ __global__ void __launch_bounds__(kD1Threads, 1)
         tc::prefetch_tmap(tm_sd);
         for (int i = 0; i < 8; ++i) sm.flags[i] = 0;
         for (int i = 0; i < 8; ++i) sm.jc[i] = 0;
+        for (int i = 0; i < kRgLocal; ++i) sm.rgc[i] = 0;
         tc::fence_mbar_init();
     }
     __syncthreads();
@@ -697,7 +719,7 @@ __global__ void __launch_bounds__(kD1Threads, 1)
 #pragma unroll
             for (int p = 0; p < kNPhase; ++p) {
                 const int off = phase_off(p, c, G), n = phase_jobs(p);
-                cnt[p] = off < n ? (n - off + G - 1) / G : 0;
+                cnt[p] = (off < n ? (n - off + G - 1) / G : 0) * claim_units(p);
             }
             volatile int *jc = sm.jc;
             uint32_t itq = 0, seen = 0;
@@ -747,7 +769,10 @@ __global__ void __launch_bounds__(kD1Threads, 1)
                             if (want >= 0) {
                                 const int i = atomicAdd(&sm.jc[want], 1);
                                 if (i < cnt[want]) {
-                                    j = i * G + phase_off(want, c, G);
+                                    // routed gate/up: piece i & 3 of local job i >> 2
+                                    const int u = claim_units(want);
+                                    j = (i / u) * G + phase_off(want, c, G);
+                                    pc = want == 3 ? (i % kRgP) + 4 * (i / kRgP) : 0;
                                     p = want;
                                     if (p == 4 && !((ready >> (j / (kH / 16))) & 1u)) {
                                         held = j;   // another lane took the ready one first
@@ -809,13 +834,16 @@ __global__ void __launch_bounds__(kD1Threads, 1)
                     tchunk = 8 * (j & 3);
                     bytes = 16 * 512 * 2;
                 } else if (p == 3) {
+                    // piece pq = pc & 3 of the CTA's local job pc >> 2: gate
+                    // (pq < kRgSplit) or up rows of the tile, column part
+                    // pq % kRgSplit (kRgTB tile-blocks)
                     d.kind = PK_RGU;
-                    const int k = j / (kF / 16), tile = j % (kF / 16);
-                    const uint8_t *mat = sm.eptr[(pc ? kK : 0) + k];
+                    const int k = j / (kF / 16), tile = j % (kF / 16), pq = pc & 3;
+                    const uint8_t *mat = sm.eptr[(pq >= kRgSplit ? kK : 0) + k];
                     d.e = k;
                     if (mat) {
-                        src = mat + (size_t)tile * 16 * kTB_IQ2;
-                        bytes = 16 * kTB_IQ2;
+                        src = mat + ((size_t)tile * 16 + kRgTB * (pq % kRgSplit)) * kTB_IQ2;
+                        bytes = kRgTB * kTB_IQ2;
                     } else {
                         d.e = -1;
                         flag_status(a.status, DS4G_EDEVICE, (uint32_t)sm.ids_s[k]);
@@ -935,6 +963,7 @@ __global__ void __launch_bounds__(kD1Threads, 1)
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         int pend_tile = -1;                               // tile counted by this warp, not yet examined
         uint32_t pend_old = 0u;
+        uint32_t njob = 0;                                // jobs this group has finished
         bool hs_ok = false;
         int gpar = 0;
         for (uint32_t it = 0;; ++it) {
@@ -979,28 +1008,25 @@ __global__ void __launch_bounds__(kD1Threads, 1)
                     last = d.piece == 3;
                 }
             } else if (d.kind == PK_RGU) {
-                if (d.piece == 0) acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+                // warp wq: tile-blocks (kRgTB / 4) wq .. + kRgTB / 4 of the piece
+                // (block columns kRgTB (pq % kRgSplit) + that, of the 16-row tile)
+                float t0 = 0.f, t1 = 0.f;
                 if (d.e >= 0) {
-                    float t0, t1, t2, t3;
-                    iq2_tileblock2(sm, slot + (size_t)(4 * wq) * kTB_IQ2, 4 * wq, lane, t0, t1);
-                    iq2_tileblock2(sm, slot + (size_t)(4 * wq + 2) * kTB_IQ2, 4 * wq + 2, lane, t2, t3);
-                    if (d.piece) {
-                        acc[2] += t0 + t2;
-                        acc[3] += t1 + t3;
-                    } else {
-                        acc[0] += t0 + t2;
-                        acc[1] += t1 + t3;
+                    const int b0 = kRgTB * ((d.piece & 3) % kRgSplit) + (kRgTB / 4) * wq;
+#pragma unroll
+                    for (int cb = 0; cb < kRgTB / 8; ++cb) {
+                        float u0, u1;
+                        iq2_tileblock2(sm, slot + (size_t)((kRgTB / 4) * wq + 2 * cb) * kTB_IQ2, b0 + 2 * cb, lane,
+                                       u0, u1);
+                        t0 += u0;
+                        t1 += u1;
                     }
                 }
-                if (d.piece == 1) {
-                    if ((lane & 3) == 0) {
-                        red[wq * 16 + (lane >> 2)] = acc[0];
-                        red[wq * 16 + (lane >> 2) + 8] = acc[1];
-                        red[64 + wq * 16 + (lane >> 2)] = acc[2];
-                        red[64 + wq * 16 + (lane >> 2) + 8] = acc[3];
-                    }
-                    last = true;
+                if ((lane & 3) == 0) {
+                    red[wq * 16 + (lane >> 2)] = t0;
+                    red[wq * 16 + (lane >> 2) + 8] = t1;
                 }
+                last = true;
             } else if (d.kind == PK_SDN) {
                 // shared down: 16 rows of the output tile, columns 512 kq .. +512 of h
                 float c[4] = {0.f, 0.f, 0.f, 0.f};
@@ -1034,9 +1060,13 @@ __global__ void __launch_bounds__(kD1Threads, 1)
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&sm.empty[s]);
             if (!last) continue;
-            // ---- job end: the group's four warps reduce in a fixed order
+            // ---- job end: the group's four warps reduce in a fixed order.
+            // The group's warps take turns to publish (job n: warp n mod 4),
+            // so the global round trips of a publication (fence, counters)
+            // stall one warp while the other three go on with the next job.
             asm volatile("bar.sync %0, %1;" ::"r"(2 + q), "n"(kGW * 32));
-            if (wq == 0) {
+            const bool pub = (int)(njob++ % kGW) == wq;
+            if (pub) {
                 int tile = -1;
                 if (d.kind == PK_ROUTER) {
                     if (lane == 0) {
@@ -1074,40 +1104,57 @@ __global__ void __launch_bounds__(kD1Threads, 1)
                         }
                     }
                 } else if (d.kind == PK_RGU) {
-                    // h of 16 rows of slot k: fp16 hi/lo of 2^-e h (one power of two
-                    // per 16 entries, so any finite h fits), the 16-column sum of h
-                    // the Q2_K down needs, and 2^e, where the routed-down pieces
-                    // copy them from
-                    const int k = d.job / (kF / 16), tl = d.job % (kF / 16);
-                    float hv = 0.f;
-                    if (lane < 16) {
-                        const float gs = (red[lane] + red[16 + lane]) + (red[32 + lane] + red[48 + lane]);
-                        const float us = (red[64 + lane] + red[80 + lane]) + (red[96 + lane] + red[112 + lane]);
-                        hv = silu_f(gs) * us;
-                        if (!(fabsf(hv) <= 3.4028235e38f)) flag_status(a.status, DS4G_EDEVICE, 0xF16u);
-                    }
-                    float sum = hv, m = fabsf(hv);
-#pragma unroll
-                    for (int o = 1; o < 16; o <<= 1) {
-                        sum += __shfl_xor_sync(0xffffffffu, sum, o);
-                        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-                    }
-                    const int e = h_group_exp(m);
-                    if (lane < 16) {
-                        __half hi, lo;
-                        split_f16(hv * pow2f(-e), hi, lo);
-                        __half *hq = reinterpret_cast<__half *>(a.hr + (size_t)k * kHSlot);
-                        hq[16 * tl + lane] = hi;
-                        hq[kF + 16 * tl + lane] = lo;
-                    }
-                    if (lane == 0) {
-                        const int b = tl >> 4, j16 = tl & 15;
-                        float *xs = reinterpret_cast<float *>(a.hr + (size_t)k * kHSlot + 4 * kF);
-                        xs[(b * 4 + (j16 & 3)) * 4 + (j16 >> 2)] = sum;
-                        xs[128 + (b * 4 + (j16 & 3)) * 4 + (j16 >> 2)] = pow2f(e);
-                    }
+                    // the piece's sums of 16 rows go to the CTA's join area; the
+                    // last of the job's pieces (gate, up x column part) forms
+                    // h of the 16 rows of slot k: fp16 hi/lo of 2^-e h (one power
+                    // of two per 16 entries, so any finite h fits), the 16-column
+                    // sum of h the Q2_K down needs, and 2^e, where the routed-down
+                    // pieces copy them from
+                    const int jl = (d.piece >> 2) % kRgLocal, pq = d.piece & 3;
+                    float *st = sm.rgs + jl * 64;
+                    if (lane < 16) st[16 * pq + lane] = (red[lane] + red[16 + lane]) + (red[32 + lane] + red[48 + lane]);
+                    __threadfence_block();
                     __syncwarp();
-                    if (lane == 0) red_add_release(&a.sync->rgu_done[k], 1u);
+                    int old = 0;
+                    if (lane == 0) old = atomicAdd(&sm.rgc[jl], 1);
+                    old = __shfl_sync(0xffffffffu, old, 0);
+                    if (old == kRgP - 1) {
+                        __threadfence_block();   // the other pieces' sums, stored before their counts
+                        const int k = d.job / (kF / 16), tl = d.job % (kF / 16);
+                        float hv = 0.f;
+                        if (lane < 16) {
+                            float gs = st[lane], us = st[16 * kRgSplit + lane];
+#pragma unroll
+                            for (int h = 1; h < kRgSplit; ++h) {
+                                gs += st[16 * h + lane];
+                                us += st[16 * (kRgSplit + h) + lane];
+                            }
+                            hv = silu_f(gs) * us;
+                            if (!(fabsf(hv) <= 3.4028235e38f)) flag_status(a.status, DS4G_EDEVICE, 0xF16u);
+                        }
+                        float sum = hv, m = fabsf(hv);
+#pragma unroll
+                        for (int o = 1; o < 16; o <<= 1) {
+                            sum += __shfl_xor_sync(0xffffffffu, sum, o);
+                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                        }
+                        const int e = h_group_exp(m);
+                        if (lane < 16) {
+                            __half hi, lo;
+                            split_f16(hv * pow2f(-e), hi, lo);
+                            __half *hq = reinterpret_cast<__half *>(a.hr + (size_t)k * kHSlot);
+                            hq[16 * tl + lane] = hi;
+                            hq[kF + 16 * tl + lane] = lo;
+                        }
+                        if (lane == 0) {
+                            const int b = tl >> 4, j16 = tl & 15;
+                            float *xs = reinterpret_cast<float *>(a.hr + (size_t)k * kHSlot + 4 * kF);
+                            xs[(b * 4 + (j16 & 3)) * 4 + (j16 >> 2)] = sum;
+                            xs[128 + (b * 4 + (j16 & 3)) * 4 + (j16 >> 2)] = pow2f(e);
+                        }
+                        __syncwarp();
+                        if (lane == 0) red_add_release(&a.sync->rgu_done[k], 1u);
+                    }
                 } else if (d.kind == PK_SDN) {
                     const int ot = d.job >> 2, kq = d.job & 3;
                     if (lane < 16)
@@ -1135,7 +1182,7 @@ __global__ void __launch_bounds__(kD1Threads, 1)
             }
             gpar ^= 1;
         }
-        if (wq == 0) finish_tile(a, pend_tile, pend_old, lane);
+        finish_tile(a, pend_tile, pend_old, lane);
     }
 
     // ================================================== exit protocol
@@ -1280,6 +1327,8 @@ static ds4g_status d1_setup() {
         if (cudaGetDevice(&dev) != cudaSuccess) return DS4G_ECUDA;
         if (cudaDeviceGetAttribute(&g_d1_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DS4G_ECUDA;
     }
+    // one CTA per SM; a CTA holds at most kRgLocal routed gate/up jobs
+    if ((kJRG + g_d1_sms - 1) / g_d1_sms > kRgLocal) return DS4G_EUNSUPPORTED;
     if (!g_d1_attr) {
         if (cudaFuncSetAttribute(decode_t1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kD1SmemBytes) !=
             cudaSuccess)
