@@ -51,6 +51,8 @@ WORKLOAD = ("config1 full-depth decode: 43 MoE layers x 256 experts (IQ2_XXS gat
 WORKLOAD_Q2Q4 = ("q2-q4 full-depth decode: 43 MoE layers x 256 experts, layers 0-36 IQ2_XXS gate/up + Q2_K "
                  "down, layers 37-42 Q4_K gate/up/down, bf16 shared, fp32 router, 1 token at a time, "
                  "64 tokens per step")
+WORKLOAD_Q4 = ("q4 full-depth decode: 43 MoE layers x 256 experts, Q4_K gate/up/down, bf16 shared, fp32 "
+               "router, 1 token at a time, 64 tokens per step")
 
 
 def peaks():
@@ -189,9 +191,9 @@ def run_ours(args, rank, world, local_rank):
     dev = f"cuda:{local_rank}"
     ntok = args.tokens
     nl = args.layers
-    q4 = min(Q4_LAYERS, nl) if args.model == "q2-q4" else 0
+    q4 = {"q2-q4": min(Q4_LAYERS, nl), "q4": nl}.get(args.model, 0)
     if q4 and args.decode_path != "fused":
-        raise SystemExit("--model q2-q4 runs through the decode stack (--decode-path fused)")
+        raise SystemExit("--model q2-q4 / q4 run through the decode stack (--decode-path fused)")
     t_setup = time.time()
     layers = build_model(dev, nl, q4_layers=q4)
     setup_s = time.time() - t_setup
@@ -209,8 +211,8 @@ def run_ours(args, rank, world, local_rank):
     lws = B.workspace(B.ds4g_decode_stack_workspace() if q4 else B.ds4g_layer_decode_workspace(), dev)
     fused = args.decode_path in ("fused", "layer")
     stacked = args.decode_path == "fused"
-    # q4 layers of the stack: rmsnorm, route, gate/up and down kernels
-    launches_per_step = ntok * ((nl - q4) * (1 if fused else 4) + 4 * q4)
+    # fused: one launch per layer (IQ2_XXS/Q2_K or Q4_K); split: four
+    launches_per_step = ntok * nl * (1 if fused else 4)
     stack = B.DecodeStack([(L.struct, R, b) for L, R, b in layers])
     ids_all = torch.empty(nl, K, dtype=torch.int32, device=dev)
     w_all = torch.empty(nl, K, dtype=torch.float32, device=dev)
@@ -319,11 +321,11 @@ def run_ours(args, rank, world, local_rank):
     token_bytes = (nl - q4) * LAYER_BYTES + q4 * LAYER_BYTES_Q4
     workload = WORKLOAD
     if q4:
-        # mixed stack: the figure is the whole step's, layer bytes averaged
-        # over the 43 layers (a q2 layer is one fused launch, a q4 layer four)
+        # Q4_K layers in the stack: one fused launch per layer of either type;
+        # the figure is the whole step's, layer bytes averaged over the layers
         kbytes = token_bytes // nl
-        kname = "whole stack (decode_t1_kernel for q2 layers; rmsnorm, route, gate/up, down for q4 layers)"
-        workload = WORKLOAD_Q2Q4
+        kname = "decode_t1_kernel (whole stack: %d IQ2_XXS/Q2_K + %d Q4_K layers)" % (nl - q4, q4)
+        workload = WORKLOAD_Q4 if q4 == nl else WORKLOAD_Q2Q4
     achieved = kbytes / (gu_us * 1e-6) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -1017,8 +1019,9 @@ def main():
     ap.add_argument("--cache-slots", type=int, default=256, help="decode-stream: HBM cache slots (7.1 MB each)")
     ap.add_argument("--batched-copies", type=int, default=B2_COPIES,
                     help="batched: layer copies used in turn (8 keeps every call cold in L2; fewer only for profiling)")
-    ap.add_argument("--model", choices=["q2", "q2-q4"], default="q2",
-                    help="decode model: q2 = every layer IQ2_XXS/Q2_K (headline); q2-q4 = last 6 layers Q4_K")
+    ap.add_argument("--model", choices=["q2", "q2-q4", "q4"], default="q2",
+                    help="decode model: q2 = every layer IQ2_XXS/Q2_K (headline); q2-q4 = last 6 layers Q4_K; "
+                         "q4 = every layer Q4_K")
     ap.add_argument("--decode-path", choices=["fused", "layer", "split"], default="fused",
                     help="fused = one stack call per token (one launch per layer, programmatic dependent "
                          "launches); layer = one call per layer; split = rmsnorm, route, gate/up, down launches")

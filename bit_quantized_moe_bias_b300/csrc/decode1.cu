@@ -1,14 +1,17 @@
 // decode1.cu — one decode token through one MoE layer in a single launch
 // (chenxutan ds4 article §2.3: router logic and expert compute fused into one
 // GPU dispatch, hard-coded graph; §3.2: router -> only the routed experts'
-// weights -> shared expert -> merge).  For T = 1 with IQ2_XXS/Q2_K experts.
+// weights -> shared expert -> merge).  For T = 1 with IQ2_XXS/Q2_K experts,
+// or Q4_K gate/up/down (the q4 layers of the q2-q4 model, §2.1).
 //
 // One persistent CTA per SM, 18 warps: a producer warp, a control warp and
 // four consumer groups of four warps.  The work is cut into jobs of five
 // kinds — router rows, shared gate/up (16-row tile, 1024-column quarter),
 // shared down (16-row tile, 512-column quarter), routed gate/up (slot, 16-row
-// tile), routed down (slot, 16-row tile) — each kind dealt round-robin over
-// the CTAs (alternating direction per kind, so per-CTA bytes balance).
+// tile; four pieces: gate or up x column half, claimed one at a time and
+// joined in shared memory), routed down (slot, 16-row tile; Q4_K: and half
+// of h) — each kind dealt round-robin over the CTAs (alternating direction
+// per kind, so per-CTA bytes balance).
 // Producer lane q feeds group q's two-slot shared-memory ring with pieces of
 // about 16 KB (a copy has a fixed cost, so pieces are kept large): contiguous
 // bulk copies for the router rows and the packed experts, one 3-D tensor copy
@@ -17,9 +20,10 @@
 // takes more, and each picks its next job by readiness: router rows first;
 // routed gate/up as soon as the expert ids are known, alternating with shared
 // gate/up; then routed down of the slots whose h is complete; then shared
-// down once the shared h is complete.  A group splits each piece over its four warps,
-// keeps partials in registers until the job's last piece and reduces them in
-// a fixed order behind a four-warp barrier.
+// down once the shared h is complete.  A group splits each piece over its
+// four warps, keeps partials in registers until the job's last piece and
+// reduces them in a fixed order behind a four-warp barrier; the group's warps
+// take turns publishing finished jobs.
 //
 // Dependencies are exactly those of the method, tracked by counters in the
 // workspace (release on store, acquire on read):
@@ -35,9 +39,10 @@
 //    fixed order and stores h of the tile's 16 rows; once all 128 tiles are
 //    stored the control warp copies h once into the CTA (over the bf16
 //    activation, which every job that reads it has finished by then);
-//  - out: the four shared-down quarters and six routed-down jobs of a 16-row
-//    output tile store partials; the last of the ten (a per-tile counter)
-//    sums them in a fixed order.
+//  - out: the four shared-down quarters and six routed-down jobs (Q4_K:
+//    twelve, two halves of h per slot) of a 16-row output tile store
+//    partials; the last of them (a per-tile counter) sums them in a fixed
+//    order.
 // Every wait is bounded (~1 s); a timeout records DS4G_ETIMEOUT.
 //
 // Chained layers (ds4g_moe_decode_stack) launch each layer after the first as
@@ -45,15 +50,12 @@
 // the previous layer's CTAs leave, build their tables and start streaming
 // router and shared-expert pieces, and touch the input and the workspace
 // only after griddepcontrol.wait (the previous layer complete and visible).
-// A stack's Q4_K layers (the last six of the q2-q4 model, chenxutan ds4
-// article §2.1) run as rmsnorm + route + the decode path of the forward; the
-// fused layer that follows one of them is launched in plain stream order.
 //
 // Arithmetic: router in fp32 FMA against the activation's fp16 hi + lo pair;
 // shared expert on mma.sync bf16 (weights as stored) against the activation,
 // or the shared h, as a bf16 hi + lo pair; routed experts on mma.sync with
-// exact codes (IQ2 grid value or Q2_K quant as an fp16 subnormal, sign from
-// the sign table) against the activation as an fp16 hi + lo pair (h: scaled
+// exact codes (IQ2 grid value, Q2_K or Q4_K quant as an fp16 subnormal, sign
+// from the sign table) against the activation as an fp16 hi + lo pair (h: scaled
 // per 16 entries); block, sub-block and h scales applied in fp32 to each 32-
 // or 16-column partial.  The IQ2_XXS grid values must lie in
 // {8, 25, 43} (the format's magnitudes): the grid table holds, per row, 8
@@ -71,6 +73,7 @@ constexpr int kRdnW = 8 * kTB_Q2K;               // routed down piece: 16 rows x
 constexpr int kHSlot = 2 * kF * 2 + 2 * 128 * 4; // routed h of one slot: fp16 hi, lo, 16-col sums, scales
 constexpr int kD1Slot = kRdnW + kHSlot;          // 19968 B: the largest piece
 static_assert(kD1Slot >= 16 * kTB_IQ2 && kD1Slot >= 4 * kH && (kD1Slot % 128) == 0, "slot size");
+static_assert(kD1Slot >= 8 * kTB_Q4K && kD1Slot >= 4 * kTB_Q4K + kHSlot / 2, "Q4_K pieces fit a slot");
 constexpr int kSlotsPerGrp = 2;                  // one piece in flight while one is computed
 constexpr int kD1Slots = kNGrp * kSlotsPerGrp;   // 8
 constexpr int kRep = 16;                         // table replicas: one per lane of a half-warp
@@ -83,20 +86,23 @@ constexpr int kMix = 1;                          // routed gate/up pieces betwee
 //   routed gate/up (slot, 16-row tile)  4 pieces (gate, up x column half: 8 tile-blocks each);
 //                                       the CTA's groups take its pieces one at a time, and
 //                                       the last of a job's four adds them (shared memory)
-//   routed down (slot, 16-row tile)     1 piece (8 Q2_K tile-blocks + that slot's h)
+//   routed down (slot, 16-row tile)     1 piece (8 Q2_K tile-blocks + that slot's h); Q4_K layers:
+//                                       (slot, 16-row tile, half of h), 1 piece (4 Q4_K
+//                                       tile-blocks + that half of the slot's h)
+// Q4_K layers (q4 set) take Q4_K tile-blocks in the routed gate/up pieces too
+// (8 tile-blocks, 18 KB); their output tiles have 4 + 12 parts.
 constexpr int kNPhase = 5;
 constexpr int kJR = kE;
 constexpr int kJSG = (kF / 16) * 4;   // shared gate/up: 128 tiles x 4 column quarters
 constexpr int kJSD = (kH / 16) * 4;   // shared down: 256 tiles x 4 column quarters
 constexpr int kJRG = kK * (kF / 16);
-constexpr int kJRD = kK * (kH / 16);
-constexpr int kTileParts = 4 + kK;      // jobs contributing to one 16-row output tile
-constexpr int kRgLocal = 8;             // routed gate/up jobs one CTA may hold (grid >= 96 CTAs)
+constexpr int kJRD = kK * (kH / 16);   // routed down jobs of an IQ2_XXS/Q2_K layer (twice that for Q4_K)
+constexpr int kRgLocal = 6;             // routed gate/up jobs one CTA may hold (grid >= 128 CTAs)
 constexpr int kRgSplit = 2;                 // column parts of a routed gate/up piece (1 or 2)
 constexpr int kRgP = 2 * kRgSplit;          // pieces per routed gate/up job: gate, up x column part
 constexpr int kRgTB = 16 / kRgSplit;        // tile-blocks per piece
 static_assert(kRgSplit == 1 || kRgSplit == 2, "routed gate/up split");
-static_assert((kJRG + kRgLocal - 1) / kRgLocal <= 96, "grid bound of the local join");
+static_assert((kJRG + kRgLocal - 1) / kRgLocal <= 128, "grid bound of the local join");
 
 enum : int { PK_END = 0, PK_ROUTER, PK_SGU, PK_RGU, PK_SDN, PK_RDN };
 
@@ -120,6 +126,7 @@ struct D1Args {
     const float *x;
     int normalize;
     int pdl;
+    int q4;                 // 1: Q4_K gate/up/down; 0: IQ2_XXS/Q2_K (host side: picks the kernel instance)
     uint32_t router_extra;  // 0; 1 only under the test hook (waits for a router row that does not exist)
     long long router_limit; // clock cycles the control warp waits for the router logits
     const float *router;   // [256][4096]
@@ -139,7 +146,7 @@ struct D1Args {
     __nv_bfloat16 *hsb;    // [2][kHLd] shared h as bf16 hi, lo
     float *sgu_part;       // [128 tiles][4 quarters][32]: gate (16 rows), up (16 rows) partial sums
     float *p_s;            // [4][4096] shared-expert output, per column quarter
-    float *p_r;            // [6][4096] weighted routed outputs
+    float *p_r;            // [12][4096] weighted routed outputs (per slot; Q4_K: per slot and half of h)
 };
 
 // ------------------------------------------------------------------ smem
@@ -164,7 +171,8 @@ constexpr uint32_t kOffFlags = kOffBar + (2 * kD1Slots + 2) * 8;
 constexpr uint32_t kOffJc = kOffFlags + 32;      // per kind: the CTA's next unclaimed job
 constexpr uint32_t kOffRgs = kOffJc + 32;       // [kRgLocal][4 pieces][16 rows] routed gate/up partials
 constexpr uint32_t kOffRgc = kOffRgs + kRgLocal * 4 * 16 * 4;   // [kRgLocal] pieces arrived
-constexpr size_t kD1SmemBytes = kOffRgc + kRgLocal * 4;
+constexpr uint32_t kOffXs32 = kOffRgc + 32;   // [128] 32-column sums of x (hi + lo), Q4_K layers
+constexpr size_t kD1SmemBytes = kOffXs32 + 128 * 4;
 static_assert(kD1SmemBytes <= 232448, "shared memory");
 static_assert((kOffXb % 128) == 0 && (kOffXq % 16) == 0 && (kOffEptr % 8) == 0 && (kOffBar % 8) == 0, "alignment");
 
@@ -187,6 +195,7 @@ struct D1Smem {
     int *jc;               // [5] per job kind: the CTA's next unclaimed local job index
     float *rgs;            // [kRgLocal][4][16] routed gate/up piece sums of the CTA's jobs
     int *rgc;              // [kRgLocal] pieces of each such job summed so far
+    float *xs32;           // [128] sums of x over each 32-column sub-block (Q4_K mins)
 };
 
 extern __shared__ __align__(1024) uint8_t d1_raw[];
@@ -214,6 +223,7 @@ __device__ __forceinline__ D1Smem d1_smem() {
     s.jc = reinterpret_cast<int *>(d1_raw + kOffJc);
     s.rgs = reinterpret_cast<float *>(d1_raw + kOffRgs);
     s.rgc = reinterpret_cast<int *>(d1_raw + kOffRgc);
+    s.xs32 = reinterpret_cast<float *>(d1_raw + kOffXs32);
     return s;
 }
 
@@ -518,31 +528,162 @@ __device__ __forceinline__ void q2k_tileblock(const uint8_t *tb, const __half *h
     s1 = sh;
 }
 
+// Scale and min (6 bits each) of sub-block j (0..7) of a Q4_K row from its
+// 12 raw scale bytes, given bytes j & 3 of the row's three scale words (w0:
+// bytes 0-3, w1: 4-7, w2: 8-11).
+__device__ __forceinline__ void q4k_scale_min(uint32_t w0, uint32_t w1, uint32_t w2, int j, uint32_t &sc,
+                                              uint32_t &mn) {
+    const uint32_t s0 = (w0 >> (8 * (j & 3))) & 0xffu, s1 = (w1 >> (8 * (j & 3))) & 0xffu;
+    const uint32_t s2 = (w2 >> (8 * (j & 3))) & 0xffu;
+    if (j < 4) {
+        sc = s0 & 63u;
+        mn = s1 & 63u;
+    } else {
+        sc = (s2 & 15u) | ((s0 >> 6) << 4);
+        mn = (s2 >> 4) | ((s1 >> 6) << 4);
+    }
+}
+
+// One Q4_K tile-block (16 rows x 256 cols) of a gate or up piece, block
+// column b, against x (fp16 hi at xq, lo at xq + 4096) and the 32-column sums
+// of x (hi + lo) at xs32.  A quant q enters the mma exactly as the fp16
+// subnormal q * 2^-24 (one shift and one AND build two of them); lane (g, t)
+// owns sub-blocks t and t + 4 of rows g and g + 8, and the block-diagonal B
+// (x in the lanes with g/2 == t) gives it its own sub-blocks' sums, to which
+// it applies d * sc and subtracts dmin * m * sum(x).  Returns the rows' sums
+// (all lanes of the quad hold them).
+__device__ __forceinline__ void q4k_gu_tileblock(const uint8_t *tb, const __half *xq, const float *xs32, int b,
+                                                 int lane, float &r0, float &r1) {
+    const int g = lane >> 2, t = lane & 3;
+    const bool act = (g >> 1) == t;
+    const __half *xrow = xq + (g & 1) * kH + 256 * b;
+    const uint2 dd = *reinterpret_cast<const uint2 *>(tb + 2240 + 8 * g);
+    const float dg0 = __half2float(__ushort_as_half((unsigned short)(dd.x & 0xffffu))) * 16777216.0f;
+    const float dm0 = __half2float(__ushort_as_half((unsigned short)(dd.x >> 16)));
+    const float dg1 = __half2float(__ushort_as_half((unsigned short)(dd.y & 0xffffu))) * 16777216.0f;
+    const float dm1 = __half2float(__ushort_as_half((unsigned short)(dd.y >> 16)));
+    const uint32_t *sa = reinterpret_cast<const uint32_t *>(tb + 2048 + 12 * g);
+    const uint32_t *sb = reinterpret_cast<const uint32_t *>(tb + 2048 + 12 * (g + 8));
+    const uint32_t a0 = sa[0], a1 = sa[1], a2 = sa[2], b0 = sb[0], b1 = sb[1], b2 = sb[2];
+    float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+        const int j = 4 * jj + t;
+        const uint4 qa = *reinterpret_cast<const uint4 *>(tb + 32 * lane + 16 * jj);
+        const uint4 qb = *reinterpret_cast<const uint4 *>(tb + 1024 + 32 * lane + 16 * jj);
+        const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w}, wb[4] = {qb.x, qb.y, qb.z, qb.w};
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+            const uint4 B4 = lds128_if(xrow + 32 * j + 8 * qq, act);
+            const uint32_t Bv[4] = {B4.x, B4.y, B4.z, B4.w};
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int cc = 2 * qq + h2, s0 = 8 * (cc & 1);
+                const uint32_t Wa = wa[cc >> 1], Wb = wb[cc >> 1];
+                mma_f16(c, (Wa >> s0) & 0x000F000Fu, (Wb >> s0) & 0x000F000Fu, (Wa >> (s0 + 4)) & 0x000F000Fu,
+                        (Wb >> (s0 + 4)) & 0x000F000Fu, Bv[2 * h2], Bv[2 * h2 + 1]);
+            }
+        }
+        uint32_t sc0, mn0, sc1, mn1;
+        q4k_scale_min(a0, a1, a2, j, sc0, mn0);
+        q4k_scale_min(b0, b1, b2, j, sc1, mn1);
+        const float X = xs32[8 * b + j];
+        acc0 += dg0 * small_u2f(sc0) * (c[0] + c[1]) - dm0 * small_u2f(mn0) * X;
+        acc1 += dg1 * small_u2f(sc1) * (c[2] + c[3]) - dm1 * small_u2f(mn1) * X;
+    }
+    acc0 += __shfl_xor_sync(0xffffffffu, acc0, 1);
+    acc0 += __shfl_xor_sync(0xffffffffu, acc0, 2);
+    acc1 += __shfl_xor_sync(0xffffffffu, acc1, 1);
+    acc1 += __shfl_xor_sync(0xffffffffu, acc1, 2);
+    r0 = acc0;
+    r1 = acc1;
+}
+
+// One Q4_K tile-block of a routed-down piece, local block column bl (0..3) of
+// the piece's half of h: h fp16 hi at hq, lo at hq + 1024 (each 16 entries
+// scaled by 2^-e), the half's 16-column sums xs[64] and scales xs + 64 (both
+// permuted as in the full slot: sub-block j16 = 4G + t of local block bl at
+// (4 bl + t) * 4 + G).  Returns this lane's partial for rows g and g + 8 (the
+// quad's four lanes sum to the rows).
+__device__ __forceinline__ void q4k_dn_tileblock(const uint8_t *tb, const __half *hq, const float *xs, int bl,
+                                                 int lane, float &s0, float &s1) {
+    const int g = lane >> 2, t = lane & 3;
+    const bool act = (g >> 1) == t;
+    const __half *hrow = hq + (g & 1) * (kF / 2) + 256 * bl;
+    const uint2 dd = *reinterpret_cast<const uint2 *>(tb + 2240 + 8 * g);
+    const float dg0 = __half2float(__ushort_as_half((unsigned short)(dd.x & 0xffffu))) * 16777216.0f;
+    const float dm0 = __half2float(__ushort_as_half((unsigned short)(dd.x >> 16)));
+    const float dg1 = __half2float(__ushort_as_half((unsigned short)(dd.y & 0xffffu))) * 16777216.0f;
+    const float dm1 = __half2float(__ushort_as_half((unsigned short)(dd.y >> 16)));
+    const uint32_t *sa = reinterpret_cast<const uint32_t *>(tb + 2048 + 12 * g);
+    const uint32_t *sb = reinterpret_cast<const uint32_t *>(tb + 2048 + 12 * (g + 8));
+    const uint32_t a0 = sa[0], a1 = sa[1], a2 = sa[2], b0 = sb[0], b1 = sb[1], b2 = sb[2];
+    float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+        const int j = 4 * jj + t;   // 32-column sub-block = 16-column groups 2j, 2j + 1
+        const int ja = 2 * j, jb = 2 * j + 1;
+        const int ia = (bl * 4 + (ja & 3)) * 4 + (ja >> 2), ib = (bl * 4 + (jb & 3)) * 4 + (jb >> 2);
+        const float X = xs[ia] + xs[ib], Sa = xs[64 + ia], Sb = xs[64 + ib];
+        const uint4 qa = *reinterpret_cast<const uint4 *>(tb + 32 * lane + 16 * jj);
+        const uint4 qb = *reinterpret_cast<const uint4 *>(tb + 1024 + 32 * lane + 16 * jj);
+        const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w}, wb[4] = {qb.x, qb.y, qb.z, qb.w};
+        // the two 16-column groups carry their own scales: one accumulator each
+        float c[4] = {0.f, 0.f, 0.f, 0.f}, cb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+            const uint4 B4 = lds128_if(hrow + 32 * j + 8 * qq, act);
+            const uint32_t Bv[4] = {B4.x, B4.y, B4.z, B4.w};
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int cc = 2 * qq + h2, sh = 8 * (cc & 1);
+                const uint32_t Wa = wa[cc >> 1], Wb = wb[cc >> 1];
+                mma_f16(qq < 2 ? c : cb, (Wa >> sh) & 0x000F000Fu, (Wb >> sh) & 0x000F000Fu,
+                        (Wa >> (sh + 4)) & 0x000F000Fu, (Wb >> (sh + 4)) & 0x000F000Fu, Bv[2 * h2], Bv[2 * h2 + 1]);
+            }
+        }
+        uint32_t sc0, mn0, sc1, mn1;
+        q4k_scale_min(a0, a1, a2, j, sc0, mn0);
+        q4k_scale_min(b0, b1, b2, j, sc1, mn1);
+        acc0 += dg0 * small_u2f(sc0) * ((c[0] + c[1]) * Sa + (cb[0] + cb[1]) * Sb) - dm0 * small_u2f(mn0) * X;
+        acc1 += dg1 * small_u2f(sc1) * ((c[2] + c[3]) * Sa + (cb[2] + cb[3]) * Sb) - dm1 * small_u2f(mn1) * X;
+    }
+    s0 = acc0;
+    s1 = acc1;
+}
+
 // ------------------------------------------------------------ job lists
 // Jobs of kind p go to CTA (p even ? j : G-1-j) mod G; a CTA's i-th job of
 // kind p is j = i * G + offset.  Group q takes the CTA's jobs i with
 // (i + rot_p) % 4 == q, rot_p = the CTA's job count of the earlier kinds.
-__device__ __forceinline__ int phase_jobs(int p) {
-    return p == 0 ? kJR : p == 1 ? kJSG : p == 2 ? kJSD : p == 3 ? kJRG : kJRD;
+__device__ __forceinline__ int phase_jobs(int p, int q4) {
+    return p == 0 ? kJR : p == 1 ? kJSG : p == 2 ? kJSD : p == 3 ? kJRG : (q4 ? 2 : 1) * kJRD;
 }
+// Routed slot of routed-down job j (Q4_K: two jobs per slot and tile).
+__device__ __forceinline__ int rd_slot(int j, int q4) { return j / ((q4 ? 2 : 1) * (kH / 16)); }
+// Parts of one 16-row output tile: 4 shared-down quarters + the routed parts.
+__device__ __forceinline__ uint32_t tile_parts(int q4) { return 4u + (uint32_t)((q4 ? 2 : 1) * kK); }
 __device__ __forceinline__ int phase_off(int p, int c, int G) { return (p & 1) ? (G - 1 - c) : c; }
 __device__ __forceinline__ int phase_pieces(int p) { return p == 1 ? 4 : 1; }
 // Routed gate/up claims are pieces: claim i is piece i & 3 of the CTA's job i >> 2.
 __device__ __forceinline__ int claim_units(int p) { return p == 3 ? kRgP : 1; }
 
 // If this warp's counted job was the last of its 16-row output tile (the
-// counter returned kTileParts - 1), sum the tile's partials in a fixed order:
-// the shared expert's four column quarters, then routed experts k = 0..5.
+// counter returned the tile's part count - 1), sum the tile's partials in a
+// fixed order: the shared expert's four column quarters, then the routed
+// parts (experts k = 0..5; Q4_K: expert k's two halves of h, k = 0..5).
+template <bool kQ4>
 __device__ __forceinline__ void finish_tile(const D1Args &a, int tile, uint32_t old_lane0, int lane) {
     if (tile < 0) return;
     const uint32_t old = __shfl_sync(0xffffffffu, old_lane0, 0);
-    if (old != kTileParts - 1) return;
+    if (old != tile_parts(kQ4) - 1u) return;
     if (lane < 16) {
         const int row = 16 * tile + lane;
         float v = (__ldcg(a.p_s + row) + __ldcg(a.p_s + kH + row)) +
                   (__ldcg(a.p_s + 2 * kH + row) + __ldcg(a.p_s + 3 * kH + row));
-#pragma unroll
-        for (int k = 0; k < kK; ++k) v += __ldcg(a.p_r + (size_t)k * kH + row);
+        const int nr = (kQ4 ? 2 : 1) * kK;
+        for (int k = 0; k < nr; ++k) v += __ldcg(a.p_r + (size_t)k * kH + row);
         a.out[row] = v;
     }
     if (lane == 0) a.sync->tile_cnt[tile] = 0u;
@@ -681,6 +822,9 @@ __device__ __forceinline__ void d1_control(const D1Args &a, const D1Smem &sm, in
 }
 
 // ------------------------------------------------------------ kernel
+// kQ4: Q4_K gate/up/down (else IQ2_XXS gate/up, Q2_K down); one instance per
+// layer type, so that each holds only its own decode loops.
+template <bool kQ4>
 __global__ void __launch_bounds__(kD1Threads, 1)
     decode_t1_kernel(const __grid_constant__ CUtensorMap tmSG, const __grid_constant__ CUtensorMap tmSU,
                      const __grid_constant__ CUtensorMap tmSD, D1Args a) {
@@ -718,7 +862,7 @@ __global__ void __launch_bounds__(kD1Threads, 1)
             int cnt[kNPhase];
 #pragma unroll
             for (int p = 0; p < kNPhase; ++p) {
-                const int off = phase_off(p, c, G), n = phase_jobs(p);
+                const int off = phase_off(p, c, G), n = phase_jobs(p, kQ4);
                 cnt[p] = (off < n ? (n - off + G - 1) / G : 0) * claim_units(p);
             }
             volatile int *jc = sm.jc;
@@ -744,7 +888,7 @@ __global__ void __launch_bounds__(kD1Threads, 1)
                         const int off4 = phase_off(4, c, G);
                         int want = -1;
                         if (held >= 0) {
-                            if ((ready >> (held / (kH / 16))) & 1u) {
+                            if ((ready >> rd_slot(held, kQ4)) & 1u) {
                                 p = 4;
                                 j = held;
                                 held = -1;
@@ -759,7 +903,7 @@ __global__ void __launch_bounds__(kD1Threads, 1)
                                 want = 3;
                             } else if (a1) {
                                 want = 1;
-                            } else if (held < 0 && a4 && ((ready >> ((jc[4] * G + off4) / (kH / 16))) & 1u)) {
+                            } else if (held < 0 && a4 && ((ready >> rd_slot(jc[4] * G + off4, kQ4)) & 1u)) {
                                 want = 4;
                             } else if (a2 && hs_ok) {
                                 want = 2;
@@ -774,7 +918,7 @@ __global__ void __launch_bounds__(kD1Threads, 1)
                                     j = (i / u) * G + phase_off(want, c, G);
                                     pc = want == 3 ? (i % kRgP) + 4 * (i / kRgP) : 0;
                                     p = want;
-                                    if (p == 4 && !((ready >> (j / (kH / 16))) & 1u)) {
+                                    if (p == 4 && !((ready >> rd_slot(j, kQ4)) & 1u)) {
                                         held = j;   // another lane took the ready one first
                                         p = -1;
                                     }
@@ -785,7 +929,7 @@ __global__ void __launch_bounds__(kD1Threads, 1)
                         if (p == 3) ++turn;
                         if (p == 1) turn = 0;
                         if (p == 4) {
-                            const int k4 = j / (kH / 16);
+                            const int k4 = rd_slot(j, kQ4);
                             if (!((seen >> k4) & 1u)) {
                                 fence_proxy_async_global();
                                 seen |= 1u << k4;
@@ -812,13 +956,14 @@ __global__ void __launch_bounds__(kD1Threads, 1)
                 d.job = j;
                 d.piece = pc;
                 d.e = 0;
-                const void *src = nullptr, *src2 = nullptr;
+                const uint8_t *src = nullptr, *src2 = nullptr;
+                int rd_half = 0;
                 const CUtensorMap *tmap = nullptr;   // shared-expert pieces: one 3-D tensor copy
                 int trow = 0, tchunk = 0;
                 uint32_t bytes = 0;
                 if (p == 0) {
                     d.kind = PK_ROUTER;
-                    src = a.router + (size_t)j * kH;
+                    src = reinterpret_cast<const uint8_t *>(a.router + (size_t)j * kH);
                     bytes = kH * 4;
                 } else if (p == 1) {
                     // 16 rows x 512 columns of gate (pieces 0, 1) or up (2, 3)
@@ -842,20 +987,30 @@ __global__ void __launch_bounds__(kD1Threads, 1)
                     const uint8_t *mat = sm.eptr[(pq >= kRgSplit ? kK : 0) + k];
                     d.e = k;
                     if (mat) {
-                        src = mat + ((size_t)tile * 16 + kRgTB * (pq % kRgSplit)) * kTB_IQ2;
-                        bytes = kRgTB * kTB_IQ2;
+                        const int tbb = kQ4 ? kTB_Q4K : kTB_IQ2;
+                        src = mat + ((size_t)tile * 16 + kRgTB * (pq % kRgSplit)) * tbb;
+                        bytes = (uint32_t)(kRgTB * tbb);
                     } else {
                         d.e = -1;
                         flag_status(a.status, DS4G_EDEVICE, (uint32_t)sm.ids_s[k]);
                     }
                 } else {
+                    // Q2_K: 8 tile-blocks (16 rows x 2048) + the slot's h; Q4_K:
+                    // 4 tile-blocks (16 rows x 1024, half rd_half of h) + that half
                     d.kind = PK_RDN;
-                    const int k = j / (kH / 16), tile = j % (kH / 16);
+                    const int k = rd_slot(j, kQ4);
+                    const int tile = kQ4 ? (j % (2 * (kH / 16))) >> 1 : j % (kH / 16);
+                    rd_half = kQ4 ? (j & 1) : 0;
                     const uint8_t *mat = sm.eptr[2 * kK + k];
                     d.e = k;
                     if (mat) {
-                        src = mat + (size_t)tile * 8 * kTB_Q2K;
-                        bytes = kRdnW;
+                        if (kQ4) {
+                            src = mat + ((size_t)tile * 8 + 4 * rd_half) * kTB_Q4K;
+                            bytes = 4 * kTB_Q4K;
+                        } else {
+                            src = mat + (size_t)tile * 8 * kTB_Q2K;
+                            bytes = kRdnW;
+                        }
                         src2 = a.hr + (size_t)k * kHSlot;
                     } else {
                         d.e = -1;
@@ -867,9 +1022,19 @@ __global__ void __launch_bounds__(kD1Threads, 1)
                     tc::mbar_arrive_expect_tx(&sm.full[s], bytes);
                     tc::tma_load_3d(slot_al1024(dst), tmap, 0, trow, tchunk, &sm.full[s]);
                 } else if (bytes) {
-                    tc::mbar_arrive_expect_tx(&sm.full[s], bytes + (src2 ? (uint32_t)kHSlot : 0u));
+                    const uint32_t hbytes = !src2 ? 0u : (uint32_t)(kQ4 ? kHSlot / 2 : kHSlot);
+                    tc::mbar_arrive_expect_tx(&sm.full[s], bytes + hbytes);
                     bulk_load(dst, src, bytes, &sm.full[s]);
-                    if (src2) bulk_load(dst + kRdnW, src2, kHSlot, &sm.full[s]);
+                    if (src2 && !kQ4) bulk_load(dst + kRdnW, src2, kHSlot, &sm.full[s]);
+                    if (src2 && kQ4) {
+                        // half rd_half of the slot's h: fp16 hi, lo (1024 each), the
+                        // 64 16-column sums and 64 scales of its four blocks
+                        uint8_t *hd = dst + bytes;
+                        bulk_load(hd, src2 + 2048 * rd_half, 2048, &sm.full[s]);
+                        bulk_load(hd + 2048, src2 + 2 * kF + 2048 * rd_half, 2048, &sm.full[s]);
+                        bulk_load(hd + 4096, src2 + 4 * kF + 256 * rd_half, 256, &sm.full[s]);
+                        bulk_load(hd + 4352, src2 + 4 * kF + 512 + 256 * rd_half, 256, &sm.full[s]);
+                    }
                 } else {
                     tc::mbar_arrive(&sm.full[s]);
                 }
@@ -902,7 +1067,7 @@ __global__ void __launch_bounds__(kD1Threads, 1)
         const int q = cw / kGW, wq = cw % kGW;
         // tables (all 16 consumer warps) while the activation streams in
         bool gbad = false;
-        if (ct < 256) {
+        if (ct < 256 && !kQ4) {   // Q4_K layers have no grid (a.grid may be NULL)
             const unsigned long long grow = __ldg(reinterpret_cast<const unsigned long long *>(a.grid) + ct);
             uint32_t sel = 0;
             bool bad = false;
@@ -957,6 +1122,21 @@ __global__ void __launch_bounds__(kD1Threads, 1)
             sm.xb[kXLd + ct + 512 * i] = bl;
         }
         asm volatile("bar.sync 1, %0;" ::"n"(kD1Cons * 32));
+        if (kQ4) {
+            // sums of x (fp16 hi + lo, as the mma sees it) over each 32-column
+            // sub-block, for the Q4_K mins: four threads per sub-block
+            const int sb = ct >> 2, part = ct & 3;
+            float xs = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int col = 32 * sb + 8 * part + i;
+                xs += __half2float(sm.xq[col]) + __half2float(sm.xq[kH + col]);
+            }
+            xs += __shfl_xor_sync(0xffffffffu, xs, 1);
+            xs += __shfl_xor_sync(0xffffffffu, xs, 2);
+            if (part == 0) sm.xs32[sb] = xs;
+            asm volatile("bar.sync 1, %0;" ::"n"(kD1Cons * 32));
+        }
 
         // accumulator of a gate/up job across its pieces: routed (gate rows g, g+8,
         // up rows g, g+8) or shared (the mma accumulator of gate, then of up)
@@ -1013,13 +1193,24 @@ __global__ void __launch_bounds__(kD1Threads, 1)
                 float t0 = 0.f, t1 = 0.f;
                 if (d.e >= 0) {
                     const int b0 = kRgTB * ((d.piece & 3) % kRgSplit) + (kRgTB / 4) * wq;
+                    if (kQ4) {
+#pragma unroll 1
+                        for (int u = 0; u < kRgTB / 4; ++u) {
+                            float u0, u1;
+                            q4k_gu_tileblock(slot + (size_t)((kRgTB / 4) * wq + u) * kTB_Q4K, sm.xq, sm.xs32, b0 + u,
+                                             lane, u0, u1);
+                            t0 += u0;
+                            t1 += u1;
+                        }
+                    } else {
 #pragma unroll
-                    for (int cb = 0; cb < kRgTB / 8; ++cb) {
-                        float u0, u1;
-                        iq2_tileblock2(sm, slot + (size_t)((kRgTB / 4) * wq + 2 * cb) * kTB_IQ2, b0 + 2 * cb, lane,
-                                       u0, u1);
-                        t0 += u0;
-                        t1 += u1;
+                        for (int cb = 0; cb < kRgTB / 8; ++cb) {
+                            float u0, u1;
+                            iq2_tileblock2(sm, slot + (size_t)((kRgTB / 4) * wq + 2 * cb) * kTB_IQ2, b0 + 2 * cb,
+                                           lane, u0, u1);
+                            t0 += u0;
+                            t1 += u1;
+                        }
                     }
                 }
                 if ((lane & 3) == 0) {
@@ -1038,7 +1229,12 @@ __global__ void __launch_bounds__(kD1Threads, 1)
                 last = true;
             } else {  // PK_RDN: eight Q2_K tile-blocks of one expert; warp wq: tile-blocks 2wq, 2wq+1
                 float s0 = 0.f, s1 = 0.f;
-                if (d.e >= 0) {
+                if (d.e >= 0 && kQ4) {
+                    // warp wq: tile-block wq of the piece (local block column wq of its half of h)
+                    const uint8_t *hd = slot + 4 * kTB_Q4K;
+                    q4k_dn_tileblock(slot + (size_t)wq * kTB_Q4K, reinterpret_cast<const __half *>(hd),
+                                     reinterpret_cast<const float *>(hd + 4096), wq, lane, s0, s1);
+                } else if (d.e >= 0) {
                     const __half *hq = reinterpret_cast<const __half *>(slot + kRdnW);
                     const float *xs = reinterpret_cast<const float *>(slot + kRdnW + 4 * kF);
                     float a0, a1, b0, b1;
@@ -1161,11 +1357,13 @@ __global__ void __launch_bounds__(kD1Threads, 1)
                         a.p_s[(size_t)kq * kH + 16 * ot + lane] =
                             (red[lane] + red[16 + lane]) + (red[32 + lane] + red[48 + lane]);
                     tile = ot;
-                } else {  // routed down partial of one expert, weighted
-                    const int k = d.job / (kH / 16), tl = d.job % (kH / 16);
+                } else {  // routed down partial of one expert (Q4_K: of one half of h), weighted
+                    const int k = rd_slot(d.job, kQ4);
+                    const int tl = kQ4 ? (d.job % (2 * (kH / 16))) >> 1 : d.job % (kH / 16);
+                    const int part = kQ4 ? 2 * k + (d.job & 1) : k;
                     if (lane < 16) {
                         const float v = (red[lane] + red[16 + lane]) + (red[32 + lane] + red[48 + lane]);
-                        a.p_r[(size_t)k * kH + 16 * tl + lane] = d.e >= 0 ? sm.wk[k] * v : 0.f;
+                        a.p_r[(size_t)part * kH + 16 * tl + lane] = d.e >= 0 ? sm.wk[k] * v : 0.f;
                     }
                     tile = tl;
                 }
@@ -1173,7 +1371,7 @@ __global__ void __launch_bounds__(kD1Threads, 1)
                     // Count this job into its output tile; the last of the tile's ten
                     // jobs sums the partials.  The counter's old value is examined
                     // only at this warp's next job end, so its latency is hidden.
-                    finish_tile(a, pend_tile, pend_old, lane);
+                    finish_tile<kQ4>(a, pend_tile, pend_old, lane);
                     __syncwarp();
                     pend_old = 0u;
                     if (lane == 0) pend_old = atom_add_acq_rel(&a.sync->tile_cnt[tile], 1u);
@@ -1182,7 +1380,7 @@ __global__ void __launch_bounds__(kD1Threads, 1)
             }
             gpar ^= 1;
         }
-        finish_tile(a, pend_tile, pend_old, lane);
+        finish_tile<kQ4>(a, pend_tile, pend_old, lane);
     }
 
     // ================================================== exit protocol
@@ -1223,39 +1421,15 @@ static D1Layout d1_layout() {
     L.p_s = off;
     off += align_up((size_t)4 * kH * 4, 256);
     L.p_r = off;
-    off += align_up((size_t)kK * kH * 4, 256);
+    off += align_up((size_t)2 * kK * kH * 4, 256);
     L.total = off;
     return L;
 }
 
-// Layers of a stack that are not IQ2_XXS/Q2_K (the q4 layers: Q4_K
-// gate/up/down) run as rmsnorm + route + the decode path of the forward.
-// Their scratch follows the fused kernel's part of the workspace: the
-// normalised input, the route's ids and weights (16-byte aligned rows), and
-// the route's and the forward's own workspaces.  Faults are recorded in the
-// workspace's header, as for the fused layers.
-struct StackLayout {
-    size_t xn, ids, w, route_ws, fwd_ws, total;
-};
-static StackLayout stack_layout() {
-    StackLayout L;
-    size_t off = align_up(d1_layout().total, 256);
-    L.xn = off;
-    off += align_up((size_t)kH * 4, 256);
-    L.ids = off;
-    off += 256;
-    L.w = off;
-    off += 256;
-    L.route_ws = off;
-    off += align_up(ds4g_route_workspace(1), 256);
-    L.fwd_ws = off;
-    off += align_up(decode_workspace(1), 256);
-    L.total = off;
-    return L;
-}
-
-static bool d1_fused(const ds4g_layer *L) {
-    return L->gate_up_type == DS4G_IQ2_XXS && L->down_type == DS4G_Q2_K;
+// The fused kernel's layer types: IQ2_XXS gate/up with Q2_K down, or Q4_K throughout.
+static bool d1_types_ok(const ds4g_layer *L) {
+    return (L->gate_up_type == DS4G_IQ2_XXS && L->down_type == DS4G_Q2_K) ||
+           (L->gate_up_type == DS4G_Q4_K && L->down_type == DS4G_Q4_K);
 }
 
 static int g_d1_sms = 0;
@@ -1268,56 +1442,17 @@ static ds4g_status d1_check(const float *hidden, const float *router, const floa
                             size_t ws_bytes) {
     if (!hidden || !router || !bias || !L || !ids || !w || !out || !workspace) return DS4G_EINVAL;
     if (!L->gate || !L->up || !L->down || !L->sh_gate || !L->sh_up || !L->sh_down) return DS4G_EINVAL;
-    if (L->gate_up_type != DS4G_IQ2_XXS || L->down_type != DS4G_Q2_K) return DS4G_EUNSUPPORTED;
-    if (!L->iq2_grid) return DS4G_EINVAL;
+    if (!d1_types_ok(L)) return DS4G_EUNSUPPORTED;
+    const bool iq2 = L->gate_up_type == DS4G_IQ2_XXS;
+    if (iq2 && !L->iq2_grid) return DS4G_EINVAL;
     // ids and w are written element by element: 4-byte alignment suffices (a
     // stack's per-layer rows of 6 are not 16-byte aligned)
     const uintptr_t al = (uintptr_t)hidden | (uintptr_t)router | (uintptr_t)bias | (uintptr_t)out |
                          (uintptr_t)workspace | (uintptr_t)L->gate | (uintptr_t)L->up | (uintptr_t)L->down |
-                         (uintptr_t)L->sh_gate | (uintptr_t)L->sh_up | (uintptr_t)L->sh_down | (uintptr_t)L->iq2_grid;
+                         (uintptr_t)L->sh_gate | (uintptr_t)L->sh_up | (uintptr_t)L->sh_down |
+                         (iq2 ? (uintptr_t)L->iq2_grid : 0);
     if ((al & 15) || (((uintptr_t)ids | (uintptr_t)w) & 3)) return DS4G_EALIGN;
     if (ws_bytes < d1_layout().total) return DS4G_ENOSPACE;
-    return DS4G_OK;
-}
-
-// Host checks of one stack layer: the fused kernel's for IQ2_XXS/Q2_K
-// layers; for Q4_K layers the forward's, against the larger workspace.
-static ds4g_status stack_layer_check(const float *hidden, const float *router, const float *bias,
-                                     const ds4g_layer *L, const int32_t *ids, const float *w, const float *out,
-                                     const void *workspace, size_t ws_bytes) {
-    if (!L) return DS4G_EINVAL;
-    if (d1_fused(L)) return d1_check(hidden, router, bias, L, ids, w, out, workspace, ws_bytes);
-    if (L->gate_up_type != DS4G_Q4_K || L->down_type != DS4G_Q4_K) return DS4G_EUNSUPPORTED;
-    if (!hidden || !router || !bias || !ids || !w || !out || !workspace) return DS4G_EINVAL;
-    if (!L->gate || !L->up || !L->down || !L->sh_gate || !L->sh_up || !L->sh_down) return DS4G_EINVAL;
-    const uintptr_t al = (uintptr_t)hidden | (uintptr_t)router | (uintptr_t)bias | (uintptr_t)out |
-                         (uintptr_t)workspace | (uintptr_t)L->gate | (uintptr_t)L->up | (uintptr_t)L->down |
-                         (uintptr_t)L->sh_gate | (uintptr_t)L->sh_up | (uintptr_t)L->sh_down;
-    if ((al & 15) || (((uintptr_t)ids | (uintptr_t)w) & 3)) return DS4G_EALIGN;
-    if (ws_bytes < stack_layout().total) return DS4G_ENOSPACE;
-    return DS4G_OK;
-}
-
-// One Q4_K layer of a stack: xn = rmsnorm(x); ids, w = route(xn); o = the
-// decode forward of xn.  ids/w rows of the stack are only 4-byte aligned,
-// so the route writes aligned scratch rows that are then copied out.
-static ds4g_status stack_run_unfused(const float *x, const float *router, const float *bias, const ds4g_layer *L,
-                                     int32_t *ids, float *w, float *o, void *workspace, cudaStream_t s) {
-    const StackLayout lay = stack_layout();
-    uint8_t *ws = (uint8_t *)workspace;
-    float *xn = (float *)(ws + lay.xn);
-    int32_t *ids_t = (int32_t *)(ws + lay.ids);
-    float *w_t = (float *)(ws + lay.w);
-    ds4g_status st = ds4g_rmsnorm(x, 1, xn, (ds4g_stream_t)s);
-    if (st != DS4G_OK) return st;
-    st = ds4g_moe_route(xn, 1, router, bias, ids_t, w_t, ws + lay.route_ws, ds4g_route_workspace(1),
-                        (ds4g_stream_t)s);
-    if (st != DS4G_OK) return st;
-    st = decode_forward(xn, 1, L, ids_t, w_t, o, ws + lay.fwd_ws, s, 3, (uint32_t *)ws);
-    if (st != DS4G_OK) return st;
-    if (cudaMemcpyAsync(ids, ids_t, kK * sizeof(int32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
-        cudaMemcpyAsync(w, w_t, kK * sizeof(float), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
-        return DS4G_ECUDA;
     return DS4G_OK;
 }
 
@@ -1330,8 +1465,10 @@ static ds4g_status d1_setup() {
     // one CTA per SM; a CTA holds at most kRgLocal routed gate/up jobs
     if ((kJRG + g_d1_sms - 1) / g_d1_sms > kRgLocal) return DS4G_EUNSUPPORTED;
     if (!g_d1_attr) {
-        if (cudaFuncSetAttribute(decode_t1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kD1SmemBytes) !=
-            cudaSuccess)
+        if (cudaFuncSetAttribute(decode_t1_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kD1SmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(decode_t1_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kD1SmemBytes) != cudaSuccess)
             return DS4G_ECUDA;
         g_d1_attr = true;
     }
@@ -1346,6 +1483,7 @@ static D1Args d1_args(const float *hidden, int normalize, const float *router, c
     a.x = hidden;
     a.normalize = normalize ? 1 : 0;
     a.pdl = 0;
+    a.q4 = L->gate_up_type == DS4G_Q4_K ? 1 : 0;
     // under the test hook the control warp waits for one router row more
     // than exists and gives up after ~130 us (2^18 cycles) instead of ~1 s
     a.router_extra = g_d1_force_timeout ? 1u : 0u;
@@ -1393,7 +1531,9 @@ static ds4g_status d1_launch(const D1Args &a, cudaStream_t s, bool pdl) {
     if (!tmap_bf16_rowtile(&mg, a.sh_gate, kF, kH, 16, 8) || !tmap_bf16_rowtile(&mu, a.sh_up, kF, kH, 16, 8) ||
         !tmap_bf16_rowtile(&md, a.sh_down, kH, kF, 16, 8))
         return DS4G_ECUDA;
-    return cudaLaunchKernelEx(&cfg, decode_t1_kernel, mg, mu, md, b) == cudaSuccess ? DS4G_OK : DS4G_ECUDA;
+    const cudaError_t e = a.q4 ? cudaLaunchKernelEx(&cfg, decode_t1_kernel<true>, mg, mu, md, b)
+                               : cudaLaunchKernelEx(&cfg, decode_t1_kernel<false>, mg, mu, md, b);
+    return e == cudaSuccess ? DS4G_OK : DS4G_ECUDA;
 }
 
 }  // namespace ds4g
@@ -1404,7 +1544,7 @@ extern "C" size_t ds4g_layer_decode_workspace(void) { return d1_layout().total; 
 
 extern "C" void ds4g_test_force_timeout(int on) { g_d1_force_timeout = on ? 1 : 0; }
 
-extern "C" size_t ds4g_decode_stack_workspace(void) { return stack_layout().total; }
+extern "C" size_t ds4g_decode_stack_workspace(void) { return d1_layout().total; }
 
 extern "C" ds4g_status ds4g_moe_layer_decode(const float *hidden, int normalize, const float *router,
                                              const float *bias, const ds4g_layer *L, int32_t *ids, float *w,
@@ -1425,8 +1565,8 @@ extern "C" ds4g_status ds4g_moe_decode_stack(const float *hidden, int n_layers, 
     if (n_layers < 1 || n_layers > 1024 || !routers || !biases || !layers || !hbuf || !ids || !w) return DS4G_EINVAL;
     if (((uintptr_t)hbuf | (uintptr_t)ids | (uintptr_t)w) & 15) return DS4G_EALIGN;
     for (int l = 0; l < n_layers; ++l) {
-        const ds4g_status st = stack_layer_check(hidden, routers[l], biases[l], &layers[l], ids + kK * l,
-                                                 w + kK * l, out, workspace, ws_bytes);
+        const ds4g_status st = d1_check(hidden, routers[l], biases[l], &layers[l], ids + kK * l, w + kK * l, out,
+                                        workspace, ws_bytes);
         if (st != DS4G_OK) return st;
     }
     ds4g_status st = d1_setup();
@@ -1434,16 +1574,9 @@ extern "C" ds4g_status ds4g_moe_decode_stack(const float *hidden, int n_layers, 
     for (int l = 0; l < n_layers; ++l) {
         const float *x = l == 0 ? hidden : hbuf + (size_t)((l - 1) & 1) * kH;
         float *o = l == n_layers - 1 ? out : hbuf + (size_t)(l & 1) * kH;
-        if (d1_fused(&layers[l])) {
-            // a programmatic dependent only of the same kernel (a fused previous layer)
-            const bool pdl = l > 0 && d1_fused(&layers[l - 1]);
-            st = d1_launch(
-                d1_args(x, 1, routers[l], biases[l], &layers[l], ids + kK * l, w + kK * l, o, workspace),
-                (cudaStream_t)s, pdl);
-        } else {
-            st = stack_run_unfused(x, routers[l], biases[l], &layers[l], ids + kK * l, w + kK * l, o, workspace,
-                                   (cudaStream_t)s);
-        }
+        // each layer after the first: a programmatic dependent of the previous one
+        st = d1_launch(d1_args(x, 1, routers[l], biases[l], &layers[l], ids + kK * l, w + kK * l, o, workspace),
+                       (cudaStream_t)s, l > 0);
         if (st != DS4G_OK) return st;
     }
     return DS4G_OK;

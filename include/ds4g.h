@@ -261,9 +261,12 @@ ds4g_status ds4g_moe_down(const float *hidden, int T, const ds4g_layer *L,
  *   out    = ds4g_moe_forward(xn, ids, w)
  * hidden [4096] f32 dev (T = 1), router [256][4096] f32 dev, bias [256] f32
  * dev, ids [6] int32 dev (out), w [6] f32 dev (out), out [4096] f32 dev.
- * Only IQ2_XXS/Q2_K layers (else DS4G_EUNSUPPORTED; use route + forward).
- * Arithmetic as the decode path of ds4g_moe_forward, except that the shared
- * expert is summed in fp32 FMA.  workspace dev >= ds4g_layer_decode_workspace()
+ * Layer types: IQ2_XXS gate/up with Q2_K down, or Q4_K gate/up/down (the q4
+ * layers of the q2-q4 model, [P1] §2.1; iq2_grid may be NULL for them); any
+ * other pair -> DS4G_EUNSUPPORTED.  Arithmetic as the decode path of
+ * ds4g_moe_forward (exact codes, fp16 hi+lo activation, fp32 scales), except
+ * that the shared expert runs on bf16 tensor cores with the activation and
+ * the shared h as bf16 hi+lo pairs.  workspace dev >= ds4g_layer_decode_workspace()
  * bytes, zeroed once before first use (the kernel leaves its counters at
  * zero); one call at a time per workspace.  h enters the down projection
  * as an fp16 hi+lo pair scaled by a power of two per 16 entries (any finite
@@ -286,11 +289,9 @@ ds4g_status ds4g_moe_layer_decode(const float *hidden, int normalize, const floa
  *   x_0 = hidden,  x_l = output of layer l-1  (l >= 1);
  * every layer's input is RMS-normalised and no residual is added (the
  * full-depth decode workload of 43 such layers).  Layer l is
- *  - IQ2_XXS gate/up + Q2_K down: ds4g_moe_layer_decode with normalize = 1;
- *  - Q4_K gate/up/down (the q4 layers of the q2-q4 model, chenxutan ds4
- *    article §2.1): ds4g_rmsnorm, then ds4g_moe_route, then the T = 1
- *    ds4g_moe_forward, all on s;
- *  - any other type combination: DS4G_EUNSUPPORTED.
+ * ds4g_moe_layer_decode with normalize = 1, for either layer type that call
+ * takes (IQ2_XXS/Q2_K, or Q4_K throughout: the q2-q4 and q4 models,
+ * chenxutan ds4 article §2.1); any other type pair: DS4G_EUNSUPPORTED.
  *   hidden   [4096] f32 dev            routers  host array [n_layers] of dev
  *   layers   host array [n_layers]       pointers to [256][4096] f32
  *   biases   host array [n_layers] of dev pointers to [256] f32
@@ -298,14 +299,13 @@ ds4g_status ds4g_moe_layer_decode(const float *hidden, int normalize, const floa
  *   hbuf     [2][4096] f32 dev: scratch for the intermediate outputs
  *   out      [4096] f32 dev: the last layer's output
  *   workspace dev, zeroed once before first use, one call at a time; one
- *            workspace serves all layers: >= ds4g_layer_decode_workspace()
- *            bytes if every layer is IQ2_XXS/Q2_K, >=
- *            ds4g_decode_stack_workspace() bytes if any layer is Q4_K (else
- *            DS4G_ENOSPACE).  Faults are read with ds4g_last_error.
+ *            workspace serves all layers: >= ds4g_decode_stack_workspace()
+ *            bytes (equal to ds4g_layer_decode_workspace()), else
+ *            DS4G_ENOSPACE.  Faults are read with ds4g_last_error.
  * 1 <= n_layers <= 1024, else DS4G_EINVAL.  All checks of every layer run
  * before the first launch.  Same results, bit for bit, as the per-layer
- * calls listed above.  A fused layer that follows a fused layer is a
- * programmatic dependent launch: its CTAs start on the SMs that the previous
+ * calls.  Every layer after the first is a programmatic dependent launch of
+ * the previous one: its CTAs start on the SMs that the previous
  * layer's CTAs leave, build their tables and begin streaming the layer's
  * router and shared-expert weights, and read their input and the workspace
  * only after the previous layer has completed.
@@ -319,8 +319,8 @@ ds4g_status ds4g_moe_decode_stack(const float *hidden, int n_layers, const float
 /* ------------------------------------------------------------------------
  * Test hook of the bounded waits (no counterpart in the pages: it exists to
  * exercise DS4G_ETIMEOUT without hanging or faulting a GPU).  While on != 0,
- * every launch of the fused layer kernel (ds4g_moe_layer_decode and the
- * IQ2_XXS/Q2_K layers of ds4g_moe_decode_stack) makes its control warps wait
+ * every launch of the fused layer kernel (ds4g_moe_layer_decode and every
+ * layer of ds4g_moe_decode_stack) makes its control warps wait
  * for one router row more than the layer has, giving up after about 130 us:
  * the launch aborts, drains its copies, records DS4G_ETIMEOUT in the
  * workspace and leaves it usable.  Process-wide, host-side only;

@@ -138,16 +138,18 @@ def test_gpu_entry_points_validate_before_launch():
 
 
 def test_decode_stack_validates_layer_types_and_workspace():
-    """The stack checks every layer before any CUDA call: Q4_K layers need
-    the larger stack workspace, mixed IQ2/Q4_K types are refused."""
+    """The stack checks every layer before any CUDA call: IQ2_XXS/Q2_K and
+    Q4_K layers share the fused kernel's workspace; mixed IQ2/Q4_K types in
+    one layer, a misaligned pointer and a missing router are refused."""
     L = B.lib()
     fake = 0x10000000
     q2 = B.ds4g_layer(0, 1, fake, fake, fake, fake, fake, fake, fake)
-    q4 = B.ds4g_layer(2, 2, fake, fake, fake, fake, fake, fake, None)
+    q4 = B.ds4g_layer(2, 2, fake, fake, fake, fake, fake, fake, None)   # Q4_K layers need no grid
     mix = B.ds4g_layer(0, 2, fake, fake, fake, fake, fake, fake, fake)
     q4_odd = B.ds4g_layer(2, 2, fake, fake, fake, fake + 8, fake, fake, None)
-    small, big = B.ds4g_layer_decode_workspace(), B.ds4g_decode_stack_workspace()
-    assert small < big
+    q2_nogrid = B.ds4g_layer(0, 1, fake, fake, fake, fake, fake, fake, None)
+    ws = B.ds4g_decode_stack_workspace()
+    assert ws == B.ds4g_layer_decode_workspace()
 
     def stack(layers, ws_bytes, routers=True):
         n = len(layers)
@@ -156,11 +158,11 @@ def test_decode_stack_validates_layer_types_and_workspace():
         return L.ds4g_moe_decode_stack(fake, n, ptrs if routers else None, ptrs, structs, fake, fake, fake, fake,
                                        fake, ws_bytes, None)
 
-    assert stack([q2, q4], small) == 3          # q4 layers use scratch beyond the fused kernel's
-    assert stack([q4], big - 1) == 3
-    assert stack([q2, mix], big) == 5
-    assert stack([q4_odd], big) == 2
-    assert stack([q2, q4], big, routers=False) == 1
+    assert stack([q2, q4], ws - 1) == 3
+    assert stack([q2, mix], ws) == 5
+    assert stack([q4_odd], ws) == 2
+    assert stack([q2_nogrid], ws) == 1
+    assert stack([q2, q4], ws, routers=False) == 1
 
 
 def test_workspace_sizes_grow_with_T():

@@ -149,9 +149,10 @@ def test_decode_stack_rejects_bad_arguments():
 
 def test_decode_stack_q2_q4_layers():
     """A stack of IQ2_XXS/Q2_K and Q4_K layers (the q2-q4 model keeps its
-    last layers at Q4_K): the fused kernel runs the q2 layers, rmsnorm +
-    route + forward the q4 layers.  Equal bit for bit to those calls made
-    one at a time, and following the oracle's chain."""
+    last layers at Q4_K), every layer on the fused kernel (Q4_K tile-blocks
+    in its routed pieces).  Equal bit for bit to single-layer calls made one
+    at a time, and following the oracle's chain (chained Q4_K layers drive h
+    far beyond the fp16 range)."""
     seed, cfg = 5, 4
     kinds = [(synth.IQ2_XXS, synth.Q2_K), (synth.Q4_K, synth.Q4_K), (synth.Q4_K, synth.Q4_K),
              (synth.IQ2_XXS, synth.Q2_K)]
@@ -174,10 +175,7 @@ def test_decode_stack_q2_q4_layers():
     hbuf = torch.zeros(2, H, dtype=torch.float32, device=DEV)
     out = torch.full((H,), float("nan"), dtype=torch.float32, device=DEV)
     xd = _t(x[0])
-    assert B.ds4g_decode_stack_workspace() > B.ds4g_layer_decode_workspace()
-    with pytest.raises(B.DS4GError) as e:       # q4 layers need the larger workspace
-        B.ds4g_moe_decode_stack(xd, stack, ids, w, hbuf, out, B.workspace(B.ds4g_layer_decode_workspace()))
-    assert e.value.code == 3
+    assert B.ds4g_decode_stack_workspace() == B.ds4g_layer_decode_workspace()
     ws = B.workspace(B.ds4g_decode_stack_workspace())
     for _ in range(2):                               # the workspace is reusable call after call
         B.ds4g_moe_decode_stack(xd, stack, ids, w, hbuf, out, ws)
@@ -189,24 +187,36 @@ def test_decode_stack_q2_q4_layers():
     assert_close_fwd(out_s[None], refs[-1][4])
     # the same layers one call at a time
     wsl = B.workspace(B.ds4g_layer_decode_workspace())
-    rws = B.workspace(B.ds4g_route_workspace(1))
-    fws = B.workspace(B.ds4g_forward_workspace(1))
     xl = xd[None]
-    for l, ((gut, _), (L, R, b)) in enumerate(zip(kinds, layers)):
+    for l, (L, R, b) in enumerate(layers):
         i1 = torch.full((1, K), -1, dtype=torch.int32, device=DEV)
         w1 = torch.zeros(1, K, dtype=torch.float32, device=DEV)
         o1 = torch.empty(1, H, dtype=torch.float32, device=DEV)
-        if gut == synth.IQ2_XXS:
-            B.ds4g_moe_layer_decode(xl[0], R, b, L.struct, i1[0], w1[0], o1[0], wsl)
-        else:
-            xn = torch.empty(1, H, dtype=torch.float32, device=DEV)
-            B.ds4g_rmsnorm(xl, xn)
-            B.ds4g_moe_route(xn, R, b, i1, w1, rws)
-            B.ds4g_moe_forward(xn, L.struct, i1, w1, o1, fws)
+        B.ds4g_moe_layer_decode(xl[0], R, b, L.struct, i1[0], w1[0], o1[0], wsl)
         assert np.array_equal(i1.cpu().numpy()[0], ids_s[l]) and np.array_equal(w1.cpu().numpy()[0], w_s[l])
         xl = o1
     assert np.array_equal(xl.cpu().numpy()[0], out_s)
-    assert B.ds4g_last_error(wsl) == 0 and B.ds4g_last_error(fws) == 0
+    assert B.ds4g_last_error(wsl) == 0
+
+
+@pytest.mark.parametrize("seed,zipf", [(8, False), (9, True)])
+def test_layer_decode_q4k_matches_oracle(seed, zipf):
+    """One Q4_K layer (gate/up/down) on the fused kernel: routed gate/up
+    pieces of 8 Q4_K tile-blocks, routed down in halves of h (16 output
+    parts per tile), against the oracle; repeatable on one workspace."""
+    xraw = synth.hidden(seed, 4, 1, layer=3, normalise=False)
+    R = synth.router(seed, 4)
+    b = synth.bias_zipf(seed, 4) if zipf else synth.bias_normal(seed, 4)
+    xn = oracle.rmsnorm(xraw)
+    ids_r, w_r, keys, margin = oracle.route(xn, R, b)
+    L, hx, shared, grid = device_layer(seed, 4, 0, ids_r.reshape(-1), synth.Q4_K, synth.Q4_K)
+    ws = B.workspace(B.ds4g_layer_decode_workspace())
+    ids, w, out, st = _run(xraw[0], R, b, L, ws)
+    assert st == 0
+    check_route(ids[None], w[None], ids_r, w_r, keys, margin)
+    assert_close_fwd(out[None], oracle_forward(xn, ids[None], w[None], hx, shared, grid, synth.Q4_K, synth.Q4_K))
+    again = _run(xraw[0], R, b, L, ws)
+    assert again[3] == 0 and np.array_equal(again[2], out)
 
 
 def test_layer_decode_h_beyond_fp16_range():
