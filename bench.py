@@ -376,6 +376,11 @@ def run_stream(args, rank, world, local_rank):
         for hb, t in zip(host, L.tensors[:3]):
             hb.copy_(t)
         src = B.HostExperts(*[{e: hb[e] for e in range(E)} for hb in host])
+        if args.stream_source == "file":
+            # the layer's experts in an expert file; the host copies are dropped
+            path = os.path.join(args.stream_dir, "ds4g_layer%d.ds4gexp" % len(layers))
+            B.ds4g_expert_file_write(path, src)
+            src, host = B.ExpertFile(path), None
         layers.append((src, host, L.tensors[3:7], R, b))
     del built, L, t
     torch.cuda.synchronize()
@@ -400,7 +405,10 @@ def run_stream(args, rank, world, local_rank):
                 dst = out_all[i:i + 1] if l == nl - 1 else act[l & 1]
                 B.ds4g_rmsnorm(cur, xn)
                 B.ds4g_moe_route(xn, R, b, ids, w, rws)
-                B.ds4g_moe_forward_streamed(xn, l, src, sg, su, sd, grid, ids, w, dst, cache, fws)
+                if args.stream_source == "file":
+                    B.ds4g_moe_forward_streamed_file(xn, l, src, sg, su, sd, grid, ids, w, dst, cache, fws)
+                else:
+                    B.ds4g_moe_forward_streamed(xn, l, src, sg, su, sd, grid, ids, w, dst, cache, fws)
                 cur = dst
 
     for _ in range(args.warmup):
@@ -462,7 +470,9 @@ def run_stream(args, rank, world, local_rank):
         "metric": METRIC, "value": round(tokens / dev_s, 3), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dev_s / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": ST_WORKLOAD.format(nl=nl, slots=slots, ntok=ntok), "layers": nl,
+        "config": {"workload": ST_WORKLOAD.format(nl=nl, slots=slots, ntok=ntok).replace(
+                       "in pinned host memory", "in pinned host memory" if args.stream_source == "host"
+                       else "in expert files (read with pread on a miss)"), "layers": nl,
                    "tokens_per_step": ntok, "cache_slots": slots,
                    "cache_gb": round(slots * per_expert / 1e9, 3), "host_expert_gb": round(nl * E * per_expert / 1e9, 2),
                    "global_batch": 1, "seq_len": 1, "parallelism": "replicas" if world > 1 else "single",
@@ -471,7 +481,9 @@ def run_stream(args, rank, world, local_rank):
                        round(misses / (ntok * args.steps * nl), 3), "setup_s": round(setup_s, 1)},
         "e2e": {"value": round(tokens / e2e_s, 3), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(x_host.numel() * 4), "d2h_bytes_per_step": int(y_host.numel() * 4)},
-        "roofline": {"bound": "h2d", "kernel": "expert copies host -> HBM (cudaMemcpyAsync from pinned memory)",
+        "roofline": {"bound": "h2d", "kernel": ("expert copies host -> HBM (cudaMemcpyAsync from pinned memory)"
+                                                if args.stream_source == "host" else
+                                                "expert reads (pread, 2 pinned staging buffers) + copies -> HBM"),
                      "achieved": round(achieved, 2), "peak": round(h2d_peak, 2),
                      "peak_kind": "measured in this run: 1 GiB pinned host -> device copy", "unit": "GB/s",
                      "frac": round(achieved / h2d_peak, 4), "bytes_copied": int(nbytes), "traffic": None},
@@ -1017,6 +1029,9 @@ def main():
                          "memory through an HBM cache")
     ap.add_argument("--stream-layers", type=int, default=4, help="decode-stream: layers (host memory 1.8 GB each)")
     ap.add_argument("--cache-slots", type=int, default=256, help="decode-stream: HBM cache slots (7.1 MB each)")
+    ap.add_argument("--stream-source", choices=["host", "file"], default="host",
+                    help="decode-stream: routed experts in pinned host memory, or in expert files read on a miss")
+    ap.add_argument("--stream-dir", default="/tmp", help="decode-stream --stream-source file: directory of the files")
     ap.add_argument("--batched-copies", type=int, default=B2_COPIES,
                     help="batched: layer copies used in turn (8 keeps every call cold in L2; fewer only for profiling)")
     ap.add_argument("--model", choices=["q2", "q2-q4", "q4"], default="q2",

@@ -85,6 +85,10 @@ def lib():
             "ds4g_moe_forward_streamed": ([vp, i, i, C.POINTER(ds4g_host_experts), vp, vp, vp, vp, vp, vp, vp, vp,
                                            vp, sz, vp], i),
             "ds4g_expert_lru_simulate": ([i, i, vp, vp, vp, vp], i),
+            "ds4g_expert_file_write": ([C.c_char_p, C.POINTER(ds4g_host_experts)], i),
+            "ds4g_expert_file_open": ([C.c_char_p, C.POINTER(vp)], i),
+            "ds4g_expert_file_close": ([vp], i),
+            "ds4g_moe_forward_streamed_file": ([vp, i, i, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i),
             "ds4g_rmsnorm": ([vp, i, vp, vp], i),
             "ds4g_last_error": ([vp, vp], i),
         }
@@ -325,6 +329,41 @@ def ds4g_moe_forward_streamed(hidden, layer_key, src: HostExperts, sh_gate, sh_u
            lib().ds4g_moe_forward_streamed(_ptr(hidden), T, layer_key, C.byref(src.struct), _ptr(sh_gate),
                                            _ptr(sh_up), _ptr(sh_down), _ptr(grid), _ptr(ids), _ptr(w), _ptr(out),
                                            cache.handle, _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def ds4g_expert_file_write(path, src: HostExperts):
+    """Writes the layer's experts of src (host memory) to an expert file."""
+    _check("ds4g_expert_file_write", lib().ds4g_expert_file_write(os.fsencode(path), C.byref(src.struct)))
+
+
+class ExpertFile:
+    """An open expert file (ds4g_expert_file_open) for ds4g_moe_forward_streamed_file."""
+
+    def __init__(self, path):
+        h = C.c_void_p()
+        _check("ds4g_expert_file_open", lib().ds4g_expert_file_open(os.fsencode(path), C.byref(h)))
+        self.handle = h
+
+    def close(self):
+        if self.handle is not None and self.handle.value:
+            _check("ds4g_expert_file_close", lib().ds4g_expert_file_close(self.handle))
+        self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def ds4g_moe_forward_streamed_file(hidden, layer_key, src: ExpertFile, sh_gate, sh_up, sh_down, grid, ids, w, out,
+                                   cache: ExpertCache, workspace, stream=None):
+    """ds4g_moe_forward_streamed with the missing experts read from an expert file."""
+    T = hidden.shape[0]
+    _check("ds4g_moe_forward_streamed_file",
+           lib().ds4g_moe_forward_streamed_file(_ptr(hidden), T, layer_key, src.handle, _ptr(sh_gate), _ptr(sh_up),
+                                                _ptr(sh_down), _ptr(grid), _ptr(ids), _ptr(w), _ptr(out),
+                                                cache.handle, _ptr(workspace), workspace.numel(), _stream(stream)))
 
 
 def ds4g_expert_lru_simulate(n_slots, calls):

@@ -107,6 +107,17 @@ static ds4g_status run_forward(const float *hidden, int T, const ds4g_layer *L, 
     return DS4G_OK;
 }
 
+namespace ds4g {
+ds4g_status forward_streamed_decode(const float *hidden, int T, const ds4g_layer *L, const int32_t *ids,
+                                    const float *w, float *out, void *workspace, size_t ws_bytes, cudaStream_t st,
+                                    const uint32_t *ready, uint32_t epoch) {
+    const ds4g_status chk = check_forward_args(hidden, T, L, ids, w, out, workspace, ws_bytes);
+    if (chk != DS4G_OK) return chk;
+    if (T > kDecodeMaxT) return DS4G_EUNSUPPORTED;
+    return decode_forward(hidden, T, L, ids, w, out, workspace, st, 3, nullptr, ready, epoch);
+}
+}  // namespace ds4g
+
 extern "C" ds4g_status ds4g_moe_forward(const float *hidden, int T, const ds4g_layer *L,
                                         const int32_t *ids, const float *w, float *out,
                                         void *workspace, size_t ws_bytes, ds4g_stream_t s) {

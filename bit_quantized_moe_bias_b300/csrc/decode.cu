@@ -59,7 +59,33 @@ struct DecodeArgs {
     __nv_bfloat16 *hs;    // [T][2][2048]   shared h as bf16 (hi, lo)
     float *part_dr;       // [T][256][8][16]
     float *part_ds;       // [256][8][T][16]
+    const uint32_t *ready; // streamed experts: ready[slot] == epoch once the slot's expert has landed (or NULL)
+    uint32_t epoch;
 };
+
+// Streamed experts (ds4g_moe_forward_streamed): a copy stream writes
+// ready[slot] = epoch after the slot's expert (gate, up, down) has been copied
+// into its cache slot, while this kernel already runs the shared expert.
+// Lane 0 waits for it (bounded: ~1 s, then DS4G_ETIMEOUT) before the warp
+// reads the expert.  The flag follows the expert's copies on that stream, and
+// the expert is read through L2 (no L1 allocation), so the data is there.
+__device__ __forceinline__ void wait_expert(const DecodeArgs &a, int slot) {
+    if (!a.ready) return;
+    if ((threadIdx.x & 31) == 0) {
+        const long long t0 = clock64();
+        while (true) {
+            uint32_t v;
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a.ready + slot) : "memory");
+            if (v == a.epoch) break;
+            if (clock64() - t0 > (2ll << 30)) {
+                flag_status(a.status, DS4G_ETIMEOUT, 0x5700u + (uint32_t)slot);
+                break;
+            }
+            __nanosleep(256);
+        }
+    }
+    __syncwarp();
+}
 
 // ------------------------------------------------------------- task mixing
 // Interleave the two task kinds evenly (Bresenham) so every SM sees the same
@@ -164,6 +190,7 @@ __device__ __forceinline__ void gu_routed_iq2(const DecodeArgs &a, const GUSmem 
     const int rem = (int)(r % (kTilesGU * kSplitR));
     const int tile = rem / kSplitR, split = rem % kSplitR;
     const int e = a.ids[slot];
+    wait_expert(a, slot);
     float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // [matrix][row g / g+8]
     if (expert_ok(e, (const void *const *)a.gate, (const void *const *)a.up, nullptr)) {
         const uint8_t *mat[2] = {a.gate[e], a.up[e]};
@@ -239,6 +266,7 @@ __device__ __forceinline__ void gu_routed_q4k(const DecodeArgs &a, const GUSmem 
     const int rem = (int)(r % (kTilesGU * kSplitR));
     const int tile = rem / kSplitR, split = rem % kSplitR;
     const int e = a.ids[slot];
+    wait_expert(a, slot);
     float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
     if (expert_ok(e, (const void *const *)a.gate, (const void *const *)a.up, nullptr)) {
         const uint8_t *mat[2] = {a.gate[e], a.up[e]};
@@ -434,7 +462,16 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(DecodeArgs a
     const long long W = (long long)gridDim.x * kWarps;
     for (long long tau = blockIdx.x * kWarps + (tid >> 5); tau < NR + NS; tau += W) {
         long long idx;
-        if (task_kind(tau, NR, NS, idx)) gu_shared(a, sm, idx);
+        bool sh;
+        if (a.ready) {
+            // streamed experts: the shared expert's tasks first, while the
+            // routed experts are still being copied
+            sh = tau < NS;
+            idx = sh ? tau : tau - NS;
+        } else {
+            sh = task_kind(tau, NR, NS, idx);
+        }
+        if (sh) gu_shared(a, sm, idx);
         else if (a.gu_type == DS4G_IQ2_XXS) gu_routed_iq2(a, sm, idx);
         else gu_routed_q4k(a, sm, idx);
     }
@@ -720,7 +757,7 @@ static int g_num_sms = 0;
 
 ds4g_status decode_forward(const float *hidden, int T, const ds4g_layer *L, const int32_t *ids,
                            const float *w, float *out, void *workspace, cudaStream_t st, int phases,
-                           uint32_t *status_word) {
+                           uint32_t *status_word, const uint32_t *ready, uint32_t epoch) {
     if (!g_num_sms) {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess) return DS4G_ECUDA;
@@ -755,6 +792,8 @@ ds4g_status decode_forward(const float *hidden, int T, const ds4g_layer *L, cons
     a.hs = (__nv_bfloat16 *)(ws + wl.hs);
     a.part_dr = (float *)(ws + wl.part_dr);
     a.part_ds = (float *)(ws + wl.part_ds);
+    a.ready = ready;
+    a.epoch = epoch;
 
     const size_t ns = (size_t)kK * T;
     const size_t smem_gu = 256 * 16 * 8 + 128 * 16 * 8 + (size_t)T * 2 * kH * 2 * 2;

@@ -87,11 +87,19 @@ struct TraceRange {
 // Decode path of the MoE block (decode.cu, 1 <= T <= 64): workspace bytes,
 // and the launch of its kernels (phases: 1 gate/up, 2 down, 3 both).
 // status_word: where its kernels record a fault (nullptr: the workspace's
-// own header).
+// own header).  ready/epoch (streamed experts): the routed tasks of slot i
+// wait until ready[i] == epoch (written by a copy stream after the slot's
+// expert has landed); nullptr: no waiting.
 size_t decode_workspace(int T);
 ds4g_status decode_forward(const float *hidden, int T, const ds4g_layer *L, const int32_t *ids, const float *w,
                            float *out, void *workspace, cudaStream_t st, int phases,
-                           uint32_t *status_word = nullptr);
+                           uint32_t *status_word = nullptr, const uint32_t *ready = nullptr, uint32_t epoch = 0);
+
+// ds4g_moe_forward's checks, then, for T <= kDecodeMaxT, the decode kernels
+// with the ready flags above; DS4G_EUNSUPPORTED for larger T (api.cu).
+ds4g_status forward_streamed_decode(const float *hidden, int T, const ds4g_layer *L, const int32_t *ids,
+                                    const float *w, float *out, void *workspace, size_t ws_bytes, cudaStream_t st,
+                                    const uint32_t *ready, uint32_t epoch);
 
 // Batched decode path (batch.cu, 4 <= T < 64, IQ2_XXS gate/up and Q2_K
 // down): the batch's slots grouped by expert, each selected expert read once

@@ -384,7 +384,8 @@ ds4g_status ds4g_moe_forward_noalloc(const float *hidden, int T, const ds4g_laye
  * need; a slot is keyed by (layer_key, expert).
  *
  * ds4g_expert_cache_pool_bytes: device bytes of the pool for n_slots slots
- *   of the type pair (the slots plus a 6 KB pointer table); 0 for an
+ *   of the type pair (the slots, a 6 KB pointer table and 256 B of ready
+ *   flags); 0 for an
  *   unsupported pair or n_slots < 1.
  * ds4g_expert_cache_create: pool dev, 16-byte aligned, >= pool_bytes, owned
  *   by the caller and kept alive until destroy.  The cache object and two
@@ -407,10 +408,16 @@ ds4g_status ds4g_moe_forward_noalloc(const float *hidden, int T, const ds4g_laye
  *   layer_key >= 0 names the layer in the cache's keys.
  *   sh_*, iq2_grid (dev), hidden, ids, w, out, workspace as for
  *     ds4g_moe_forward.
- * Steps, on s: copy ids to the host and synchronise s (this also retires the
- * kernels of every earlier call on s, so any slot may be rewritten); give
- * each distinct selected expert its slot, copying those not resident (three
- * cudaMemcpyAsync each); copy the pointer tables; run ds4g_moe_forward.
+ * Steps: copy ids to the host and synchronise s (this also retires the
+ * kernels and copies of every earlier call on the cache, so any slot may be
+ * rewritten); give each distinct selected expert its slot; copy the pointer
+ * tables on s; copy the experts not resident (three cudaMemcpyAsync each).
+ * For T <= 3 the copies run on the cache's own copy stream while the decode
+ * kernels of ds4g_moe_forward already run on s: the shared expert's work
+ * first, and each slot's routed work once a flag, written on the copy stream
+ * after that slot's expert, shows it has landed (a bounded wait; s then
+ * waits for the copies).  For larger T the copies come first on s, then
+ * ds4g_moe_forward.
  * Output bit-identical to ds4g_moe_forward with the same experts resident.
  * Errors: T < 1 or > max_tokens, NULL argument, a selected expert whose host
  * pointer is NULL: DS4G_EINVAL; more distinct experts than n_slots:
@@ -449,6 +456,46 @@ ds4g_status ds4g_moe_forward_streamed(const float *hidden, int T, int layer_key,
                                       void *workspace, size_t ws_bytes, ds4g_stream_t s);
 ds4g_status ds4g_expert_lru_simulate(int n_slots, int n_calls, const int32_t *call_sizes,
                                      const int64_t *keys, int32_t *slot_out, uint8_t *miss_out);
+
+/* ------------------------------------------------------------------------
+ * Expert files: the routed experts of one layer read from storage when they
+ * miss the cache ([P1] §3.5 "SSD streaming"; the yudady DS-4 DwarfStar page,
+ * "SSD Streaming").  File layout (little-endian): a 4096-byte header —
+ * magic "DS4GEXP1", uint32 gate_up_type, uint32 down_type, uint32 256,
+ * uint32 0, uint64 bytes of one packed gate (= up) matrix, uint64 bytes of
+ * one packed down matrix, uint64 record stride, a 32-byte presence bitmap
+ * (bit e % 8 of byte e / 8: expert e stored), zeros — then expert e's packed
+ * gate, up and down (the layout of ds4g_quantize_pack) back to back at byte
+ * 4096 + e * stride; stride = that record's size rounded up to 4096.
+ *
+ * ds4g_expert_file_write: writes src's experts (host pointers; an expert
+ *   whose three pointers are NULL is not stored, and a partial one is
+ *   DS4G_EINVAL) to path, replacing the file.  No CUDA call.  Errors:
+ *   DS4G_EINVAL (NULL argument, partial expert, I/O failure),
+ *   DS4G_EUNSUPPORTED (type pair).
+ * ds4g_expert_file_open: validates the header (magic, types, sizes, stride,
+ *   file length; DS4G_EINVAL before any CUDA call if one is wrong) and
+ *   allocates two pinned staging buffers of one expert each; the handle
+ *   keeps the file open.  ds4g_expert_file_close waits for the staging
+ *   buffers' last copies, frees them and closes the file.
+ * ds4g_moe_forward_streamed_file: ds4g_moe_forward_streamed with the missing
+ *   experts read from the file: each is read (pread) into a staging buffer
+ *   and copied to its slot on s; the read of one expert overlaps the copy
+ *   of the one before (a buffer is reused after its copy's event).  Same
+ *   results, bit for bit, and the same errors; an expert absent from the
+ *   file, or a failed read, is DS4G_EINVAL.  The cache's types must equal
+ *   the file's.  One call at a time per file handle.
+ * ------------------------------------------------------------------------ */
+typedef struct ds4g_expert_file ds4g_expert_file;
+ds4g_status ds4g_expert_file_write(const char *path, const ds4g_host_experts *src);
+ds4g_status ds4g_expert_file_open(const char *path, ds4g_expert_file **file);
+ds4g_status ds4g_expert_file_close(ds4g_expert_file *file);
+ds4g_status ds4g_moe_forward_streamed_file(const float *hidden, int T, int layer_key,
+                                           ds4g_expert_file *file, const uint16_t *sh_gate,
+                                           const uint16_t *sh_up, const uint16_t *sh_down,
+                                           const uint64_t *iq2_grid, const int32_t *ids,
+                                           const float *w, float *out, ds4g_expert_cache *cache,
+                                           void *workspace, size_t ws_bytes, ds4g_stream_t s);
 
 /* RMS norm between chained layers (pages silent; reading: eps = 1e-6, no
  * learned gain): y[t] = x[t] / sqrt(mean_j x[t][j]^2 + 1e-6).  In place

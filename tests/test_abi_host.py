@@ -2,6 +2,7 @@
 header declares, packs/unpacks losslessly into the documented layout, and
 rejects bad arguments before touching the GPU."""
 import ctypes as C
+import os
 
 import numpy as np
 import pytest
@@ -175,3 +176,41 @@ def test_workspace_sizes_grow_with_T():
 def test_status_strings():
     assert B.ds4g_status_str(0) == "ok"
     assert "bad data" in B.ds4g_status_str(7)
+
+
+def test_expert_file_layout_and_header_checks(tmp_path):
+    """ds4g_expert_file_write stores the documented layout (no GPU needed);
+    ds4g_expert_file_open refuses a bad header before any CUDA call."""
+    import struct
+    gate = {3: np.arange(B.ds4g_packed_size(0, 2048, 4096), dtype=np.uint64).astype(np.uint8)}
+    up = {3: np.full(B.ds4g_packed_size(0, 2048, 4096), 7, np.uint8)}
+    down = {3: np.full(B.ds4g_packed_size(1, 4096, 2048), 9, np.uint8)}
+    src = B.HostExperts(gate, up, down, 0, 1)
+    path = tmp_path / "e.ds4gexp"
+    B.ds4g_expert_file_write(path, src)
+    raw = path.read_bytes()
+    magic, gut, dt, n, zero, gb, db, stride = struct.unpack_from("<8sIIIIQQQ", raw, 0)
+    assert (magic, gut, dt, n, zero) == (b"DS4GEXP1", 0, 1, 256, 0)
+    assert gb == B.ds4g_packed_size(0, 2048, 4096) and db == B.ds4g_packed_size(1, 4096, 2048)
+    assert stride % 4096 == 0 and stride >= 2 * gb + db
+    bitmap = raw[48:80]
+    assert bitmap[0] == 1 << 3 and not any(bitmap[1:])
+    assert len(raw) == 4096 + 256 * stride
+    base = 4096 + 3 * stride
+    assert raw[base:base + gb] == gate[3].tobytes()
+    assert raw[base + gb:base + 2 * gb] == up[3].tobytes()
+    assert raw[base + 2 * gb:base + 2 * gb + db] == down[3].tobytes()
+    # a partial expert is refused
+    with pytest.raises(B.DS4GError) as e:
+        B.ds4g_expert_file_write(tmp_path / "p.ds4gexp", B.HostExperts(gate, up, {}, 0, 1))
+    assert e.value.code == 1
+    # headers that open must refuse before any CUDA call
+    L = B.lib()
+    h = C.c_void_p()
+    bad = bytearray(raw[:4096])
+    bad[0:8] = b"XXXXXXXX"
+    (tmp_path / "bad.ds4gexp").write_bytes(bytes(bad))
+    assert L.ds4g_expert_file_open(os.fsencode(tmp_path / "bad.ds4gexp"), C.byref(h)) == 1
+    (tmp_path / "short.ds4gexp").write_bytes(raw[:4096 + stride])   # truncated
+    assert L.ds4g_expert_file_open(os.fsencode(tmp_path / "short.ds4gexp"), C.byref(h)) == 1
+    assert L.ds4g_expert_file_open(os.fsencode(tmp_path / "none.ds4gexp"), C.byref(h)) == 1

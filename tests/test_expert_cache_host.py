@@ -115,7 +115,8 @@ def test_host_checks_before_any_cuda_call():
     assert L.ds4g_expert_cache_pool_bytes(0, 1, 0) == 0
     q2 = L.ds4g_expert_cache_pool_bytes(0, 1, 8)
     q4 = L.ds4g_expert_cache_pool_bytes(2, 2, 8)
-    assert q2 == 8 * (2 * 2162688 + 2752512) + 6144 and q4 == 8 * 3 * 4718592 + 6144
+    # slots, the [3][256] pointer table (6 KB) and 256 B of ready flags
+    assert q2 == 8 * (2 * 2162688 + 2752512) + 6144 + 256 and q4 == 8 * 3 * 4718592 + 6144 + 256
     import ctypes as C
     h = C.c_void_p()
     fake = 0x10000000

@@ -110,3 +110,55 @@ def test_streamed_refusals_and_recovery():
     B.ds4g_moe_forward_streamed(xd, lay, src, sg, su, sd, gr, bad, wd, out, cache, ws)
     assert B.ds4g_last_error(ws) == 7
     cache.close()
+
+
+@pytest.mark.parametrize("gut,dt", [(synth.IQ2_XXS, synth.Q2_K), (synth.Q4_K, synth.Q4_K)])
+def test_streamed_from_file_equals_host_and_resident(gut, dt, tmp_path):
+    """Experts read from an expert file (pread into pinned staging, then
+    copied): bit-identical to the host-memory source and to the resident
+    forward, the same hit/miss counts, and an expert absent from the file is
+    refused."""
+    seed, cfg, lay = 7, 1, 1
+    experts = [1, 2, 5, 8, 13, 21, 34, 55, 89, 144]
+    L, hx, shared, grid = device_layer(seed, cfg, lay, experts, gut, dt)
+    src = _host_experts(hx, experts, gut, dt)
+    path = tmp_path / "layer1.ds4gexp"
+    B.ds4g_expert_file_write(path, src)
+    f = B.ExpertFile(path)
+    cache_f = B.ExpertCache(10, max_tokens=2, gate_up_type=gut, down_type=dt)
+    cache_h = B.ExpertCache(10, max_tokens=2, gate_up_type=gut, down_type=dt)
+    ws = B.workspace(B.ds4g_forward_workspace(2))
+    sg, su, sd, gridt = L.tensors[3], L.tensors[4], L.tensors[5], L.tensors[6]
+    rng = np.random.default_rng(5)
+    # 10 slots: the last call needs all ten experts, so each earlier miss is evicted at most once
+    calls = [[[1, 2, 5, 8, 13, 21]], [[34, 55, 89, 144, 1, 2]], [[5, 8, 13, 21, 34, 55], [89, 144, 1, 2, 5, 8]],
+             [[21, 34, 55, 89, 144, 13]]]
+    for i, c in enumerate(calls):
+        ids = np.array(c, np.int32)
+        T = ids.shape[0]
+        x = synth.hidden(seed, cfg, T, layer=70 + i)
+        w = rng.dirichlet(np.ones(K), T).astype(np.float32)
+        xd, idd, wd = (torch.from_numpy(np.ascontiguousarray(a)).to(DEV) for a in (x, ids, w))
+        outs = []
+        for mode in ("file", "host", "resident"):
+            o = torch.full((T, H), float("nan"), device=DEV)
+            if mode == "file":
+                B.ds4g_moe_forward_streamed_file(xd, lay, f, sg, su, sd, gridt, idd, wd, o, cache_f, ws)
+            elif mode == "host":
+                B.ds4g_moe_forward_streamed(xd, lay, src, sg, su, sd, gridt, idd, wd, o, cache_h, ws)
+            else:
+                B.ds4g_moe_forward(xd, L.struct, idd, wd, o, ws)
+            assert B.ds4g_last_error(ws) == 0
+            outs.append(o.cpu().numpy())
+        assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+    assert cache_f.stats() == cache_h.stats()
+    ids = np.array([[1, 2, 3, 5, 8, 13]], np.int32)       # expert 3 is not in the file
+    idd = torch.from_numpy(ids).to(DEV)
+    o = torch.empty(1, H, device=DEV)
+    with pytest.raises(B.DS4GError) as e:
+        B.ds4g_moe_forward_streamed_file(torch.zeros(1, H, device=DEV), lay, f, sg, su, sd, gridt, idd,
+                                         torch.full((1, K), 1.0 / K, device=DEV), o, cache_f, ws)
+    assert e.value.code == 1
+    f.close()
+    cache_f.close()
+    cache_h.close()
