@@ -24,7 +24,7 @@
 //               shared expert, its bf16 weight tiles
 //   warp 1      TMEM owner and MMA issuer (tcgen05.mma, M = 128, N <= 128)
 //   warps 2-5   epilogue (TMEM -> registers -> global)
-//   warps 6-13  dequantisers: packed IQ2_XXS / Q2_K / Q4_K tile-blocks are
+//   warps 6-21  dequantisers: packed IQ2_XXS / Q2_K / Q4_K tile-blocks are
 //               read straight from HBM into registers (one block column
 //               prefetched ahead) and written as bf16 into the 128-byte
 //               swizzled shared-memory layout the tensor core reads.
@@ -55,7 +55,7 @@ constexpr int kNC = 128;        // bucket rows per task (MMA N <= 128)
 constexpr int kStages = 3;
 constexpr int kTile = kBM * kBK * 2;   // 16 KB: A tile, and the largest B tile
 constexpr int kStageBytes = 3 * kTile; // A0, A1, B
-constexpr int kDqWarps = 8;
+constexpr int kDqWarps = 16;   // two threads per weight row and matrix: each takes half of a stage's columns
 constexpr int kPFThreads = (6 + kDqWarps) * 32;
 constexpr int kGroups = kE + 1;        // routed experts + shared expert
 
@@ -233,39 +233,45 @@ __device__ __forceinline__ void sts128(uint8_t *tile, int m, int chunk, uint4 v)
     *reinterpret_cast<uint4 *>(tile + m * 128 + ((chunk ^ (m & 7)) << 4)) = v;
 }
 
-// One dequantiser thread's packed data for one 256-column block column.
+// One dequantiser thread's packed data for one 256-column block column: the
+// half of its row segment that its parity `par` of the stage's columns needs.
+//   IQ2_XXS (phase 1): the 8-byte records j = 2 ks + par (ks = 0..3): the
+//     row's 16-byte words par and 2 + par;
+//   Q4_K: the 32-column sub-blocks j = 2 ks + h (h = par in phase 1, the
+//     k-half in phase 2): the row's 16-byte words 2h, 2h + 1, 4 + 2h, 5 + 2h,
+//     plus the 12 scale bytes;
+//   Q2_K (phase 2): the 32-bit words par * 4 .. + 3 of the row's k-half and
+//     their scale word.
 struct BlockRegs {
-    uint4 q[8];
+    uint4 q[4];
     uint32_t s[3];
     uint32_t dd;
 };
 
-// Load the packed bytes of row `r` (global row of the matrix) in block
-// column kb that thread half `kh` (phase 2) or the whole row (phase 1) needs.
-__device__ __forceinline__ void load_block(const PFArgs &a, const uint8_t *mat, int r, int kb, int kh,
+__device__ __forceinline__ void load_block(const PFArgs &a, const uint8_t *mat, int r, int kb, int kh, int par,
                                            BlockRegs &R) {
     const int nbc = a.Kdim / 256;
     const int rr = r & 15, g8 = rr & 7, hrow = rr >> 3;
     if (a.qt == DS4G_IQ2_XXS) {
         const uint8_t *tb = mat + ((size_t)(r >> 4) * nbc + kb) * kTB_IQ2;
         const uint8_t *row = tb + 512 * hrow + 64 * g8;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) R.q[i] = ldg_nc128(row + 16 * i);
+        R.q[0] = ldg_nc128(row + 16 * par);
+        R.q[1] = ldg_nc128(row + 16 * (2 + par));
         R.dd = ldg_nc32(tb + 1024 + 4 * g8) >> (16 * hrow);
     } else if (a.qt == DS4G_Q2_K) {
         const uint8_t *tb = mat + ((size_t)(r >> 4) * nbc + kb) * kTB_Q2K;
         const uint8_t *row = tb + 512 * hrow + 64 * g8 + 32 * kh;
-        R.q[0] = ldg_nc128(row);
-        R.q[1] = ldg_nc128(row + 16);
-        const uint2 sc = ldg_nc64(tb + 1024 + 128 * hrow + 16 * g8 + 8 * kh);
-        R.s[0] = sc.x;
-        R.s[1] = sc.y;
+        R.q[0] = ldg_nc128(row + 16 * par);
+        R.s[0] = ldg_nc32(tb + 1024 + 128 * hrow + 16 * g8 + 8 * kh + 4 * par);
         R.dd = ldg_nc32(tb + 1280 + 8 * g8 + 4 * hrow);
     } else {  // Q4_K
+        const int h = a.phase == 1 ? par : kh;
         const uint8_t *tb = mat + ((size_t)(r >> 4) * nbc + kb) * kTB_Q4K;
         const uint8_t *row = tb + 1024 * hrow + 128 * g8;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) R.q[i] = ldg_nc128(row + 16 * i);
+        R.q[0] = ldg_nc128(row + 16 * (2 * h));
+        R.q[1] = ldg_nc128(row + 16 * (2 * h + 1));
+        R.q[2] = ldg_nc128(row + 16 * (4 + 2 * h));
+        R.q[3] = ldg_nc128(row + 16 * (5 + 2 * h));
         const uint8_t *sc = tb + 2048 + 12 * rr;
         R.s[0] = ldg_nc32(sc);
         R.s[1] = ldg_nc32(sc + 4);
@@ -292,12 +298,14 @@ __device__ __forceinline__ uint32_t word_of(const BlockRegs &R, int i) {
     const int k = i & 3;
     return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
 }
+__device__ __forceinline__ uint32_t word4(uint4 v, int k) { return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w; }
 
-// IQ2_XXS: 32 weights of sub-block j (record of the row's 64 bytes) -> 4 chunks.
-__device__ __forceinline__ void dq_iq2_record(const PFSmem &sm, const BlockRegs &R, int j, uint8_t *tile, int m,
-                                              int chunk0, int rep8) {
-    const int wi = 4 * (j & 3) + 2 * (j >> 2);
-    const uint32_t ia = word_of(R, wi), v = word_of(R, wi + 1);
+// IQ2_XXS: 32 weights of record j (8 bytes of the row; qw = the 16-byte word of the row that holds it) -> 4 chunks.
+__device__ __forceinline__ void dq_iq2_record(const PFSmem &sm, const BlockRegs &R, uint4 qw, int j, uint8_t *tile,
+                                              int m, int chunk0, int rep8) {
+    // record j sits in the row's 16-byte word j & 3, 32-bit words 2 (j >> 2), +1;
+    // qw is that 16-byte word
+    const uint32_t ia = word4(qw, 2 * (j >> 2)), v = word4(qw, 2 * (j >> 2) + 1);
     const float d = f16lo(R.dd);
     const float db = __fmul_rn(__fmul_rn(d, __fadd_rn(0.5f, (float)(v >> 28))), 0.25f);
     uint32_t rlo, rhi;
@@ -332,9 +340,10 @@ __device__ __forceinline__ void dq_q2k_sub(const PFSmem &sm, uint32_t W, uint32_
            make_uint4(prmt(rlo, rhi, s2.x), prmt(rlo, rhi, s2.y), prmt(rlo, rhi, s3.x), prmt(rlo, rhi, s3.y)));
 }
 
-// Q4_K: 32 weights of sub-block j -> 4 chunks (natural order), fp32 formula.
+// Q4_K: weights of sub-block j, 8-column chunks cq0 .. cq0 + ncq - 1 of its 4
+// (natural order) -> tile chunks chunk0 + cq, fp32 formula.
 __device__ __forceinline__ void dq_q4k_sub(bool f16, const BlockRegs &R, int j, uint4 qv, uint8_t *tile, int m,
-                                           int chunk0) {
+                                           int chunk0, int cq0 = 0, int ncq = 4) {
     const uint32_t s0 = (R.s[0] >> (8 * (j & 3))) & 0xffu;
     const uint32_t s1 = (R.s[1] >> (8 * (j & 3))) & 0xffu;
     const uint32_t s2 = (R.s[2] >> (8 * (j & 3))) & 0xffu;
@@ -351,6 +360,7 @@ __device__ __forceinline__ void dq_q4k_sub(bool f16, const BlockRegs &R, int j, 
     const uint32_t words[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
     for (int cq = 0; cq < 4; ++cq) {  // chunk cq = columns 8cq .. 8cq+7 = c in {2cq, 2cq+1}
+        if (cq < cq0 || cq >= cq0 + ncq) continue;
         uint32_t o[4];
 #pragma unroll
         for (int pr = 0; pr < 4; ++pr) {  // pair pr: columns 8cq + 2pr, +1
@@ -613,9 +623,10 @@ __global__ void __launch_bounds__(kPFThreads, 1)
         }
     } else {
         // ---------------------------------------------------- dequantisers
-        const int dq = tid - 6 * 32;           // 0..255
+        const int dq = tid - 6 * 32;           // 0..511
         const int m = dq & 127;
-        const int half = dq >> 7;              // phase 1: matrix; phase 2: k-half
+        const int half = (dq >> 7) & 1;        // phase 1: matrix; phase 2: k-half
+        const int par = dq >> 8;               // which half of the stage's work of (m, half)
         const int nblk = a.Kdim / 256;
         uint32_t it = 0;
         BlockRegs cur, nxt;
@@ -626,7 +637,7 @@ __global__ void __launch_bounds__(kPFThreads, 1)
             t = decode_task(a, sm.tp, tau);
             if (!t.shared) {
                 const uint8_t *mat = (a.phase == 1 && half) ? a.A1[t.g] : a.A0[t.g];
-                load_block(a, mat, t.mt * kBM + m, 0, half, cur);
+                load_block(a, mat, t.mt * kBM + m, 0, half, par, cur);
             }
         }
         for (; tau < ntask && !*abort_flag; tau += gridDim.x) {
@@ -641,12 +652,12 @@ __global__ void __launch_bounds__(kPFThreads, 1)
                 // prefetch the next block column (possibly of the next task)
                 if (kb + 1 < nblk) {
                     if (!t.shared) {
-                        load_block(a, mat, r, kb + 1, half, nxt);
+                        load_block(a, mat, r, kb + 1, half, par, nxt);
                         prefetch_block(a, mat, r, kb + 2, half);
                     }
                 } else if (taun < ntask && !tn.shared) {
                     const uint8_t *matn = (a.phase == 1 && half) ? a.A1[tn.g] : a.A0[tn.g];
-                    load_block(a, matn, tn.mt * kBM + m, 0, half, nxt);
+                    load_block(a, matn, tn.mt * kBM + m, 0, half, par, nxt);
                 }
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
@@ -662,25 +673,26 @@ __global__ void __launch_bounds__(kPFThreads, 1)
                         uint8_t *st = sm.stage + (size_t)s * kStageBytes;
                         if (a.phase == 1) {
                             uint8_t *tile = st + half * kTile;
+                            // record / sub-block 2 ks + par -> chunks 4 par .. 4 par + 3
+                            const int j = 2 * ks + par;
                             if (a.qt == DS4G_IQ2_XXS) {
-                                dq_iq2_record(sm, cur, 2 * ks, tile, m, 0, lane & 7);
-                                dq_iq2_record(sm, cur, 2 * ks + 1, tile, m, 4, lane & 7);
+                                // the row's 16-byte word j & 3 = 2 (ks & 1) + par is held as cur.q[ks & 1]
+                                dq_iq2_record(sm, cur, cur.q[ks & 1], j, tile, m, 4 * par, lane & 7);
                             } else {
-                                dq_q4k_sub(true, cur, 2 * ks, cur.q[2 * ((2 * ks) & 3) + ((2 * ks) >> 2)], tile, m, 0);
-                                dq_q4k_sub(true, cur, 2 * ks + 1, cur.q[2 * ((2 * ks + 1) & 3) + ((2 * ks + 1) >> 2)],
-                                           tile, m, 4);
+                                // sub-block j = row word 2 (j & 3) + (j >> 2), held as cur.q[2 (ks & 1) + (ks >> 1)]
+                                dq_q4k_sub(true, cur, j, cur.q[2 * (ks & 1) + (ks >> 1)], tile, m, 4 * par);
                             }
                         } else {
                             if (a.qt == DS4G_Q2_K) {
+                                // word ks of this thread's 4 (row word 4 par + ks) -> chunks 4 half + 2 par, + 1
                                 const float d = f16lo(cur.dd), dmin = f16hi(cur.dd);
-                                const uint32_t sc0 = cur.s[0] >> (8 * ks), sc1 = cur.s[1] >> (8 * ks);
-                                dq_q2k_sub(sm, word_of(cur, ks), sc0 & 255u, d, dmin, st, m, 4 * half, lane & 15);
-                                dq_q2k_sub(sm, word_of(cur, 4 + ks), sc1 & 255u, d, dmin, st, m, 4 * half + 2,
-                                           lane & 15);
+                                dq_q2k_sub(sm, word_of(cur, ks), (cur.s[0] >> (8 * ks)) & 255u, d, dmin, st, m,
+                                           4 * half + 2 * par, lane & 15);
                             } else {
-                                const int j0 = 2 * ks, j1 = 2 * ks + 1;
-                                const uint4 q0 = cur.q[2 * (j0 & 3) + (j0 >> 2)], q1 = cur.q[2 * (j1 & 3) + (j1 >> 2)];
-                                dq_q4k_sub(true, cur, half ? j1 : j0, half ? q1 : q0, st, m, 4 * half);
+                                // sub-block j = 2 ks + half, chunks 2 par, 2 par + 1 of its 4
+                                const int j = 2 * ks + half;
+                                dq_q4k_sub(true, cur, j, cur.q[2 * (ks & 1) + (ks >> 1)], st, m, 4 * half, 2 * par,
+                                           2);
                             }
                         }
                         tc::fence_proxy_async_smem();
