@@ -46,6 +46,9 @@ LAYER_BYTES_Q4 = ROUTED_BYTES_Q4 + SHARED_BYTES + ROUTER_BYTES + ACT_BYTES
 # gate/up launch (dominant kernel): routed gate+up + shared gate+up + x
 GATEUP_BYTES = 6 * 2 * 2162688 + 2 * F * H * 2 + H * 4
 METRIC = "routed-MoE tokens/s (decode, prefill) and achieved HBM GB/s vs B300 peak"
+# decode arithmetic: exact quant codes on fp16 tensor cores against the activation as an fp16 hi + lo
+# pair, fp32 scales and accumulation; the shared expert's bf16 weights against a bf16 hi + lo pair
+DECODE_DTYPE = "fp16x2-split activations x exact codes -> f32 (shared expert bf16x2-split)"
 WORKLOAD = ("config1 full-depth decode: 43 MoE layers x 256 experts (IQ2_XXS gate/up, Q2_K down, "
             "bf16 shared, fp32 router), 1 token at a time, 64 tokens per step")
 WORKLOAD_Q2Q4 = ("q2-q4 full-depth decode: 43 MoE layers x 256 experts, layers 0-36 IQ2_XXS gate/up + Q2_K "
@@ -330,7 +333,7 @@ def run_ours(args, rank, world, local_rank):
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dev_s / args.steps * 1e3, 3), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": DECODE_DTYPE, "data": "synthetic",
         "config": {"workload": workload, "layers": nl, "q4_layers": q4, "tokens_per_step": ntok, "global_batch": 1,
                    "seq_len": 1, "parallelism": "replicas" if world > 1 else "single",
                    "l2": f"no flush: each token streams {token_bytes / 1e9:.2f} GB of weights >> 126 MB L2",
@@ -469,7 +472,7 @@ def run_stream(args, rank, world, local_rank):
     line = {
         "metric": METRIC, "value": round(tokens / dev_s, 3), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dev_s / args.steps * 1e3, 3),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DECODE_DTYPE, "data": "synthetic",
         "config": {"workload": ST_WORKLOAD.format(nl=nl, slots=slots, ntok=ntok).replace(
                        "in pinned host memory", "in pinned host memory" if args.stream_source == "host"
                        else "in expert files (read with pread on a miss)"), "layers": nl,
