@@ -242,7 +242,14 @@ def run_ours(args, rank, world, local_rank):
                     continue
                 B.ds4g_rmsnorm(cur, xn)
                 B.ds4g_moe_route(xn, R, b, ids, w, rws)
-                if timing is not None and i < timing[2]:
+                if args.decode_path == "q8":
+                    # int8 activations for the routed gate/up (timed: the whole forward)
+                    if timing is not None and i < timing[2]:
+                        timing[0][l + nl * i].record()
+                    B.ds4g_moe_forward_q8(xn, L.struct, ids, w, dst, fws)
+                    if timing is not None and i < timing[2]:
+                        timing[1][l + nl * i].record()
+                elif timing is not None and i < timing[2]:
                     timing[0][l + nl * i].record()
                     B.ds4g_moe_gate_up(xn, L.struct, ids, w, dst, fws)
                     timing[1][l + nl * i].record()
@@ -321,6 +328,9 @@ def run_ours(args, rank, world, local_rank):
     hbm, kind = peaks()
     kbytes = LAYER_BYTES if fused else GATEUP_BYTES
     kname = "decode_t1_kernel (whole layer)" if fused else "gateup_decode_kernel"
+    if args.decode_path == "q8":
+        kbytes = ROUTED_BYTES + SHARED_BYTES + ACT_BYTES
+        kname = "ds4g_moe_forward_q8 (gate/up with int8 activations + down; per-slot kernels)"
     token_bytes = (nl - q4) * LAYER_BYTES + q4 * LAYER_BYTES_Q4
     workload = WORKLOAD
     if q4:
@@ -345,8 +355,8 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1),
                      "peak": hbm, "peak_kind": kind, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                      "bytes_per_launch": kbytes, "launch_us": round(gu_us, 3),
-                     "traffic": None if q4 else traffic_record("decode_t1_kernel" if fused else
-                                                               "gateup_decode_kernel")},
+                     "traffic": None if q4 or args.decode_path == "q8" else traffic_record(
+                         "decode_t1_kernel" if fused else "gateup_decode_kernel")},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
@@ -594,7 +604,7 @@ def run_prefill(args, rank, world, local_rank):
         "roofline": {"bound": "tensor", "kernel": "prefill_gemm_kernel (gate/up phase, incl. bucket + permute)",
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": kind, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "flop_per_launch": PF_GATEUP_FLOP,
-                     "launch_us": round(gu_us, 2), "traffic": None},
+                     "launch_us": round(gu_us, 2), "traffic": traffic_record("prefill_gemm_kernel")},
         "gpu_launches": 6 * args.steps,   # route, bucket, permute, 2 x gemm, combine
         "clocks": clk.summary(),
     }
@@ -1040,7 +1050,7 @@ def main():
     ap.add_argument("--model", choices=["q2", "q2-q4", "q4"], default="q2",
                     help="decode model: q2 = every layer IQ2_XXS/Q2_K (headline); q2-q4 = last 6 layers Q4_K; "
                          "q4 = every layer Q4_K")
-    ap.add_argument("--decode-path", choices=["fused", "layer", "split"], default="fused",
+    ap.add_argument("--decode-path", choices=["fused", "layer", "split", "q8"], default="fused",
                     help="fused = one stack call per token (one launch per layer, programmatic dependent "
                          "launches); layer = one call per layer; split = rmsnorm, route, gate/up, down launches")
     args = ap.parse_args()

@@ -68,6 +68,7 @@ def lib():
             "ds4g_moe_bucket": ([vp, i, vp, vp, vp, vp, vp, sz, vp], i),
             "ds4g_forward_workspace": ([i], sz),
             "ds4g_moe_forward": (fwd, i),
+            "ds4g_moe_forward_q8": (fwd, i),
             "ds4g_moe_gate_up": (fwd, i),
             "ds4g_moe_down": (fwd, i),
             "ds4g_layer_decode_workspace": ([], sz),
@@ -204,6 +205,11 @@ def _fwd(name, hidden, layer, ids, w, out, workspace, stream):
 
 def ds4g_moe_forward(hidden, layer: ds4g_layer, ids, w, out, workspace, stream=None):
     _fwd("ds4g_moe_forward", hidden, layer, ids, w, out, workspace, stream)
+
+
+def ds4g_moe_forward_q8(hidden, layer: ds4g_layer, ids, w, out, workspace, stream=None):
+    """ds4g_moe_forward (T <= 3) with the routed IQ2_XXS gate/up on int8 activations."""
+    _fwd("ds4g_moe_forward_q8", hidden, layer, ids, w, out, workspace, stream)
 
 
 def ds4g_moe_gate_up(hidden, layer: ds4g_layer, ids, w, out, workspace, stream=None):

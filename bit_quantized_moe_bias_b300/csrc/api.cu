@@ -125,6 +125,16 @@ extern "C" ds4g_status ds4g_moe_forward(const float *hidden, int T, const ds4g_l
     return run_forward(hidden, T, L, ids, w, out, workspace, ws_bytes, s, 3);
 }
 
+extern "C" ds4g_status ds4g_moe_forward_q8(const float *hidden, int T, const ds4g_layer *L,
+                                           const int32_t *ids, const float *w, float *out,
+                                           void *workspace, size_t ws_bytes, ds4g_stream_t s) {
+    DS4G_TRACE();
+    const ds4g_status chk = check_forward_args(hidden, T, L, ids, w, out, workspace, ws_bytes);
+    if (chk != DS4G_OK) return chk;
+    if (T > kDecodeMaxT || L->gate_up_type != DS4G_IQ2_XXS) return DS4G_EUNSUPPORTED;
+    return decode_forward(hidden, T, L, ids, w, out, workspace, (cudaStream_t)s, 3, nullptr, nullptr, 0, 1);
+}
+
 extern "C" ds4g_status ds4g_moe_gate_up(const float *hidden, int T, const ds4g_layer *L,
                                         const int32_t *ids, const float *w, float *out,
                                         void *workspace, size_t ws_bytes, ds4g_stream_t s) {

@@ -61,6 +61,7 @@ struct DecodeArgs {
     float *part_ds;       // [256][8][T][16]
     const uint32_t *ready; // streamed experts: ready[slot] == epoch once the slot's expert has landed (or NULL)
     uint32_t epoch;
+    int q8;               // routed IQ2_XXS gate/up on int8 activations (dp4a)
 };
 
 // Streamed experts (ds4g_moe_forward_streamed): a copy stream writes
@@ -124,6 +125,10 @@ struct GUSmem {
     uint2 *stab;  // [128][16] sign bytes (0x80 / 0x00) of each 7-bit sign index
     __half *xq;   // [T][2][4096] activation fp16 (hi, lo)
     __nv_bfloat16 *xb;  // [T][2][4096] activation bf16 (hi, lo)
+    // q8 only:
+    uint4 *stab8;  // [128][16] per sign index: 0xFF / 0x00 masks (bytes 0-3, 4-7), then 0x01 / 0x00
+    int8_t *x8;    // [T][4096] activation as int8 (blocks of 256)
+    float *dx;     // [T][16] the blocks' scales
 };
 
 // Reduction of one (slot, tile) of routed gate/up: 8 split partials in fixed
@@ -250,6 +255,82 @@ __device__ __forceinline__ void gu_routed_iq2(const DecodeArgs &a, const GUSmem 
                     }
                     acc[m][0] = fmaf(d4g * half_plus(va >> 28), c[0] + c[1], acc[m][0]);
                     acc[m][1] = fmaf(d4h * half_plus(vb >> 28), c[2] + c[3], acc[m][1]);
+                }
+            }
+        }
+    } else if (lane == 0) {
+        flag_status(a.status, DS4G_EDEVICE, (uint32_t)e);
+    }
+    gu_write_partial(a, slot, tile, split, acc);
+}
+
+// IQ2_XXS gate/up on int8 activations (the int8 path: chenxutan ds4 article
+// §2.4, dot_iq2_pair_16: int8 grid values against int8 activations).  x is
+// held as q8 (blocks of 256: q = x / d to nearest, ties to even, d =
+// max|x| / 127).  Lane (g, t) owns sub-blocks 4jj + t of rows g and g + 8 (the
+// packed layout's ownership) and forms each sub-block's exact integer sum
+// S = sum (sign * grid value) * q with dp4a: a negative byte is taken as
+// (g ^ 0xFF) = -g - 1 and the +1 is added back by a dp4a of the 0x01 mask.
+// Then acc += (d (0.5 + ls) 0.25) * d_x * S in fp32.
+__device__ __forceinline__ void gu_routed_iq2_q8(const DecodeArgs &a, const GUSmem &sm, long long r) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3, p = lane & 15;
+    const int slot = (int)(r / (kTilesGU * kSplitR));
+    const int rem = (int)(r % (kTilesGU * kSplitR));
+    const int tile = rem / kSplitR, split = rem % kSplitR;
+    const int e = a.ids[slot];
+    wait_expert(a, slot);
+    float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+    if (expert_ok(e, (const void *const *)a.gate, (const void *const *)a.up, nullptr)) {
+        const uint8_t *mat[2] = {a.gate[e], a.up[e]};
+        uint4 qa[2][2], qb[2][2];
+        uint32_t dd[2][2];
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int s2 = 0; s2 < 2; ++s2) {
+                const uint8_t *tb = mat[m] + ((size_t)tile * 16 + 2 * split + s2) * kTB_IQ2;
+                qa[m][s2] = ldg_stream128(tb + 16 * lane);
+                qb[m][s2] = ldg_stream128(tb + 512 + 16 * lane);
+                dd[m][s2] = ldg_stream32(tb + 1024 + 4 * g);
+            }
+        const int tok = slot / kK;
+#pragma unroll
+        for (int s2 = 0; s2 < 2; ++s2) {
+            const int b = 2 * split + s2;
+            const float dxb = sm.dx[tok * 16 + b];
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                const int j = 4 * jj + t;
+                const uint4 *xs = reinterpret_cast<const uint4 *>(sm.x8 + (size_t)tok * kH + 256 * b + 32 * j);
+                const uint4 x0 = xs[0], x1 = xs[1];
+                const int xw[8] = {(int)x0.x, (int)x0.y, (int)x0.z, (int)x0.w,
+                                   (int)x1.x, (int)x1.y, (int)x1.z, (int)x1.w};
+#pragma unroll
+                for (int m = 0; m < 2; ++m) {
+                    const uint32_t ia = jj ? qa[m][s2].z : qa[m][s2].x, va = jj ? qa[m][s2].w : qa[m][s2].y;
+                    const uint32_t ib = jj ? qb[m][s2].z : qb[m][s2].x, vb = jj ? qb[m][s2].w : qb[m][s2].y;
+                    int Sa = 0, Sb = 0;
+#pragma unroll
+                    for (int l = 0; l < 4; ++l) {
+                        const uint2 ga = sm.gtab[((ia >> (8 * l)) & 255u) * 16 + p];
+                        const uint4 sa = sm.stab8[((va >> (7 * l)) & 127u) * 16 + p];
+                        const uint2 gb = sm.gtab[((ib >> (8 * l)) & 255u) * 16 + p];
+                        const uint4 sb = sm.stab8[((vb >> (7 * l)) & 127u) * 16 + p];
+                        Sa = __dp4a((int)(ga.x ^ sa.x), xw[2 * l], Sa);
+                        Sa = __dp4a((int)(ga.y ^ sa.y), xw[2 * l + 1], Sa);
+                        Sa = __dp4a((int)sa.z, xw[2 * l], Sa);
+                        Sa = __dp4a((int)sa.w, xw[2 * l + 1], Sa);
+                        Sb = __dp4a((int)(gb.x ^ sb.x), xw[2 * l], Sb);
+                        Sb = __dp4a((int)(gb.y ^ sb.y), xw[2 * l + 1], Sb);
+                        Sb = __dp4a((int)sb.z, xw[2 * l], Sb);
+                        Sb = __dp4a((int)sb.w, xw[2 * l + 1], Sb);
+                    }
+                    const float dga = __half2float(__ushort_as_half((unsigned short)(dd[m][s2] & 0xffffu)));
+                    const float dgb = __half2float(__ushort_as_half((unsigned short)(dd[m][s2] >> 16)));
+                    const float dba = __fmul_rn(__fmul_rn(dga, half_plus(va >> 28)), 0.25f);
+                    const float dbb = __fmul_rn(__fmul_rn(dgb, half_plus(vb >> 28)), 0.25f);
+                    acc[m][0] = fmaf(dba * dxb, (float)Sa, acc[m][0]);
+                    acc[m][1] = fmaf(dbb * dxb, (float)Sb, acc[m][1]);
                 }
             }
         }
@@ -425,6 +506,9 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(DecodeArgs a
     sm.stab = sm.gtab + 256 * 16;
     sm.xq = reinterpret_cast<__half *>(sm.stab + 128 * 16);
     sm.xb = reinterpret_cast<__nv_bfloat16 *>(sm.xq + (size_t)a.T * 2 * kH);
+    sm.stab8 = reinterpret_cast<uint4 *>(sm.xb + (size_t)a.T * 2 * kH);
+    sm.x8 = reinterpret_cast<int8_t *>(sm.stab8 + 128 * 16);
+    sm.dx = reinterpret_cast<float *>(sm.x8 + (size_t)a.T * kH);
     const int tid = threadIdx.x;
     if (a.gu_type == DS4G_IQ2_XXS) {
         for (int i = tid; i < 256 * 16; i += kThreads) {
@@ -441,6 +525,42 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(DecodeArgs a
                 hi |= ((sg >> (j + 4)) & 1u) << (8 * j + 7);
             }
             sm.stab[i] = make_uint2(lo, hi);
+            if (a.q8) {
+                uint32_t mlo = 0, mhi = 0, olo = 0, ohi = 0;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    mlo |= ((sg >> j) & 1u) * (0xFFu << (8 * j));
+                    mhi |= ((sg >> (j + 4)) & 1u) * (0xFFu << (8 * j));
+                    olo |= ((sg >> j) & 1u) << (8 * j);
+                    ohi |= ((sg >> (j + 4)) & 1u) << (8 * j);
+                }
+                sm.stab8[i] = make_uint4(mlo, mhi, olo, ohi);
+            }
+        }
+    }
+    if (a.q8) {
+        // q8 activations: per token and 256-column block, d = max|x| / 127,
+        // q = x / d to nearest (ties to even), clamped to +-127; one warp per block
+        const int wid = tid >> 5, lane = tid & 31;
+        for (int blk = wid; blk < a.T * 16; blk += kWarps) {
+            const int tk = blk >> 4, b = blk & 15;
+            const float *xr = a.x + (size_t)tk * kH + 256 * b;
+            float v[8], amax = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                v[i] = xr[lane + 32 * i];
+                amax = fmaxf(amax, fabsf(v[i]));
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            const float db = __fdiv_rn(amax, 127.0f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                int q = 0;
+                if (db > 0.f) q = max(-127, min(127, __float2int_rn(__fdiv_rn(v[i], db))));
+                sm.x8[(size_t)tk * kH + 256 * b + lane + 32 * i] = (int8_t)q;
+            }
+            if (lane == 0) sm.dx[tk * 16 + b] = db;
         }
     }
     for (int i = tid; i < a.T * kH; i += kThreads) {
@@ -472,6 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_decode_kernel(DecodeArgs a
             sh = task_kind(tau, NR, NS, idx);
         }
         if (sh) gu_shared(a, sm, idx);
+        else if (a.gu_type == DS4G_IQ2_XXS && a.q8) gu_routed_iq2_q8(a, sm, idx);
         else if (a.gu_type == DS4G_IQ2_XXS) gu_routed_iq2(a, sm, idx);
         else gu_routed_q4k(a, sm, idx);
     }
@@ -757,7 +878,7 @@ static int g_num_sms = 0;
 
 ds4g_status decode_forward(const float *hidden, int T, const ds4g_layer *L, const int32_t *ids,
                            const float *w, float *out, void *workspace, cudaStream_t st, int phases,
-                           uint32_t *status_word, const uint32_t *ready, uint32_t epoch) {
+                           uint32_t *status_word, const uint32_t *ready, uint32_t epoch, int q8) {
     if (!g_num_sms) {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess) return DS4G_ECUDA;
@@ -794,9 +915,11 @@ ds4g_status decode_forward(const float *hidden, int T, const ds4g_layer *L, cons
     a.part_ds = (float *)(ws + wl.part_ds);
     a.ready = ready;
     a.epoch = epoch;
+    a.q8 = q8 && L->gate_up_type == DS4G_IQ2_XXS ? 1 : 0;
 
     const size_t ns = (size_t)kK * T;
-    const size_t smem_gu = 256 * 16 * 8 + 128 * 16 * 8 + (size_t)T * 2 * kH * 2 * 2;
+    const size_t smem_gu = 256 * 16 * 8 + 128 * 16 * 8 + (size_t)T * 2 * kH * 2 * 2 +
+                           (q8 ? 128 * 16 * 16 + (size_t)T * kH + (size_t)T * 16 * 4 : 0);
     const size_t smem_dn = ns * 2 * kF * 2 + 2 * ns * 128 * 4 + (size_t)T * 2 * kF * 2;
     static bool attr_done = false;
     if (!attr_done) {

@@ -89,11 +89,13 @@ struct TraceRange {
 // status_word: where its kernels record a fault (nullptr: the workspace's
 // own header).  ready/epoch (streamed experts): the routed tasks of slot i
 // wait until ready[i] == epoch (written by a copy stream after the slot's
-// expert has landed); nullptr: no waiting.
+// expert has landed); nullptr: no waiting.  q8: routed IQ2_XXS gate/up on
+// int8 activations (ds4g_moe_forward_q8).
 size_t decode_workspace(int T);
 ds4g_status decode_forward(const float *hidden, int T, const ds4g_layer *L, const int32_t *ids, const float *w,
                            float *out, void *workspace, cudaStream_t st, int phases,
-                           uint32_t *status_word = nullptr, const uint32_t *ready = nullptr, uint32_t epoch = 0);
+                           uint32_t *status_word = nullptr, const uint32_t *ready = nullptr, uint32_t epoch = 0,
+                           int q8 = 0);
 
 // ds4g_moe_forward's checks, then, for T <= kDecodeMaxT, the decode kernels
 // with the ready flags above; DS4G_EUNSUPPORTED for larger T (api.cu).

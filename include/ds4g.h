@@ -253,6 +253,25 @@ ds4g_status ds4g_moe_down(const float *hidden, int T, const ds4g_layer *L,
                           void *workspace, size_t ws_bytes, ds4g_stream_t s);
 
 /* ------------------------------------------------------------------------
+ * The int8-activation decode path (chenxutan ds4 article §2.4: the
+ * dot_iq2_pair_16 kernel, int8 grid values against int8 activations; here
+ * with dp4a).  ds4g_moe_forward for 1 <= T <= 3 with the routed IQ2_XXS gate
+ * and up projections on q8 activations: per token and 256-column block,
+ * d = max|x| / 127 (fp32) and q = x / d rounded to nearest, ties to even,
+ * clamped to +-127 (a reading: the pages give the dot, not the quantiser);
+ * per 32-weight sub-block the exact integer sum S of (sign * grid value) * q,
+ * then d_sub * d * S in fp32.  The down projection, the shared expert and
+ * everything else are those of ds4g_moe_forward.  Same arguments and checks;
+ * T > 3 or a gate/up type other than IQ2_XXS: DS4G_EUNSUPPORTED.  Results
+ * differ from ds4g_moe_forward by the activation rounding (about 0.4 % of
+ * each block's largest value per entry): an alternative path, not the
+ * default (see the design notes for its measured speed).
+ * ------------------------------------------------------------------------ */
+ds4g_status ds4g_moe_forward_q8(const float *hidden, int T, const ds4g_layer *L,
+                                const int32_t *ids, const float *w, float *out,
+                                void *workspace, size_t ws_bytes, ds4g_stream_t s);
+
+/* ------------------------------------------------------------------------
  * One decode token through one whole MoE layer in a single launch ([P1]
  * §2.3: router logic and expert compute fused into one GPU dispatch; §3.2
  * moe_forward).  With xn = hidden / sqrt(mean(hidden^2) + 1e-6) if normalize

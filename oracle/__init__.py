@@ -59,6 +59,8 @@ def lib():
         L.oracle_moe_forward.argtypes = [vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp,
                                          vp, vp, vp, vp, vp, vp, vp, i32]
         L.oracle_expert_mlp.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, i32]
+        L.oracle_quantize_q8.argtypes = [vp, i32, vp, vp]
+        L.oracle_moe_forward_q8.argtypes = L.oracle_moe_forward.argtypes
         _lib = L
     return _lib
 
@@ -158,6 +160,38 @@ def moe_forward(hidden, ids, w, gate, up, down, sh_gate, sh_up, sh_down, grid,
                                   nthreads)
     if rc:
         raise ValueError(f"oracle_moe_forward rc={rc}")
+    return out
+
+
+def quantize_q8(x: np.ndarray):
+    """q8 activations of one row (blocks of 256): (int8 q [n], f32 d [n/256])."""
+    x = _c(x, np.float32).reshape(-1)
+    q = np.empty(x.size, np.int8)
+    d = np.empty(x.size // 256, np.float32)
+    if lib().oracle_quantize_q8(_p(x), x.size, _p(q), _p(d)):
+        raise ValueError("oracle_quantize_q8: n must be a positive multiple of 256")
+    return q, d
+
+
+def moe_forward_q8(hidden, ids, w, gate, up, down, sh_gate, sh_up, sh_down, grid,
+                   gate_up_type=IQ2_XXS, down_type=Q2_K, F=None, nthreads=0):
+    """moe_forward with the routed IQ2_XXS gate/up on q8 activations."""
+    hidden = _c(hidden, np.float32)
+    ids = _c(ids, np.int32)
+    w = _c(w, np.float32)
+    T, H = hidden.shape
+    K = ids.shape[1]
+    E = len(gate)
+    F = F if F is not None else sh_gate.shape[0]
+    keep = [None if m is None else _c(m, np.uint8) for m in gate + up + down]
+    ga, ua, da = (_ptr_array(keep[0:E]), _ptr_array(keep[E:2 * E]), _ptr_array(keep[2 * E:]))
+    shg, shu, shd = (_c(a, np.uint16) for a in (sh_gate, sh_up, sh_down))
+    g = _c(grid, np.uint8)
+    out = np.empty((T, H), np.float32)
+    rc = lib().oracle_moe_forward_q8(_p(hidden), T, H, F, E, K, gate_up_type, down_type, ga, ua, da,
+                                     _p(shg), _p(shu), _p(shd), _p(g), _p(ids), _p(w), _p(out), nthreads)
+    if rc:
+        raise ValueError(f"oracle_moe_forward_q8 rc={rc}")
     return out
 
 

@@ -368,3 +368,129 @@ int oracle_moe_forward(const float *hidden, int T, int H, int F, int E, int K,
     free(y);
     return rc;
 }
+
+/* ------------------------------------------------------------ q8 path */
+
+int oracle_quantize_q8(const float *x, int n, int8_t *q, float *d) {
+    if (!x || !q || !d || n <= 0 || n % 256) return -1;
+    for (int b = 0; b < n / 256; ++b) {
+        float amax = 0.0f;
+        for (int i = 0; i < 256; ++i) {
+            const float a = fabsf(x[256 * b + i]);
+            if (a > amax) amax = a;
+        }
+        const float db = amax / 127.0f;
+        d[b] = db;
+        for (int i = 0; i < 256; ++i) {
+            int v = 0;
+            if (db > 0.0f) {
+                const float r = rintf(x[256 * b + i] / db); /* default mode: nearest, ties to even */
+                v = r > 127.0f ? 127 : r < -127.0f ? -127 : (int)r;
+            }
+            q[256 * b + i] = (int8_t)v;
+        }
+    }
+    return 0;
+}
+
+/* The pages' dot of 16 int8 grid values (two grid rows) against 16 int8
+ * activations (chenxutan ds4 article §2.4, dot_iq2_pair_16), restated. */
+static int32_t dot16_i8(const int8_t *g0, const int8_t *g1, const int8_t *q) {
+    int32_t s = 0;
+    for (int i = 0; i < 8; ++i) s += (int32_t)g0[i] * q[i] + (int32_t)g1[i] * q[i + 8];
+    return s;
+}
+
+/* One IQ2_XXS row [cols] on q8 activations (q, dx per 256 columns). */
+static double iq2_row_dot_q8(const uint8_t *row_blocks, int cols, const uint8_t *grid, const int8_t *q,
+                             const float *dx) {
+    double acc = 0.0;
+    for (int b = 0; b < cols / 256; ++b) {
+        const uint8_t *blk = row_blocks + (size_t)b * 66;
+        const float d = oracle_fp16_to_f32(rd16(blk));
+        for (int sb = 0; sb < 8; ++sb) {
+            const uint8_t *c = blk + 2 + 8 * sb;
+            const uint32_t v = rd32(c + 4);
+            const float db = (d * (0.5f + (float)(v >> 28))) * 0.25f;
+            int8_t gs[4][8]; /* signed grid values of the sub-block's four rows */
+            for (int l = 0; l < 4; ++l) {
+                const uint32_t s7 = (v >> (7 * l)) & 127u;
+                uint32_t sg = s7;
+                int par = 0;
+                for (int k = 0; k < 7; ++k) par ^= (int)((s7 >> k) & 1u);
+                sg |= (uint32_t)par << 7;
+                for (int i = 0; i < 8; ++i) {
+                    const int g = grid[8 * c[l] + i];
+                    gs[l][i] = (int8_t)(((sg >> i) & 1u) ? -g : g);
+                }
+            }
+            const int8_t *qs = q + 256 * b + 32 * sb;
+            const int32_t S = dot16_i8(gs[0], gs[1], qs) + dot16_i8(gs[2], gs[3], qs + 16);
+            acc += (double)db * (double)dx[b] * (double)S;
+        }
+    }
+    return acc;
+}
+
+static int expert_mlp_q8(const double *x, const int8_t *q, const float *dx, int H, int F, int dt, const void *G,
+                         const void *U, const void *D, const uint8_t *grid, double *y, int nthreads) {
+    double *g = (double *)malloc(sizeof(double) * (size_t)F);
+    double *u = (double *)malloc(sizeof(double) * (size_t)F);
+    int rc = (!g || !u || !G || !U) ? -1 : 0;
+    if (!rc) {
+#pragma omp parallel for num_threads(nthreads > 0 ? nthreads : omp_get_max_threads()) schedule(static)
+        for (int r = 0; r < F; ++r) {
+            g[r] = iq2_row_dot_q8((const uint8_t *)G + (size_t)r * (H / 256) * 66, H, grid, q, dx);
+            u[r] = iq2_row_dot_q8((const uint8_t *)U + (size_t)r * (H / 256) * 66, H, grid, q, dx);
+        }
+        for (int i = 0; i < F; ++i) g[i] = silu(g[i]) * u[i];
+        rc = matvec(dt, D, H, F, grid, g, y, nthreads);
+    }
+    (void)x;
+    free(g);
+    free(u);
+    return rc;
+}
+
+int oracle_moe_forward_q8(const float *hidden, int T, int H, int F, int E, int K,
+                          int gate_up_type, int down_type, const void *const *gate,
+                          const void *const *up, const void *const *down,
+                          const uint16_t *sh_gate, const uint16_t *sh_up,
+                          const uint16_t *sh_down, const uint8_t *grid, const int32_t *ids,
+                          const float *w, float *out, int nthreads) {
+    if (!hidden || !gate || !up || !down || !sh_gate || !sh_up || !sh_down || !ids || !w || !grid ||
+        !out || T < 1 || K < 1 || E < 1 || H % 256 || F % 256 || H <= 0 || F <= 0 ||
+        gate_up_type != ORACLE_IQ2_XXS)
+        return -1;
+    double *x = (double *)malloc(sizeof(double) * (size_t)H);
+    double *acc = (double *)malloc(sizeof(double) * (size_t)H);
+    double *y = (double *)malloc(sizeof(double) * (size_t)H);
+    int8_t *q = (int8_t *)malloc((size_t)H);
+    float *dx = (float *)malloc(sizeof(float) * (size_t)(H / 256));
+    int rc = (!x || !acc || !y || !q || !dx) ? -1 : 0;
+    for (int t = 0; t < T && rc == 0; ++t) {
+        const float *xt = hidden + (size_t)t * H;
+        for (int j = 0; j < H; ++j) x[j] = (double)xt[j];
+        for (int j = 0; j < H; ++j) acc[j] = 0.0;
+        rc = oracle_quantize_q8(xt, H, q, dx);
+        for (int k = 0; k < K && rc == 0; ++k) {
+            const int e = ids[(size_t)t * K + k];
+            if (e < 0 || e >= E || !gate[e] || !up[e] || !down[e]) {
+                rc = -2;
+                break;
+            }
+            rc = expert_mlp_q8(x, q, dx, H, F, down_type, gate[e], up[e], down[e], grid, y, nthreads);
+            const double wk = (double)w[(size_t)t * K + k];
+            for (int j = 0; j < H; ++j) acc[j] += wk * y[j];
+        }
+        if (rc) break;
+        rc = expert_mlp_d(x, H, F, ORACLE_BF16, ORACLE_BF16, sh_gate, sh_up, sh_down, NULL, y, nthreads);
+        for (int j = 0; j < H; ++j) out[(size_t)t * H + j] = (float)(y[j] + acc[j]);
+    }
+    free(x);
+    free(acc);
+    free(y);
+    free(q);
+    free(dx);
+    return rc;
+}

@@ -79,4 +79,26 @@ int oracle_expert_mlp(const float *x, int H, int F, int gate_up_type,
                       const void *D, const uint8_t *grid, double *y,
                       int nthreads);
 
+/* q8 activations (the int8 path: chenxutan ds4 article §2.4, the
+ * dot_iq2_pair_16 kernel, int8 grid values against int8 activations).
+ * Reading (the pages give the dot, not the quantiser): blocks of 256
+ * columns; d = max|x| / 127 in fp32 (0 for an all-zero block); q = x / d in
+ * fp32 rounded to the nearest integer, ties to even, clamped to [-127, 127].
+ * q [n] int8, d [n / 256]; n a multiple of 256.  Returns 0 or -1. */
+int oracle_quantize_q8(const float *x, int n, int8_t *q, float *d);
+
+/* oracle_moe_forward with the routed IQ2_XXS gate and up projections on q8
+ * activations: per 32-weight sub-block the exact integer sum S of
+ * (sign * grid value) * q (as dot_iq2_pair_16 forms it, 16 products at a
+ * time), then row += db * d_x * S (fp64, in index order; db the sub-block
+ * scale of the format).  The down projection and the shared expert are as in
+ * oracle_moe_forward.  gate_up_type must be IQ2_XXS (-1 otherwise). */
+int oracle_moe_forward_q8(const float *hidden, int T, int H, int F, int E, int K,
+                          int gate_up_type, int down_type,
+                          const void *const *gate, const void *const *up,
+                          const void *const *down, const uint16_t *sh_gate,
+                          const uint16_t *sh_up, const uint16_t *sh_down,
+                          const uint8_t *grid, const int32_t *ids, const float *w,
+                          float *out, int nthreads);
+
 #endif

@@ -110,3 +110,12 @@ class FullLayer:
         for e in sorted(set(int(v) for v in ids.reshape(-1))):
             gate[e], up[e], down[e] = synth.expert(self.seed, self.cfg, self.lay, e, self.gut, self.dt)
         return oracle.moe_forward(x, ids, w, gate, up, down, *self.shared, self.grid, self.gut, self.dt)
+
+
+def oracle_forward_q8(x, ids, w, hx, shared, grid, gut=synth.IQ2_XXS, dt=synth.Q2_K, nthreads=0):
+    """The oracle's q8 mode (routed IQ2_XXS gate/up on int8 activations)."""
+    import oracle
+    gate, up, down = [None] * E, [None] * E, [None] * E
+    for e, (g, u, d) in hx.items():
+        gate[e], up[e], down[e] = g, u, d
+    return oracle.moe_forward_q8(x, ids, w, gate, up, down, *shared, grid, gut, dt, nthreads=nthreads)
