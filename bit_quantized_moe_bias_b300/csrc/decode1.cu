@@ -116,7 +116,7 @@ struct D1Sync {
     uint32_t router_done;  // router logits stored
     uint32_t sgu_done;     // shared gate/up tiles whose h is stored
     uint32_t exit_count;
-    uint32_t pad0[5];
+    uint32_t pad0[5];      // [1]: a CTA of this launch gave up (per-tile counters need a reset)
     uint32_t rgu_done[8];  // per routed slot: gate/up 16-row tiles stored
     uint32_t tile_cnt[kH / 16];
     uint32_t sgu_cnt[kF / 16];   // per shared gate/up tile: column quarters stored
@@ -1386,15 +1386,23 @@ __global__ void __launch_bounds__(kD1Threads, 1)
     // ================================================== exit protocol
     __syncthreads();
     if (tid == 0) {
+        // a CTA that gave up may leave per-tile counters non-zero: say so
+        if (*abort_flag) a.sync->pad0[1] = 1u;
         __threadfence();
         const uint32_t done = atomicAdd(&a.sync->exit_count, 1u);
         if (done == gridDim.x - 1) {
-            // every CTA has finished: reset the coordination block for the next launch
+            // every CTA has finished: reset the coordination block for the next
+            // launch (the per-tile counters are reset by their last arrivals,
+            // so only after a launch that gave up)
+            __threadfence();
             a.sync->router_done = 0;
             a.sync->sgu_done = 0;
-            for (int t = 0; t < kF / 16; ++t) a.sync->sgu_cnt[t] = 0;   // already zero unless a launch gave up
             for (int k = 0; k < 8; ++k) a.sync->rgu_done[k] = 0;
-            for (int t = 0; t < kH / 16; ++t) a.sync->tile_cnt[t] = 0;   // already zero unless a launch gave up
+            if (*reinterpret_cast<volatile uint32_t *>(&a.sync->pad0[1])) {
+                for (int t = 0; t < kF / 16; ++t) a.sync->sgu_cnt[t] = 0;
+                for (int t = 0; t < kH / 16; ++t) a.sync->tile_cnt[t] = 0;
+                a.sync->pad0[1] = 0;
+            }
             __threadfence();
             a.sync->exit_count = 0;
         }
