@@ -605,7 +605,7 @@ def run_prefill(args, rank, world, local_rank):
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": kind, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "flop_per_launch": PF_GATEUP_FLOP,
                      "launch_us": round(gu_us, 2), "traffic": traffic_record("prefill_gemm_kernel")},
-        "gpu_launches": 6 * args.steps,   # route, bucket, permute, 2 x gemm, combine
+        "gpu_launches": 7 * args.steps,   # route, bucket, permute, gemm, h cast, gemm, combine
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:
@@ -843,7 +843,7 @@ def run_q2q4_prefill(args, rank, world, local_rank):
                                                   "8 layers", "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": kind, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "flop_per_launch": gu_flop // nl, "launch_us": round(gu_us / nl, 2), "traffic": None},
-        "gpu_launches": (nl * 6 + (nl - 1)) * args.steps,
+        "gpu_launches": (nl * 7 + (nl - 1)) * args.steps,   # per layer as in the prefill line; rmsnorm between
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:

@@ -7,6 +7,7 @@
 // One launch for any T:
 //   small T (<= 64): CTA (expert group of 8, k-quarter); each warp streams one
 //     router row quarter once and dots it with all T tokens (4 at a time);
+//     above 8 tokens a second launch runs the top-6, one warp per token;
 //   large T: 32-token x 64-expert fp32 SIMT tiles over the full K.
 // Partial logits go to the workspace; the last CTA to finish a token range
 // (atomic ticket, no waiting) sums them in a fixed order and runs the top-k,
@@ -19,6 +20,7 @@ namespace ds4g {
 
 constexpr int kRouteSmallT = 64;
 constexpr int kRouteKS = 4;   // k-splits on the small-T path
+constexpr int kRouteFusedTopK = 8;   // up to here the last CTA runs the top-6 itself
 constexpr int kTileT = 32, kTileE = 64, kTileK = 32;
 
 struct RouteArgs {
@@ -125,6 +127,7 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteArgs a) {
             if (lane == 0 && t0 + u < a.T) a.part[((size_t)ks * a.T + t0 + u) * kE + e] = v;
         }
     }
+    if (a.T > kRouteFusedTopK) return;   // the top-6 runs in route_topk_kernel
     __threadfence();  // every writer publishes its partials before the ticket
     __shared__ uint32_t last;
     __syncthreads();
@@ -148,6 +151,22 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteArgs a) {
         __syncwarp();
     }
     if (threadIdx.x == 0) *a.cnt = 0u;
+}
+
+// Small-T path above kRouteFusedTopK tokens: the top-6 of each token from the
+// k-quarter partials (summed in order), one warp per token, ceil(T/8) CTAs.
+__global__ void __launch_bounds__(256) route_topk_kernel(RouteArgs a) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + warp;
+    __shared__ float lg[8][kE];
+    if (t >= a.T) return;
+    for (int ee = lane; ee < kE; ee += 32) {
+        float v = 0.f;
+        for (int s = 0; s < kRouteKS; ++s) v += __ldcg(a.part + ((size_t)s * a.T + t) * kE + ee);
+        lg[warp][ee] = v;
+    }
+    __syncwarp();
+    topk_warp(a, t, lg[warp]);
 }
 
 // grid (ceil(T/32), 4), block 128: fp32 tile 32 tokens x 64 experts; thread
@@ -290,6 +309,7 @@ extern "C" ds4g_status ds4g_moe_route(const float *hidden, int T, const float *r
     cudaStream_t st = (cudaStream_t)s;
     if (T <= kRouteSmallT) {
         route_small_kernel<<<dim3(kE / 8, kRouteKS), 256, 0, st>>>(a);
+        if (T > kRouteFusedTopK) route_topk_kernel<<<(T + 7) / 8, 256, 0, st>>>(a);
     } else {
         route_tiled_kernel<<<dim3((unsigned)ntile, kE / kTileE), kRouteTiledThreads, 0, st>>>(a);
     }
