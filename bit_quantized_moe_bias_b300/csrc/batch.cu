@@ -147,13 +147,95 @@ struct BgGuSmem {
     int *next;       // the CTA's next unclaimed task
 };
 
+// One pass of bg_gu_routed over up to 4 of a bucket's slots (s0 ..): every
+// grid row's operands are built once and multiplied by each token's
+// block-diagonal activation.  NT = 1, 2 or 4 (3 and 4 tokens): each token
+// accumulates into 4 / NT independent chains, so that few tokens still keep
+// several MMAs in flight.
+template <int NT>
+__device__ __forceinline__ void bg_gu_pass(const BGArgs &a, const BgGuSmem &sm, const uint4 (&qa)[4],
+                                           const uint4 (&qb)[4], const uint32_t (&dd)[4], int s0, int nt, int q,
+                                           int rt, int m) {
+    constexpr int CH = 4 / NT;   // accumulator chains per token
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3, p = lane & 15;
+    const BgBuckets &bk = *sm.bk;
+    const bool act = (g >> 1) == t;
+    int tok[NT];
+#pragma unroll
+    for (int i = 0; i < NT; ++i) tok[i] = i < nt ? bk.slot[s0 + i] / kK : 0;
+    float acc[NT][2];
+#pragma unroll
+    for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = 0.f;
+#pragma unroll
+    for (int kb = 0; kb < 4; ++kb) {
+        // d * 0.25 * 2^24 (the codes enter the mma as code * 2^-24)
+        const float d4g = __half2float(__ushort_as_half((unsigned short)(dd[kb] & 0xffffu))) * 4194304.0f;
+        const float d4h = __half2float(__ushort_as_half((unsigned short)(dd[kb] >> 16))) * 4194304.0f;
+#pragma unroll 1
+        for (int jj = 0; jj < 2; ++jj) {
+            const uint32_t ia = jj ? qa[kb].z : qa[kb].x, va = jj ? qa[kb].w : qa[kb].y;
+            const uint32_t ib = jj ? qb[kb].z : qb[kb].x, vb = jj ? qb[kb].w : qb[kb].y;
+            float c[4][4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) c[i][0] = c[i][1] = c[i][2] = c[i][3] = 0.f;
+#pragma unroll
+            for (int l = 0; l < 4; ++l) {
+                const uint2 ga = sm.gtab[((ia >> (8 * l)) & 255u) * 16 + p];
+                const uint2 sa = sm.stab[((va >> (7 * l)) & 127u) * 16 + p];
+                const uint2 gb = sm.gtab[((ib >> (8 * l)) & 255u) * 16 + p];
+                const uint2 sbv = sm.stab[((vb >> (7 * l)) & 127u) * 16 + p];
+                const uint32_t a0 = prmt(ga.x, sa.x, 0x5140), a1 = prmt(gb.x, sbv.x, 0x5140);
+                const uint32_t a2 = prmt(ga.x, sa.x, 0x7362), a3 = prmt(gb.x, sbv.x, 0x7362);
+                const uint32_t b0 = prmt(ga.y, sa.y, 0x5140), b1 = prmt(gb.y, sbv.y, 0x5140);
+                const uint32_t b2 = prmt(ga.y, sa.y, 0x7362), b3 = prmt(gb.y, sbv.y, 0x7362);
+                const int col = 256 * kb + 32 * (4 * jj + t) + 8 * l;
+#pragma unroll
+                for (int i = 0; i < NT; ++i) {
+                    if (i < nt) {
+                        uint4 B4 = make_uint4(0, 0, 0, 0);
+                        if (act) B4 = *reinterpret_cast<const uint4 *>(sm.x + ((size_t)tok[i] * 2 + (g & 1)) * kBXLd + col);
+                        mma_f16(c[i * CH + (2 * l) % CH], a0, a1, a2, a3, B4.x, B4.y);
+                        mma_f16(c[i * CH + (2 * l + 1) % CH], b0, b1, b2, b3, B4.z, B4.w);
+                    }
+                }
+            }
+            const float sg = d4g * half_plus(va >> 28), sh = d4h * half_plus(vb >> 28);
+#pragma unroll
+            for (int i = 0; i < NT; ++i) {
+                float u0 = 0.f, u1 = 0.f;
+#pragma unroll
+                for (int ch = 0; ch < CH; ++ch) {
+                    u0 += c[i * CH + ch][0] + c[i * CH + ch][1];
+                    u1 += c[i * CH + ch][2] + c[i * CH + ch][3];
+                }
+                acc[i][0] = fmaf(sg, u0, acc[i][0]);
+                acc[i][1] = fmaf(sh, u1, acc[i][1]);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < NT; ++i) {
+        float r0 = acc[i][0], r1 = acc[i][1];
+        r0 += __shfl_xor_sync(0xffffffffu, r0, 1);
+        r0 += __shfl_xor_sync(0xffffffffu, r0, 2);
+        r1 += __shfl_xor_sync(0xffffffffu, r1, 1);
+        r1 += __shfl_xor_sync(0xffffffffu, r1, 2);
+        if (i < nt && t == 0) {
+            const int slot = bk.slot[s0 + i];
+            float *pp = a.P + (((size_t)q * kK * a.T + slot) * 2 + m) * kF + 16 * rt;
+            pp[g] = r0;
+            pp[g + 8] = r1;
+        }
+    }
+}
+
 // A selected expert's gate or up rows 16 rt .. +16 over the CTA's quarter, for
 // all slots of bucket bi (4 tokens per pass).  The quarter's four tile-blocks
 // are loaded up front (four loads in flight per lane) and stay in registers
 // across the passes; pf: the next task's tile-blocks, prefetched into L2.
 __device__ __forceinline__ void bg_gu_routed(const BGArgs &a, const BgGuSmem &sm, int q, int bi, int rt, int m,
                                              const uint8_t *pf) {
-    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3, p = lane & 15;
+    const int lane = threadIdx.x & 31, g = lane >> 2;
     const BgBuckets &bk = *sm.bk;
     const int e = bk.eid[bi];
     const uint8_t *tb0 = (m ? a.up[e] : a.gate[e]) + ((size_t)rt * 16 + 4 * q) * kTB_IQ2;
@@ -166,70 +248,12 @@ __device__ __forceinline__ void bg_gu_routed(const BGArgs &a, const BgGuSmem &sm
         dd[kb] = ldg_stream32(tb0 + kb * kTB_IQ2 + 1024 + 4 * g);
     }
     if (pf) asm volatile("prefetch.global.L2 [%0];" ::"l"(pf + 128 * lane));   // 4 tile-blocks = 4224 B
-    const bool act = (g >> 1) == t;
     for (int s0 = bk.start[bi]; s0 < bk.start[bi + 1]; s0 += 4) {
         const int nt = min(4, bk.start[bi + 1] - s0);
-        int tok[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) tok[i] = i < nt ? bk.slot[s0 + i] / kK : 0;
-        float acc[4][2];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = 0.f;
-#pragma unroll
-        for (int kb = 0; kb < 4; ++kb) {
-            // d * 0.25 * 2^24 (the codes enter the mma as code * 2^-24)
-            const float d4g = __half2float(__ushort_as_half((unsigned short)(dd[kb] & 0xffffu))) * 4194304.0f;
-            const float d4h = __half2float(__ushort_as_half((unsigned short)(dd[kb] >> 16))) * 4194304.0f;
-#pragma unroll 1
-            for (int jj = 0; jj < 2; ++jj) {
-                const uint32_t ia = jj ? qa[kb].z : qa[kb].x, va = jj ? qa[kb].w : qa[kb].y;
-                const uint32_t ib = jj ? qb[kb].z : qb[kb].x, vb = jj ? qb[kb].w : qb[kb].y;
-                float c[4][4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) c[i][0] = c[i][1] = c[i][2] = c[i][3] = 0.f;
-#pragma unroll
-                for (int l = 0; l < 4; ++l) {
-                    const uint2 ga = sm.gtab[((ia >> (8 * l)) & 255u) * 16 + p];
-                    const uint2 sa = sm.stab[((va >> (7 * l)) & 127u) * 16 + p];
-                    const uint2 gb = sm.gtab[((ib >> (8 * l)) & 255u) * 16 + p];
-                    const uint2 sbv = sm.stab[((vb >> (7 * l)) & 127u) * 16 + p];
-                    const uint32_t a0 = prmt(ga.x, sa.x, 0x5140), a1 = prmt(gb.x, sbv.x, 0x5140);
-                    const uint32_t a2 = prmt(ga.x, sa.x, 0x7362), a3 = prmt(gb.x, sbv.x, 0x7362);
-                    const uint32_t b0 = prmt(ga.y, sa.y, 0x5140), b1 = prmt(gb.y, sbv.y, 0x5140);
-                    const uint32_t b2 = prmt(ga.y, sa.y, 0x7362), b3 = prmt(gb.y, sbv.y, 0x7362);
-                    const int col = 256 * kb + 32 * (4 * jj + t) + 8 * l;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        if (i < nt) {
-                            uint4 B4 = make_uint4(0, 0, 0, 0);
-                            if (act) B4 = *reinterpret_cast<const uint4 *>(sm.x + ((size_t)tok[i] * 2 + (g & 1)) * kBXLd + col);
-                            mma_f16(c[i], a0, a1, a2, a3, B4.x, B4.y);
-                            mma_f16(c[i], b0, b1, b2, b3, B4.z, B4.w);
-                        }
-                    }
-                }
-                const float sg = d4g * half_plus(va >> 28), sh = d4h * half_plus(vb >> 28);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    acc[i][0] = fmaf(sg, c[i][0] + c[i][1], acc[i][0]);
-                    acc[i][1] = fmaf(sh, c[i][2] + c[i][3], acc[i][1]);
-                }
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float r0 = acc[i][0], r1 = acc[i][1];
-            r0 += __shfl_xor_sync(0xffffffffu, r0, 1);
-            r0 += __shfl_xor_sync(0xffffffffu, r0, 2);
-            r1 += __shfl_xor_sync(0xffffffffu, r1, 1);
-            r1 += __shfl_xor_sync(0xffffffffu, r1, 2);
-            if (i < nt && t == 0) {
-                const int slot = bk.slot[s0 + i];
-                float *pp = a.P + (((size_t)q * kK * a.T + slot) * 2 + m) * kF + 16 * rt;
-                pp[g] = r0;
-                pp[g + 8] = r1;
-            }
-        }
+        // fewer tokens, more independent accumulator chains per token
+        if (nt == 1) bg_gu_pass<1>(a, sm, qa, qb, dd, s0, nt, q, rt, m);
+        else if (nt == 2) bg_gu_pass<2>(a, sm, qa, qb, dd, s0, nt, q, rt, m);
+        else bg_gu_pass<4>(a, sm, qa, qb, dd, s0, nt, q, rt, m);
     }
 }
 
