@@ -462,76 +462,124 @@ __device__ __forceinline__ uint32_t and_here(uint32_t x, uint32_t sh, uint32_t m
     return r;
 }
 
-// A selected expert's Q2_K down rows 64 og .. +64 (four 16-row tiles), block
-// b, for every slot of bucket bi: the four tile-blocks are loaded up front
-// (four loads in flight per lane); exact quants q * 4^s * 2^-24 with one mask
-// per slot s of the word, as in the per-slot path; h of each slot as the
-// block-diagonal B (one mma per 4 columns and slot).
-__device__ __forceinline__ void bg_dn_routed(const BGArgs &a, const BgDnSmem &sm, int b, int bi, int og) {
+// One pass of bg_dn_routed over up to NS of a bucket's slots (s0 ..): each
+// masked Q2_K operand of the two tile-blocks is built once per pass and
+// multiplied by every slot's block-diagonal h; per slot the arithmetic (mma
+// chain over cc, then the scale and min terms, summed over G in order) is
+// the same as for a single slot.
+template <int NS>
+__device__ __forceinline__ void bg_dn_pass(const BGArgs &a, const BgDnSmem &sm, int b, int og, const uint4 (&qa)[2],
+                                           const uint4 (&qb)[2], const uint32_t (&sca)[2], const uint32_t (&scb)[2],
+                                           const uint2 (&dd)[2], int s0, int ns) {
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const BgBuckets &bk = *sm.bk;
-    const int e = bk.eid[bi];
-    uint4 qa[4], qb[4];
-    uint32_t sca[4], scb[4];
-    uint2 dd[4];
+    // B: h of the slot (the lanes with g == 2t; column 2t + 1 of B stays zero)
+    const bool act = g == 2 * t;
+    int slot[NS];
+    float4 X[NS], S[NS];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const uint8_t *tb = a.down[e] + ((size_t)(4 * og + u) * kBB + b) * kTB_Q2K;
+    for (int i = 0; i < NS; ++i) {
+        slot[i] = bk.slot[s0 + (i < ns ? i : 0)];
+        X[i] = *reinterpret_cast<const float4 *>(sm.xs + (size_t)slot[i] * 16 + 4 * t);
+        S[i] = *reinterpret_cast<const float4 *>(sm.hsc + (size_t)slot[i] * 16 + 4 * t);
+    }
+    float dg[2], mg[2], dh[2], mh[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        dg[u] = __half2float(__ushort_as_half((unsigned short)(dd[u].x & 0xffff))) * 16777216.0f;
+        mg[u] = __half2float(__ushort_as_half((unsigned short)(dd[u].x >> 16)));
+        dh[u] = __half2float(__ushort_as_half((unsigned short)(dd[u].y & 0xffff))) * 16777216.0f;
+        mh[u] = __half2float(__ushort_as_half((unsigned short)(dd[u].y >> 16)));
+    }
+    float sg[NS][2], sh[NS][2];
+#pragma unroll
+    for (int i = 0; i < NS; ++i) sg[i][0] = sg[i][1] = sh[i][0] = sh[i][1] = 0.f;
+#pragma unroll
+    for (int G = 0; G < 4; ++G) {
+        uint2 hv[NS][4];
+#pragma unroll
+        for (int i = 0; i < NS; ++i) {
+            const __half *hrow = sm.h + (size_t)slot[i] * kBHLd + 16 * t + 64 * G;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+                hv[i][cc] = act ? *reinterpret_cast<const uint2 *>(hrow + 4 * cc) : make_uint2(0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const uint32_t Wa = G == 0 ? qa[u].x : G == 1 ? qa[u].y : G == 2 ? qa[u].z : qa[u].w;
+            const uint32_t Wb = G == 0 ? qb[u].x : G == 1 ? qb[u].y : G == 2 ? qb[u].z : qb[u].w;
+            uint32_t op[4][4];
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                op[cc][0] = and_here(Wa, 4 * cc, 0x00030003u);
+                op[cc][1] = and_here(Wb, 4 * cc, 0x00030003u);
+                op[cc][2] = and_here(Wa, 4 * cc + 2, 0x00030003u);
+                op[cc][3] = and_here(Wb, 4 * cc + 2, 0x00030003u);
+            }
+            const uint32_t ba = (sca[u] >> (8 * G)) & 0xffu, bb = (scb[u] >> (8 * G)) & 0xffu;
+            const float kg = dg[u] * small_u2f(ba & 15u), ng = mg[u] * small_u2f(ba >> 4);
+            const float kh = dh[u] * small_u2f(bb & 15u), nh = mh[u] * small_u2f(bb >> 4);
+#pragma unroll
+            for (int i = 0; i < NS; ++i) {
+                if (i < ns) {
+                    const float Xg = G == 0 ? X[i].x : G == 1 ? X[i].y : G == 2 ? X[i].z : X[i].w;
+                    const float Sg = G == 0 ? S[i].x : G == 1 ? S[i].y : G == 2 ? S[i].z : S[i].w;
+                    float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc)
+                        mma_f16(c, op[cc][0], op[cc][1], op[cc][2], op[cc][3], hv[i][cc].x, hv[i][cc].y);
+                    sg[i][u] += kg * ((c[0] + c[1]) * Sg) - ng * Xg;
+                    sh[i][u] += kh * ((c[2] + c[3]) * Sg) - nh * Xg;
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            float r0 = sg[i][u], r1 = sh[i][u];
+            r0 += __shfl_xor_sync(0xffffffffu, r0, 1);
+            r0 += __shfl_xor_sync(0xffffffffu, r0, 2);
+            r1 += __shfl_xor_sync(0xffffffffu, r1, 1);
+            r1 += __shfl_xor_sync(0xffffffffu, r1, 2);
+            if (i < ns && t == 0) {
+                float *yy = a.Y + ((size_t)b * kK * a.T + slot[i]) * kH + 16 * (2 * og + u);
+                yy[g] = r0;
+                yy[g + 8] = r1;
+            }
+        }
+    }
+}
+
+// A selected expert's Q2_K down rows 32 og .. +32 (two 16-row tiles), block
+// b of h, for all slots of bucket bi (two slots per pass).  The two
+// tile-blocks are loaded up front and stay in registers across the passes;
+// pf: the warp's next task's tile-blocks, prefetched into L2.
+__device__ __forceinline__ void bg_dn_routed(const BGArgs &a, const BgDnSmem &sm, int b, int bi, int og,
+                                             const uint8_t *pf) {
+    const int lane = threadIdx.x & 31, g = lane >> 2;
+    const BgBuckets &bk = *sm.bk;
+    const int e = bk.eid[bi];
+    uint4 qa[2], qb[2];
+    uint32_t sca[2], scb[2];
+    uint2 dd[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const uint8_t *tb = a.down[e] + ((size_t)(2 * og + u) * kBB + b) * kTB_Q2K;
         qa[u] = ldg_stream128(tb + 16 * lane);
         qb[u] = ldg_stream128(tb + 512 + 16 * lane);
         sca[u] = ldg_stream32(tb + 1024 + 4 * lane);
         scb[u] = ldg_stream32(tb + 1152 + 4 * lane);
         dd[u] = ldg_stream64(tb + 1280 + 8 * g);
     }
-    // B: h of the slot (the lanes with g == 2t; column 2t + 1 of B stays zero)
-    const bool act = g == 2 * t;
-#pragma unroll 1
-    for (int i = bk.start[bi]; i < bk.start[bi + 1]; ++i) {
-        const int slot = bk.slot[i];
-        const __half *hrow = sm.h + (size_t)slot * kBHLd + 16 * t;
-        const float4 X = *reinterpret_cast<const float4 *>(sm.xs + (size_t)slot * 16 + 4 * t);
-        const float4 S = *reinterpret_cast<const float4 *>(sm.hsc + (size_t)slot * 16 + 4 * t);
-        const float Xg[4] = {X.x, X.y, X.z, X.w};
-        const float Sg[4] = {S.x, S.y, S.z, S.w};
-        float sg[4] = {0.f, 0.f, 0.f, 0.f}, sh[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int G = 0; G < 4; ++G) {
-            uint2 hv[4];
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
-                hv[cc] = act ? *reinterpret_cast<const uint2 *>(hrow + 64 * G + 4 * cc) : make_uint2(0, 0);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const uint32_t Wa = G == 0 ? qa[u].x : G == 1 ? qa[u].y : G == 2 ? qa[u].z : qa[u].w;
-                const uint32_t Wb = G == 0 ? qb[u].x : G == 1 ? qb[u].y : G == 2 ? qb[u].z : qb[u].w;
-                float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-                    mma_f16(c, and_here(Wa, 4 * cc, 0x00030003u), and_here(Wb, 4 * cc, 0x00030003u),
-                            and_here(Wa, 4 * cc + 2, 0x00030003u), and_here(Wb, 4 * cc + 2, 0x00030003u),
-                            hv[cc].x, hv[cc].y);
-                const float dg = __half2float(__ushort_as_half((unsigned short)(dd[u].x & 0xffff))) * 16777216.0f;
-                const float mg = __half2float(__ushort_as_half((unsigned short)(dd[u].x >> 16)));
-                const float dh = __half2float(__ushort_as_half((unsigned short)(dd[u].y & 0xffff))) * 16777216.0f;
-                const float mh = __half2float(__ushort_as_half((unsigned short)(dd[u].y >> 16)));
-                const uint32_t ba = (sca[u] >> (8 * G)) & 0xffu, bb = (scb[u] >> (8 * G)) & 0xffu;
-                sg[u] += dg * small_u2f(ba & 15u) * ((c[0] + c[1]) * Sg[G]) - mg * small_u2f(ba >> 4) * Xg[G];
-                sh[u] += dh * small_u2f(bb & 15u) * ((c[2] + c[3]) * Sg[G]) - mh * small_u2f(bb >> 4) * Xg[G];
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            float r0 = sg[u], r1 = sh[u];
-            r0 += __shfl_xor_sync(0xffffffffu, r0, 1);
-            r0 += __shfl_xor_sync(0xffffffffu, r0, 2);
-            r1 += __shfl_xor_sync(0xffffffffu, r1, 1);
-            r1 += __shfl_xor_sync(0xffffffffu, r1, 2);
-            if (t == 0) {
-                float *yy = a.Y + ((size_t)b * kK * a.T + slot) * kH + 16 * (4 * og + u);
-                yy[g] = r0;
-                yy[g + 8] = r1;
-            }
-        }
+    // lanes 0..10: the first tile-block (1344 B), lanes 16..26: the second
+    if (pf && (lane & 15) < 11)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(pf + (size_t)(lane >> 4) * kBB * kTB_Q2K + 128 * (lane & 15)));
+    for (int s0 = bk.start[bi]; s0 < bk.start[bi + 1]; s0 += 2) {
+        const int ns = min(2, bk.start[bi + 1] - s0);
+        if (ns == 1) bg_dn_pass<1>(a, sm, b, og, qa, qb, sca, scb, dd, s0, ns);
+        else bg_dn_pass<2>(a, sm, b, og, qa, qb, sca, scb, dd, s0, ns);
     }
 }
 
@@ -624,17 +672,31 @@ __global__ void __launch_bounds__(kBThreads, 1) bg_down_kernel(BGArgs a) {
     }
     if (tid == 0) *sm.next = 0;
     bg_buckets(a, *sm.bk, false);   // ends with __syncthreads
-    // tasks: 256 shared (16-row tile), then per bucket 64 routed (four tiles)
-    const int nshared = kH / 16, ntask = nshared + sm.bk->ne * (kH / 64);
+    // tasks: 256 shared (16-row tile), then per bucket 128 routed (two tiles)
+    const int nshared = kH / 16, ntask = nshared + sm.bk->ne * (kH / 32);
     const int nmine = ntask > ci ? (ntask - ci + ncb - 1) / ncb : 0;
-    while (true) {
-        int k = 0;
-        if ((tid & 31) == 0) k = atomicAdd(sm.next, 1);
-        k = __shfl_sync(0xffffffffu, k, 0);
-        if (k >= nmine) break;
+    // the warp claims its next task one ahead, so that task's weights can be
+    // prefetched into L2 while the current one runs
+    int k = 0;
+    if ((tid & 31) == 0) k = atomicAdd(sm.next, 1);
+    k = __shfl_sync(0xffffffffu, k, 0);
+    while (k < nmine) {
+        int kn = 0;
+        if ((tid & 31) == 0) kn = atomicAdd(sm.next, 1);
+        kn = __shfl_sync(0xffffffffu, kn, 0);
         const int task = ci + k * ncb;
-        if (task < nshared) bg_dn_shared(a, sm, b, task);
-        else bg_dn_routed(a, sm, b, (task - nshared) / (kH / 64), (task - nshared) % (kH / 64));
+        if (task < nshared) {
+            bg_dn_shared(a, sm, b, task);
+        } else {
+            const uint8_t *pf = nullptr;
+            const int taskn = ci + kn * ncb;
+            if (kn < nmine && taskn >= nshared) {
+                const int rn = taskn - nshared;
+                pf = a.down[sm.bk->eid[rn / (kH / 32)]] + ((size_t)(2 * (rn % (kH / 32))) * kBB + b) * kTB_Q2K;
+            }
+            bg_dn_routed(a, sm, b, (task - nshared) / (kH / 32), (task - nshared) % (kH / 32), pf);
+        }
+        k = kn;
     }
 }
 
