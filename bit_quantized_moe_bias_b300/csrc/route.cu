@@ -5,9 +5,11 @@
 // renormalised to sum 1.
 //
 // One launch for any T:
-//   small T (<= 64): CTA (expert group of 8, k-quarter); each warp streams one
+//   small T (<= 8): CTA (expert group of 8, k-quarter); each warp streams one
 //     router row quarter once and dots it with all T tokens (4 at a time);
-//     above 8 tokens a second launch runs the top-6, one warp per token;
+//   mid T (9..64): CTA (expert group of 16, 512-column k-slice) with the
+//     slice of x and of R staged in shared memory, one lane per token; a
+//     second launch runs the top-6, one warp per token;
 //   large T: 32-token x 64-expert fp32 SIMT tiles over the full K.
 // Partial logits go to the workspace; the last CTA to finish a token range
 // (atomic ticket, no waiting) sums them in a fixed order and runs the top-k,
@@ -20,7 +22,11 @@ namespace ds4g {
 
 constexpr int kRouteSmallT = 64;
 constexpr int kRouteKS = 4;   // k-splits on the small-T path
-constexpr int kRouteFusedTopK = 8;   // up to here the last CTA runs the top-6 itself
+constexpr int kRouteFusedTopK = 8;   // up to here: the small-T path, whose last CTA runs the top-6
+constexpr int kMidKS = 8;            // k-splits on the mid-T path
+constexpr int kMidKC = kH / kMidKS;  // 512 columns per split
+constexpr int kMidE = 16;            // experts per CTA (4 warps x 4)
+constexpr int kMidXLd = kMidKC + 4;  // x row in shared memory (+16 B: rows start on distinct banks)
 constexpr int kTileT = 32, kTileE = 64, kTileK = 32;
 
 struct RouteArgs {
@@ -30,7 +36,8 @@ struct RouteArgs {
     const float *bias;
     int32_t *ids;
     float *w;
-    float *part;      // small: [KS][T][256]; large: [T][256]
+    float *part;      // small / mid: [KS][T][256]; large: [T][256]
+    int nks;          // k-splits summed by route_topk_kernel
     uint32_t *cnt;    // small: [1]; large: [ceil(T/32)]
     uint32_t *status;
 };
@@ -127,7 +134,6 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteArgs a) {
             if (lane == 0 && t0 + u < a.T) a.part[((size_t)ks * a.T + t0 + u) * kE + e] = v;
         }
     }
-    if (a.T > kRouteFusedTopK) return;   // the top-6 runs in route_topk_kernel
     __threadfence();  // every writer publishes its partials before the ticket
     __shared__ uint32_t last;
     __syncthreads();
@@ -153,18 +159,89 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteArgs a) {
     if (threadIdx.x == 0) *a.cnt = 0u;
 }
 
-// Small-T path above kRouteFusedTopK tokens: the top-6 of each token from the
-// k-quarter partials (summed in order), one warp per token, ceil(T/8) CTAs.
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem)),
+                 "l"(gmem)
+                 : "memory");
+}
+
+// Mid-T path: grid (256 / 16, 8), block 128, dynamic shared memory
+// route_mid_smem(T).  CTA (g, ks) stages x[:, 512 ks .. +512] and the 16
+// router rows 16 g .. +16 over the same columns, then lane l of warp w dots
+// token l (and l + 32) with rows 16 g + 4 w .. +3: per row two interleaved
+// accumulators over alternate 4-column steps, added at the end.  Partials
+// part[ks][t][e].
+__global__ void __launch_bounds__(128) route_mid_kernel(RouteArgs a) {
+    extern __shared__ __align__(16) float msm[];
+    float *xs = msm;                                // [T][kMidXLd]
+    float *rs = msm + (size_t)a.T * kMidXLd;        // [16][kMidKC]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int e0 = blockIdx.x * kMidE, ks = blockIdx.y, k0 = ks * kMidKC;
+    constexpr int kC4 = kMidKC / 4;                 // 16-byte chunks per row slice
+    for (int i = tid; i < a.T * kC4; i += 128) {
+        const int t = i / kC4, c4 = i % kC4;
+        cp_async16(xs + (size_t)t * kMidXLd + 4 * c4, a.x + (size_t)t * kH + k0 + 4 * c4);
+    }
+    for (int i = tid; i < kMidE * kC4; i += 128) {
+        const int e = i / kC4, c4 = i % kC4;
+        cp_async16(rs + (size_t)e * kMidKC + 4 * c4, a.R + (size_t)(e0 + e) * kH + k0 + 4 * c4);
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
+    const float *rr = rs + (size_t)(4 * warp) * kMidKC;
+    for (int tb = 0; tb < a.T; tb += 32) {
+        const int t = tb + lane;
+        const bool has = t < a.T;
+        const float *xr = xs + (size_t)(has ? t : 0) * kMidXLd;
+        float acc[4][2];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = 0.f;
+#pragma unroll 2
+        for (int k = 0; k < kMidKC; k += 8) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float4 xv = *reinterpret_cast<const float4 *>(xr + k + 4 * h);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float4 rv = *reinterpret_cast<const float4 *>(rr + (size_t)j * kMidKC + k + 4 * h);
+                    float v = acc[j][h];
+                    v = fmaf(rv.x, xv.x, v);
+                    v = fmaf(rv.y, xv.y, v);
+                    v = fmaf(rv.z, xv.z, v);
+                    v = fmaf(rv.w, xv.w, v);
+                    acc[j][h] = v;
+                }
+            }
+        }
+        if (has)
+            *reinterpret_cast<float4 *>(a.part + ((size_t)ks * a.T + t) * kE + e0 + 4 * warp) =
+                make_float4(acc[0][0] + acc[0][1], acc[1][0] + acc[1][1], acc[2][0] + acc[2][1],
+                            acc[3][0] + acc[3][1]);
+    }
+}
+
+// Mid-T path: the top-6 of each token from the k-split partials (summed in
+// order), one warp per token, ceil(T/8) CTAs.
 __global__ void __launch_bounds__(256) route_topk_kernel(RouteArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + warp;
     __shared__ float lg[8][kE];
     if (t >= a.T) return;
-    for (int ee = lane; ee < kE; ee += 32) {
-        float v = 0.f;
-        for (int s = 0; s < kRouteKS; ++s) v += __ldcg(a.part + ((size_t)s * a.T + t) * kE + ee);
-        lg[warp][ee] = v;
+    // logit ee = lane + 32 i: the splits added in order; the loads of a
+    // split are independent of each other and of the previous split's adds
+    float v[kE / 32];
+#pragma unroll
+    for (int i = 0; i < kE / 32; ++i) v[i] = 0.f;
+#pragma unroll 4
+    for (int s = 0; s < a.nks; ++s) {
+        float p[kE / 32];
+#pragma unroll
+        for (int i = 0; i < kE / 32; ++i) p[i] = __ldcg(a.part + ((size_t)s * a.T + t) * kE + lane + 32 * i);
+#pragma unroll
+        for (int i = 0; i < kE / 32; ++i) v[i] += p[i];
     }
+#pragma unroll
+    for (int i = 0; i < kE / 32; ++i) lg[warp][lane + 32 * i] = v[i];
     __syncwarp();
     topk_warp(a, t, lg[warp]);
 }
@@ -271,8 +348,12 @@ __global__ void __launch_bounds__(kRouteTiledThreads) route_tiled_kernel(RouteAr
 using namespace ds4g;
 
 static size_t route_part_bytes(int T) {
-    return T <= kRouteSmallT ? (size_t)kRouteKS * T * kE * 4 : (size_t)T * kE * 4;
+    if (T <= kRouteFusedTopK) return (size_t)kRouteKS * T * kE * 4;
+    if (T <= kRouteSmallT) return (size_t)kMidKS * T * kE * 4;
+    return (size_t)T * kE * 4;
 }
+
+static size_t route_mid_smem(int T) { return ((size_t)T * kMidXLd + (size_t)kMidE * kMidKC) * 4; }
 
 // Ticket counters at a fixed offset, sized for DS4G_ROUTE_MAX_T tokens, so
 // that a workspace reused with another T never finds old partials where its
@@ -307,10 +388,22 @@ extern "C" ds4g_status ds4g_moe_route(const float *hidden, int T, const float *r
     a.cnt = (uint32_t *)(ws + kWsHeader);
     a.part = (float *)(ws + kWsHeader + kRouteCntBytes);
     cudaStream_t st = (cudaStream_t)s;
-    if (T <= kRouteSmallT) {
+    if (T <= kRouteFusedTopK) {
+        a.nks = kRouteKS;
         route_small_kernel<<<dim3(kE / 8, kRouteKS), 256, 0, st>>>(a);
-        if (T > kRouteFusedTopK) route_topk_kernel<<<(T + 7) / 8, 256, 0, st>>>(a);
+    } else if (T <= kRouteSmallT) {
+        static bool attr = false;   // the largest mid-T staging (T = 64) once per process
+        if (!attr) {
+            if (cudaFuncSetAttribute(route_mid_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)route_mid_smem(kRouteSmallT)) != cudaSuccess)
+                return DS4G_ECUDA;
+            attr = true;
+        }
+        a.nks = kMidKS;
+        route_mid_kernel<<<dim3(kE / kMidE, kMidKS), 128, route_mid_smem(T), st>>>(a);
+        route_topk_kernel<<<(T + 7) / 8, 256, 0, st>>>(a);
     } else {
+        a.nks = 1;
         route_tiled_kernel<<<dim3((unsigned)ntile, kE / kTileE), kRouteTiledThreads, 0, st>>>(a);
     }
     return cudaGetLastError() == cudaSuccess ? DS4G_OK : DS4G_ECUDA;

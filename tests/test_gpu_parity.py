@@ -77,8 +77,8 @@ def _route_gpu(x, R, b):
     return ids.cpu().numpy(), w.cpu().numpy()
 
 
-@pytest.mark.parametrize("T,zipf", [(1, False), (2, False), (8, False), (9, False), (33, True),
-                                    (300, False), (2048, False)])
+@pytest.mark.parametrize("T,zipf", [(1, False), (2, False), (8, False), (9, False), (33, True), (64, True),
+                                    (65, False), (300, False), (2048, False)])
 def test_route_parity(T, zipf):
     x = synth.hidden(0, 3, T)
     R = synth.router(0, 3)
@@ -320,7 +320,7 @@ def test_workspace_reused_across_T_and_paths():
     xr = _t(synth.hidden(5, 0, 2100))
     Rd, bd = _t(R), _t(b)
     rws = B.workspace(B.ds4g_route_workspace(2100))
-    for T in [1, 2100, 5, 2100, 1]:
+    for T in [1, 2100, 5, 40, 2100, 1]:
         outs = []
         for wsp in (rws, B.workspace(B.ds4g_route_workspace(T))):
             i = torch.full((T, K), -1, dtype=torch.int32, device=DEV)
