@@ -90,6 +90,18 @@ class ClockSampler:
         self.proc = None
 
     def __enter__(self):
+        # the fused decode kernel keeps one CTA on every SM and its CTAs wait
+        # on each other: another process's kernels on this GPU would stall it
+        # (bounded) and void the timing, so they are recorded and reported
+        self.others = []
+        try:
+            q = subprocess.run(["nvidia-smi", "-i", str(self.index), "--query-compute-apps=pid",
+                                "--format=csv,noheader"], capture_output=True, text=True, timeout=30)
+            self.others = sorted({int(v) for v in q.stdout.split() if v.isdigit() and int(v) != os.getpid()})
+        except (OSError, subprocess.SubprocessError):
+            pass
+        if self.others:
+            print(f"bench: other compute processes on GPU {self.index}: {self.others}", file=sys.stderr)
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
@@ -112,13 +124,14 @@ class ClockSampler:
 
     def summary(self):
         if not getattr(self, "samples", None):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"],
+                    "other_gpu_processes": getattr(self, "others", [])}
         sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
         mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for s in self.samples for i in range(4) if s[3 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(self.samples)}
+                "reasons": reasons, "samples": len(self.samples), "other_gpu_processes": self.others}
 
 
 # ------------------------------------------------------------------ our arm

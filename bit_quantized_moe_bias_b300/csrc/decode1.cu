@@ -1478,6 +1478,15 @@ static ds4g_status d1_setup() {
             cudaFuncSetAttribute(decode_t1_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kD1SmemBytes) != cudaSuccess)
             return DS4G_ECUDA;
+        // the CTAs wait on one another: one CTA (kD1Threads threads, kD1SmemBytes)
+        // must fit on every SM, else the launch could never make progress
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_t1_kernel<false>, kD1Threads,
+                                                          kD1SmemBytes) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_t1_kernel<true>, kD1Threads,
+                                                          kD1SmemBytes) != cudaSuccess)
+            return DS4G_ECUDA;
+        if (per_sm < 1) return DS4G_EUNSUPPORTED;
         g_d1_attr = true;
     }
     return DS4G_OK;

@@ -295,7 +295,12 @@ ds4g_status ds4g_moe_forward_q8(const float *hidden, int T, const ds4g_layer *L,
  * {8, 25, 43}, the format's magnitudes (DS4G_EUNSUPPORTED: this kernel
  * encodes grid rows as 2-bit codes of those values).
  * The kernel keeps one CTA on every SM and its CTAs wait on each other
- * (bounded), so it needs the whole GPU: run nothing else concurrently.
+ * (bounded), so it needs the whole GPU: run nothing else concurrently.  The
+ * first call checks that one CTA (its threads and 227 KB of shared memory)
+ * fits on an SM, and returns DS4G_EUNSUPPORTED without launching if not; a
+ * kernel of another stream or process that holds SMs for longer than the
+ * bounded waits (about 1 s) makes the call end with DS4G_ETIMEOUT, read
+ * back with ds4g_last_error.
  * ------------------------------------------------------------------------ */
 size_t ds4g_layer_decode_workspace(void);
 ds4g_status ds4g_moe_layer_decode(const float *hidden, int normalize, const float *router,
