@@ -224,6 +224,22 @@ def test_forward_batched_duplicates_flags_and_determinism():
     assert_close_fwd(got[ok], oracle_forward(x[ok], ids[ok], w[ok], hx, shared, grid))
 
 
+def test_forward_batched_single_hot_expert():
+    """The largest buckets of the batched path: every slot of every token
+    selects expert 7 (T = 40: a 192-slot bucket in the first 32-token chunk,
+    48 slots in the ragged second one), plus a token whose six slots are six
+    different experts next to it."""
+    T = 40
+    x = synth.hidden(4, 0, T)
+    ids = np.full((T, K), 7, np.int32)
+    ids[17] = [7, 1, 2, 3, 4, 5]
+    w = np.tile(np.array([0.25, 0.15, 0.2, 0.1, 0.2, 0.1], np.float32), (T, 1))
+    L, hx, shared, grid = device_layer(4, 0, 0, ids.reshape(-1))
+    got, st = _forward_gpu(x, ids, w, L)
+    assert st == 0
+    assert_close_fwd(got, oracle_forward(x, ids, w, hx, shared, grid))
+
+
 def test_forward_flags_missing_expert():
     x = synth.hidden(3, 0, 1)
     ids = np.array([[1, 2, 3, 4, 5, 6]], np.int32)
