@@ -11,8 +11,9 @@
 //      four tile-blocks, and (16-row tile, gate | up) of the shared expert.
 //      Routed: exact codes on mma.sync with a block-diagonal activation (one
 //      mma per token, the lane's own sub-block scales applied in fp32); the
-//      operand registers of a grid row are built once and used for up to 8
-//      tokens.  Shared: bf16 weights converted to fp16 (exact in the fp16
+//      operand registers of a grid row are built once and used for up to 4
+//      tokens (a pass), with 4 / (tokens of the pass) independent accumulator
+//      chains per token.  Shared: bf16 weights converted to fp16 (exact in the fp16
 //      normal range), the tokens as the mma's N (8 per mma, hi and lo).
 //      Output: per-quarter partial sums.
 //  bg_h_kernel       h = silu(sum_q gate) * (sum_q up) per slot and row: routed
@@ -20,8 +21,9 @@
 //      16-column sums and 2^e; shared h as fp16 hi, lo.
 //  bg_down_kernel    CTA c owns 256-column block b = c % 8 of h and keeps it for
 //      every slot in shared memory (routed: fp16 of 2^-e h; shared: hi, lo).
-//      Warp tasks: (selected expert, 16-row output tile) over that expert's
-//      slots (Q2_K quants exact, block-diagonal), and (16-row tile) of the
+//      Warp tasks: (selected expert, two 16-row output tiles) over that
+//      expert's slots, two slots per pass sharing each masked operand (Q2_K
+//      quants exact, block-diagonal), and (16-row tile) of the
 //      shared expert.  Output: per-block partials.
 //  bg_combine_kernel out[t] = sum_b shared_b[t] + sum_k w[t,k] sum_b y_b[t,k],
 //      in that fixed order.
