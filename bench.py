@@ -378,6 +378,120 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
+
+# ------------------------------------------------ single-layer workload
+S1_CFG, S1_COPIES = 0, 8
+S1_WORKLOAD = ("config0 single layer: 1 token through 1 MoE layer x 256 experts (IQ2_XXS gate/up, Q2_K down, "
+               "bf16 shared, fp32 router), route + forward in one ds4g_moe_layer_decode call; a step = {ntok} calls, "
+               "each on the next of {copies} independent layer copies")
+
+
+def run_single_layer(args, rank, world, local_rank):
+    """One token through one layer per call (rmsnorm + router + top-6 +
+    routed and shared experts: ds4g_moe_layer_decode, one launch), a fresh
+    N(0,1) token per call, the calls rotating over independent layer copies
+    so that every call reads its layer's weights from HBM (the copies
+    together are far larger than L2).  The launches are independent (no
+    programmatic overlap): each call's time is the single-layer latency."""
+    import torch
+    import bit_quantized_moe_bias_b300 as B
+    torch.cuda.set_device(local_rank)
+    dev = f"cuda:{local_rank}"
+    ntok, nc = args.tokens, S1_COPIES
+    t_setup = time.time()
+    layers = build_model(dev, nc, cfg=S1_CFG)
+    setup_s = time.time() - t_setup
+    x_host = torch.from_numpy(synth.hidden(SEED + rank, S1_CFG, ntok, layer=999, normalise=False)).pin_memory()
+    y_host = torch.empty(ntok, H, dtype=torch.float32).pin_memory()
+    x_dev = x_host.to(dev)
+    out_all = torch.empty(ntok, H, device=dev)
+    # one ids / w pair reused by every call (16-byte aligned, as the ABI requires)
+    ids = torch.empty(1, K, dtype=torch.int32, device=dev)
+    w = torch.empty(1, K, dtype=torch.float32, device=dev)
+    lws = B.workspace(B.ds4g_layer_decode_workspace(), dev)
+
+    def step():
+        for i in range(ntok):
+            L, R, b = layers[i % nc]
+            B.ds4g_moe_layer_decode(x_dev[i:i + 1], R, b, L.struct, ids, w, out_all[i:i + 1], lws)
+
+    step()
+    torch.cuda.synchronize()
+    st = B.ds4g_last_error(lws)
+    if st:
+        raise RuntimeError(f"device status {st} during warm-up")
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    with ClockSampler(local_rank) as clk:
+        ev0.record()
+        for _ in range(args.steps):
+            graph.replay()
+        ev1.record()
+        torch.cuda.synchronize()
+    barrier()
+    dev_s = ev0.elapsed_time(ev1) / 1e3
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        graph.replay()
+        y_host.copy_(out_all, non_blocking=True)
+        torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    barrier()
+    st = B.ds4g_last_error(lws)
+    if st:
+        raise RuntimeError(f"device status {st} after the timed region")
+    dev_s, e2e_s = max_over_ranks([dev_s, e2e_s], world, dev)
+    if rank != 0:
+        return None
+    tokens = ntok * args.steps * world
+    value = tokens / dev_s
+    call_us = dev_s / (ntok * args.steps) * 1e6
+    hbm, kind = peaks()
+    achieved = LAYER_BYTES / (call_us * 1e-6) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dev_s / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": DECODE_DTYPE, "data": "synthetic",
+        "config": {"workload": S1_WORKLOAD.format(ntok=ntok, copies=nc), "layers": 1, "layer_copies": nc,
+                   "tokens_per_step": ntok, "global_batch": 1, "seq_len": 1,
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": f"no flush: {nc} layer copies of 1.86 GB used in turn (>> 126 MB L2)",
+                   "us_per_call": round(call_us, 3),
+                   "packed_routed_gbs": round(ROUTED_BYTES / (call_us * 1e-6) / 1e9, 1),
+                   "setup_s": round(setup_s, 1)},
+        "e2e": {"value": round(tokens / e2e_s, 3), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(x_host.numel() * 4), "d2h_bytes_per_step": int(y_host.numel() * 4)},
+        "roofline": {"bound": "hbm", "kernel": "decode_t1_kernel (whole layer, independent launches)",
+                     "achieved": round(achieved, 1), "peak": hbm, "peak_kind": kind, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "bytes_per_launch": LAYER_BYTES,
+                     "launch_us": round(call_us, 3), "traffic": traffic_record("decode_t1_kernel")},
+        "gpu_launches": ntok * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline("single-layer", args.cpu_size, 4)
+    return line
+
 # ------------------------------------------------------ streamed workload
 ST_WORKLOAD = ("expert streaming decode: {nl} MoE layers x 256 experts (IQ2_XXS gate/up, Q2_K down) with the routed "
                "experts in pinned host memory and an HBM cache of {slots} expert slots (LRU), bf16 shared and fp32 "
@@ -865,7 +979,7 @@ def run_q2q4_prefill(args, rank, world, local_rank):
 
 
 WORKLOADS = {"decode": WORKLOAD, "prefill": PF_WORKLOAD, "batched": B2_WORKLOAD, "q2q4-prefill": Q4P_WORKLOAD,
-             "decode-stream": WORKLOAD}
+             "decode-stream": WORKLOAD, "single-layer": S1_WORKLOAD.format(ntok=64, copies=S1_COPIES)}
 
 
 # ------------------------------------------------------------- CPU oracle
@@ -975,6 +1089,9 @@ def _sampler(workload, size):
     if workload == "batched":
         return (lambda n: oracle_sample_layer(B2_CFG, size, True, n),
                 f"first {size} of the {B2_T} tokens of the batch (oracle route + forward)")
+    if workload == "single-layer":
+        return (lambda n: oracle_sample_layer(S1_CFG, size, False, n),
+                f"{size} tokens through one layer (oracle route + forward of a batch of {size} tokens)")
     if workload == "q2q4-prefill":
         return (lambda n: oracle_sample_q2q4(size, n),
                 f"first {size} of the {Q4P_T} tokens through all {Q4P_LAYERS} layers (oracle route + forward, "
@@ -986,7 +1103,7 @@ def _sampler(workload, size):
 
 
 def default_cpu_size(workload):
-    return {"prefill": 8, "batched": 32, "q2q4-prefill": 4}.get(workload, NLAYER)
+    return {"prefill": 8, "batched": 32, "q2q4-prefill": 4, "single-layer": 16}.get(workload, NLAYER)
 
 
 def run_reference(args):
@@ -1052,7 +1169,8 @@ def main():
                     help="decode = 43-layer full-depth decode (headline); prefill = T=2048 chunk, one layer; "
                          "batched = T=32 tokens, one layer, Zipf routing; q2q4-prefill = T=4096 through 8 "
                          "layers (2 q2, 6 q4), Zipf routing; decode-stream = routed experts streamed from host "
-                         "memory through an HBM cache")
+                         "memory through an HBM cache; single-layer = 1 token through 1 layer per call, 8 layer "
+                         "copies in turn")
     ap.add_argument("--stream-layers", type=int, default=4, help="decode-stream: layers (host memory 1.8 GB each)")
     ap.add_argument("--cache-slots", type=int, default=256, help="decode-stream: HBM cache slots (7.1 MB each)")
     ap.add_argument("--stream-source", choices=["host", "file"], default="host",
@@ -1080,7 +1198,7 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
     run = {"prefill": run_prefill, "decode-stream": run_stream, "batched": run_batched,
-           "q2q4-prefill": run_q2q4_prefill}.get(args.workload, run_ours)
+           "q2q4-prefill": run_q2q4_prefill, "single-layer": run_single_layer}.get(args.workload, run_ours)
     line = run(args, rank, world, local_rank)
     if line is not None:
         print(json.dumps(line), flush=True)

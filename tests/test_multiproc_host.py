@@ -60,14 +60,15 @@ def test_reference_arm_prints_only_on_rank0(monkeypatch):
     assert buf.getvalue() == ""
 
 
-def test_reference_arm_line_on_rank0(monkeypatch):
+@pytest.mark.parametrize("workload", ["decode", "single-layer"])
+def test_reference_arm_line_on_rank0(monkeypatch, workload):
     """The reference arm (the oracle on the host cores) prints one JSON line
     with the contract's keys."""
     import json
     for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
         monkeypatch.delenv(k, raising=False)
     monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference", "--steps", "1", "--warmup", "0",
-                                      "--cpu-size", "1"])
+                                      "--cpu-size", "1", "--workload", workload])
     buf = io.StringIO()
     with contextlib.redirect_stdout(buf):
         bench.main()
