@@ -164,6 +164,11 @@ __device__ __noinline__ bool pf_wait(uint64_t *bar, uint32_t parity, volatile in
         if (clock64() - t0 > (4ll << 30)) return false;  // ~2 s at 2 GHz
     }
 }
+// The same wait with its first test inline, for the single-thread producer
+// and MMA issuer, whose barriers are often complete already.
+__device__ __forceinline__ bool pf_wait_fast(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+    return tc::mbar_try_wait(bar, parity) || pf_wait(bar, parity, abort_flag);
+}
 
 // Bounded wait for one barrier phase at teardown.  It ignores the abort
 // flag: a TMA load or an MMA still in flight must finish before the CTA
@@ -491,7 +496,8 @@ __global__ void __launch_bounds__(kPFThreads, 1)
     if (warp == 0) {
         // ---------------------------------------------------- TMA producer
         if (lane == 0) {
-            uint32_t it = 0;
+            uint32_t it = 0, pph = 0;
+            int ps = 0;
             for (int tau = blockIdx.x; tau < ntask && !*abort_flag; tau += gridDim.x) {
                 const PFTask t = decode_task(a, sm.tp, tau);
                 // one box per stage: the smallest of 16/32/64/128 rows covering the chunk
@@ -499,9 +505,13 @@ __global__ void __launch_bounds__(kPFThreads, 1)
                 const CUtensorMap *tmB = brows == 16 ? &tmB16 : brows == 32 ? &tmB32 : brows == 64 ? &tmB64 : &tmB128;
                 const uint32_t bytes = (uint32_t)brows * 128u + (t.shared ? (uint32_t)nmat * kTile : 0u);
                 for (int ks = 0; ks < nkb; ++ks, ++it) {
-                    const int s = it % kStages;
-                    const uint32_t ph = (it / kStages) & 1u;
-                    if (!pf_wait(&sm.empty[s], ph ^ 1u, abort_flag)) {
+                    const int s = ps;
+                    const uint32_t ph = pph;
+                    if (++ps == kStages) {   // stage and phase of the next load
+                        ps = 0;
+                        pph ^= 1u;
+                    }
+                    if (!pf_wait_fast(&sm.empty[s], ph ^ 1u, abort_flag)) {
                         pf_abort(a, sm.abort_flag, 0x100u);
                         break;
                     }
@@ -526,7 +536,8 @@ __global__ void __launch_bounds__(kPFThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            uint32_t it = 0, ti = 0;
+            uint32_t ti = 0, ph = 0;   // stage s and phase ph of the next stage
+            int s = 0;
             for (int tau = blockIdx.x; tau < ntask && !*abort_flag; tau += gridDim.x, ++ti) {
                 const PFTask t = decode_task(a, sm.tp, tau);
                 const int ab = ti & 1;
@@ -539,10 +550,8 @@ __global__ void __launch_bounds__(kPFThreads, 1)
                 const uint32_t idesc = tc::idesc_f16(kBM, t.npad, t.shared);
                 const uint32_t dcol = tbase + (uint32_t)(ab * (a.phase == 1 ? 256 : 128));
                 bool ok = true;
-                for (int ks = 0; ks < nkb; ++ks, ++it) {
-                    const int s = it % kStages;
-                    const uint32_t ph = (it / kStages) & 1u;
-                    if (!pf_wait(&sm.full_b[s], ph, abort_flag) || !pf_wait(&sm.full_a[s], ph, abort_flag)) {
+                for (int ks = 0; ks < nkb; ++ks) {
+                    if (!pf_wait_fast(&sm.full_b[s], ph, abort_flag) || !pf_wait_fast(&sm.full_a[s], ph, abort_flag)) {
                         pf_abort(a, sm.abort_flag, 0x201u);
                         ok = false;
                         break;
@@ -556,9 +565,19 @@ __global__ void __launch_bounds__(kPFThreads, 1)
                     for (int k4 = 0; k4 < 4; ++k4) {
                         const uint32_t acc = (ks > 0 || k4 > 0) ? 1u : 0u;
                         tc::mma_f16_ss(dcol, da0 + 2 * k4, db + 2 * k4, idesc, acc);
-                        if (nmat == 2) tc::mma_f16_ss(dcol + 128, da1 + 2 * k4, db + 2 * k4, idesc, acc);
+                    }
+                    if (nmat == 2) {
+#pragma unroll
+                        for (int k4 = 0; k4 < 4; ++k4) {
+                            const uint32_t acc = (ks > 0 || k4 > 0) ? 1u : 0u;
+                            tc::mma_f16_ss(dcol + 128, da1 + 2 * k4, db + 2 * k4, idesc, acc);
+                        }
                     }
                     tc::mma_commit(&sm.empty[s]);
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
                 if (!ok) break;
                 tc::mma_commit(&sm.acc_full[ab]);
