@@ -557,10 +557,10 @@ __global__ void __launch_bounds__(kPFThreads, 1)
                         break;
                     }
                     tc::tc_fence_after();
-                    const uint8_t *st = sm.stage + (size_t)s * kStageBytes;
-                    const uint64_t da0 = tc::sw128_desc(tc::smem_u32(st));
-                    const uint64_t da1 = tc::sw128_desc(tc::smem_u32(st + kTile));
-                    const uint64_t db = tc::sw128_desc(tc::smem_u32(st + 2 * kTile));
+                    // the A1 and B tiles follow A0 at kTile and 2 kTile bytes (the
+                    // descriptors' start-address field counts 16-byte units)
+                    const uint64_t da0 = tc::sw128_desc(tc::smem_u32(sm.stage + (size_t)s * kStageBytes));
+                    const uint64_t da1 = da0 + (kTile >> 4), db = da0 + (2 * kTile >> 4);
 #pragma unroll
                     for (int k4 = 0; k4 < 4; ++k4) {
                         const uint32_t acc = (ks > 0 || k4 > 0) ? 1u : 0u;
@@ -683,7 +683,7 @@ __global__ void __launch_bounds__(kPFThreads, 1)
                     const int s = (it + ks) % kStages;
                     const uint32_t ph = ((it + ks) / kStages) & 1u;
                     if (!ok) continue;
-                    if (!pf_wait(&sm.empty[s], ph ^ 1u, abort_flag)) {
+                    if (!pf_wait_fast(&sm.empty[s], ph ^ 1u, abort_flag)) {
                         pf_abort(a, sm.abort_flag, 0x400u);
                         ok = false;
                         continue;
