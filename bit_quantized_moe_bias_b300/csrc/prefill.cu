@@ -247,23 +247,27 @@ __device__ __forceinline__ void sts128(uint8_t *tile, int m, int chunk, uint4 v)
 //     plus the 12 scale bytes;
 //   Q2_K (phase 2): the 32-bit words par * 4 .. + 3 of the row's k-half and
 //     their scale word.
+// The kernel is instantiated per weight type QT, so each instance holds only
+// its own type's registers.
+template <int QT>
 struct BlockRegs {
-    uint4 q[4];
-    uint32_t s[3];
+    uint4 q[QT == DS4G_Q4_K ? 4 : QT == DS4G_IQ2_XXS ? 2 : 1];
+    uint32_t s[QT == DS4G_Q4_K ? 3 : 1];
     uint32_t dd;
 };
 
+template <int QT>
 __device__ __forceinline__ void load_block(const PFArgs &a, const uint8_t *mat, int r, int kb, int kh, int par,
-                                           BlockRegs &R) {
+                                           BlockRegs<QT> &R) {
     const int nbc = a.Kdim / 256;
     const int rr = r & 15, g8 = rr & 7, hrow = rr >> 3;
-    if (a.qt == DS4G_IQ2_XXS) {
+    if constexpr (QT == DS4G_IQ2_XXS) {
         const uint8_t *tb = mat + ((size_t)(r >> 4) * nbc + kb) * kTB_IQ2;
         const uint8_t *row = tb + 512 * hrow + 64 * g8;
         R.q[0] = ldg_nc128(row + 16 * par);
         R.q[1] = ldg_nc128(row + 16 * (2 + par));
         R.dd = ldg_nc32(tb + 1024 + 4 * g8) >> (16 * hrow);
-    } else if (a.qt == DS4G_Q2_K) {
+    } else if constexpr (QT == DS4G_Q2_K) {
         const uint8_t *tb = mat + ((size_t)(r >> 4) * nbc + kb) * kTB_Q2K;
         const uint8_t *row = tb + 512 * hrow + 64 * g8 + 32 * kh;
         R.q[0] = ldg_nc128(row + 16 * par);
@@ -287,18 +291,21 @@ __device__ __forceinline__ void load_block(const PFArgs &a, const uint8_t *mat, 
 
 // Ask L2 to fetch the packed row segment this thread will need two block
 // columns from now (hides HBM latency behind the register double buffer).
+template <int QT>
 __device__ __forceinline__ void prefetch_block(const PFArgs &a, const uint8_t *mat, int r, int kb, int kh) {
     const int nbc = a.Kdim / 256;
     if (kb >= nbc) return;
     const int rr = r & 15, g8 = rr & 7, hrow = rr >> 3;
     const uint8_t *p;
-    if (a.qt == DS4G_IQ2_XXS) p = mat + ((size_t)(r >> 4) * nbc + kb) * kTB_IQ2 + 512 * hrow + 64 * g8;
-    else if (a.qt == DS4G_Q2_K) p = mat + ((size_t)(r >> 4) * nbc + kb) * kTB_Q2K + 512 * hrow + 64 * g8 + 32 * kh;
+    if constexpr (QT == DS4G_IQ2_XXS) p = mat + ((size_t)(r >> 4) * nbc + kb) * kTB_IQ2 + 512 * hrow + 64 * g8;
+    else if constexpr (QT == DS4G_Q2_K)
+        p = mat + ((size_t)(r >> 4) * nbc + kb) * kTB_Q2K + 512 * hrow + 64 * g8 + 32 * kh;
     else p = mat + ((size_t)(r >> 4) * nbc + kb) * kTB_Q4K + 1024 * hrow + 128 * g8;
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
-__device__ __forceinline__ uint32_t word_of(const BlockRegs &R, int i) {
+template <int QT>
+__device__ __forceinline__ uint32_t word_of(const BlockRegs<QT> &R, int i) {
     const uint4 v = R.q[i >> 2];
     const int k = i & 3;
     return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
@@ -306,7 +313,8 @@ __device__ __forceinline__ uint32_t word_of(const BlockRegs &R, int i) {
 __device__ __forceinline__ uint32_t word4(uint4 v, int k) { return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w; }
 
 // IQ2_XXS: 32 weights of record j (8 bytes of the row; qw = the 16-byte word of the row that holds it) -> 4 chunks.
-__device__ __forceinline__ void dq_iq2_record(const PFSmem &sm, const BlockRegs &R, uint4 qw, int j, uint8_t *tile,
+__device__ __forceinline__ void dq_iq2_record(const PFSmem &sm, const BlockRegs<DS4G_IQ2_XXS> &R, uint4 qw, int j,
+                                              uint8_t *tile,
                                               int m, int chunk0, int rep8) {
     // record j sits in the row's 16-byte word j & 3, 32-bit words 2 (j >> 2), +1;
     // qw is that 16-byte word
@@ -347,7 +355,8 @@ __device__ __forceinline__ void dq_q2k_sub(const PFSmem &sm, uint32_t W, uint32_
 
 // Q4_K: weights of sub-block j, 8-column chunks cq0 .. cq0 + ncq - 1 of its 4
 // (natural order) -> tile chunks chunk0 + cq, fp32 formula.
-__device__ __forceinline__ void dq_q4k_sub(bool f16, const BlockRegs &R, int j, uint4 qv, uint8_t *tile, int m,
+__device__ __forceinline__ void dq_q4k_sub(bool f16, const BlockRegs<DS4G_Q4_K> &R, int j, uint4 qv, uint8_t *tile,
+                                           int m,
                                            int chunk0, int cq0 = 0, int ncq = 4) {
     const uint32_t s0 = (R.s[0] >> (8 * (j & 3))) & 0xffu;
     const uint32_t s1 = (R.s[1] >> (8 * (j & 3))) & 0xffu;
@@ -378,6 +387,7 @@ __device__ __forceinline__ void dq_q4k_sub(bool f16, const BlockRegs &R, int j, 
 }
 
 // ------------------------------------------------------------------ kernel
+template <int QT>
 __global__ void __launch_bounds__(kPFThreads, 1)
     prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmB16, const __grid_constant__ CUtensorMap tmB32,
                         const __grid_constant__ CUtensorMap tmB64, const __grid_constant__ CUtensorMap tmB128,
@@ -415,7 +425,7 @@ __global__ void __launch_bounds__(kPFThreads, 1)
         tc::tmem_relinquish();
     }
     // lookup tables of the dequantisers
-    if (a.phase == 1 && a.qt == DS4G_IQ2_XXS) {
+    if constexpr (QT == DS4G_IQ2_XXS) {
         for (int i = tid; i < 256; i += kPFThreads) {
             const uint64_t row = a.grid[i];
             uint32_t sel[4];
@@ -447,7 +457,7 @@ __global__ void __launch_bounds__(kPFThreads, 1)
             for (int r = 0; r < 8; ++r) sm.sgn[8 * i + r] = v4;
         }
     }
-    if (a.phase == 2 && a.qt == DS4G_Q2_K) {
+    if constexpr (QT == DS4G_Q2_K) {
         for (int x = tid; x < 256; x += kPFThreads) {
             uint32_t sel[2];
 #pragma unroll
@@ -648,7 +658,7 @@ __global__ void __launch_bounds__(kPFThreads, 1)
         const int par = dq >> 8;               // which half of the stage's work of (m, half)
         const int nblk = a.Kdim / 256;
         uint32_t it = 0;
-        BlockRegs cur, nxt;
+        BlockRegs<QT> cur, nxt;
         // first block of the first task
         int tau = blockIdx.x;
         PFTask t;
@@ -672,7 +682,7 @@ __global__ void __launch_bounds__(kPFThreads, 1)
                 if (kb + 1 < nblk) {
                     if (!t.shared) {
                         load_block(a, mat, r, kb + 1, half, par, nxt);
-                        prefetch_block(a, mat, r, kb + 2, half);
+                        prefetch_block<QT>(a, mat, r, kb + 2, half);
                     }
                 } else if (taun < ntask && !tn.shared) {
                     const uint8_t *matn = (a.phase == 1 && half) ? a.A1[tn.g] : a.A0[tn.g];
@@ -694,20 +704,20 @@ __global__ void __launch_bounds__(kPFThreads, 1)
                             uint8_t *tile = st + half * kTile;
                             // record / sub-block 2 ks + par -> chunks 4 par .. 4 par + 3
                             const int j = 2 * ks + par;
-                            if (a.qt == DS4G_IQ2_XXS) {
+                            if constexpr (QT == DS4G_IQ2_XXS) {
                                 // the row's 16-byte word j & 3 = 2 (ks & 1) + par is held as cur.q[ks & 1]
                                 dq_iq2_record(sm, cur, cur.q[ks & 1], j, tile, m, 4 * par, lane & 7);
-                            } else {
+                            } else if constexpr (QT == DS4G_Q4_K) {
                                 // sub-block j = row word 2 (j & 3) + (j >> 2), held as cur.q[2 (ks & 1) + (ks >> 1)]
                                 dq_q4k_sub(true, cur, j, cur.q[2 * (ks & 1) + (ks >> 1)], tile, m, 4 * par);
                             }
                         } else {
-                            if (a.qt == DS4G_Q2_K) {
+                            if constexpr (QT == DS4G_Q2_K) {
                                 // word ks of this thread's 4 (row word 4 par + ks) -> chunks 4 half + 2 par, + 1
                                 const float d = f16lo(cur.dd), dmin = f16hi(cur.dd);
                                 dq_q2k_sub(sm, word_of(cur, ks), (cur.s[0] >> (8 * ks)) & 255u, d, dmin, st, m,
                                            4 * half + 2 * par, lane & 15);
-                            } else {
+                            } else if constexpr (QT == DS4G_Q4_K) {
                                 // sub-block j = 2 ks + half, chunks 2 par, 2 par + 1 of its 4
                                 const int j = 2 * ks + half;
                                 dq_q4k_sub(true, cur, j, cur.q[2 * (ks & 1) + (ks >> 1)], st, m, 4 * half, 2 * par,
@@ -891,6 +901,23 @@ ds4g_status bucket_launch(const int32_t *ids, int T, int32_t *counts, int32_t *o
 static int g_pf_sms = 0;
 static bool g_pf_attr = false;
 
+// One instance per weight type: IQ2_XXS (gate/up), Q2_K (down), Q4_K (both).
+template <int QT>
+static cudaError_t pf_launch_t(const CUtensorMap (&mB)[4], const CUtensorMap &m0, const CUtensorMap &m1,
+                               const PFArgs &a, cudaStream_t st) {
+    prefill_gemm_kernel<QT><<<g_pf_sms, kPFThreads, kPFSmemBytes, st>>>(mB[0], mB[1], mB[2], mB[3], m0, m1, a);
+    return cudaGetLastError();
+}
+static cudaError_t pf_launch(const CUtensorMap (&mB)[4], const CUtensorMap &m0, const CUtensorMap &m1,
+                             const PFArgs &a, cudaStream_t st) {
+    switch (a.qt) {
+    case DS4G_IQ2_XXS: return pf_launch_t<DS4G_IQ2_XXS>(mB, m0, m1, a, st);
+    case DS4G_Q2_K: return pf_launch_t<DS4G_Q2_K>(mB, m0, m1, a, st);
+    case DS4G_Q4_K: return pf_launch_t<DS4G_Q4_K>(mB, m0, m1, a, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
 // phases: 1 = bucket, permute and gate/up; 2 = down and combine; 3 = both.
 ds4g_status prefill_forward(const float *hidden, int T, const ds4g_layer *L, const int32_t *ids, const float *w,
                             float *out, void *workspace, cudaStream_t st, int phases) {
@@ -901,7 +928,11 @@ ds4g_status prefill_forward(const float *hidden, int T, const ds4g_layer *L, con
             return DS4G_ECUDA;
     }
     if (!g_pf_attr) {
-        if (cudaFuncSetAttribute(prefill_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(prefill_gemm_kernel<DS4G_IQ2_XXS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kPFSmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(prefill_gemm_kernel<DS4G_Q2_K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kPFSmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(prefill_gemm_kernel<DS4G_Q4_K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kPFSmemBytes) != cudaSuccess)
             return DS4G_ECUDA;
         g_pf_attr = true;
@@ -942,8 +973,7 @@ ds4g_status prefill_forward(const float *hidden, int T, const ds4g_layer *L, con
         a.Kdim = kH;
         a.A0 = reinterpret_cast<const uint8_t *const *>(L->gate);
         a.A1 = reinterpret_cast<const uint8_t *const *>(L->up);
-        prefill_gemm_kernel<<<g_pf_sms, kPFThreads, kPFSmemBytes, st>>>(mB[0], mB[1], mB[2], mB[3], mG, mU, a);
-        if (cudaGetLastError() != cudaSuccess) return DS4G_ECUDA;
+        if (pf_launch(mB, mG, mU, a, st) != cudaSuccess) return DS4G_ECUDA;
     }
     if (!(phases & 2)) return DS4G_OK;
     hcast_kernel<<<nrow, 256, 0, st>>>(y, offsets, T, reinterpret_cast<uint16_t *>(hb), hscale, status);
@@ -959,8 +989,7 @@ ds4g_status prefill_forward(const float *hidden, int T, const ds4g_layer *L, con
     a.Kdim = kF;
     a.A0 = reinterpret_cast<const uint8_t *const *>(L->down);
     a.A1 = nullptr;
-    prefill_gemm_kernel<<<g_pf_sms, kPFThreads, kPFSmemBytes, st>>>(mB2[0], mB2[1], mB2[2], mB2[3], mD, mD, a);
-    if (cudaGetLastError() != cudaSuccess) return DS4G_ECUDA;
+    if (pf_launch(mB2, mD, mD, a, st) != cudaSuccess) return DS4G_ECUDA;
     combine_kernel<<<T, 256, 0, st>>>(y, inv, T, out);
     if (cudaGetLastError() != cudaSuccess) return DS4G_ECUDA;
     return DS4G_OK;
