@@ -10,7 +10,8 @@
 //   mid T (9..64): CTA (expert group of 16, 512-column k-slice) with the
 //     slice of x and of R staged in shared memory, one lane per token; a
 //     second launch runs the top-6, one warp per token;
-//   large T: 32-token x 64-expert fp32 SIMT tiles over the full K.
+//   large T: 32-token x 64-expert fp32 SIMT tiles over a quarter of K each
+//     (the whole K above 16384 tokens).
 // Partial logits go to the workspace; the last CTA to finish a token range
 // (atomic ticket, no waiting) sums them in a fixed order and runs the top-k,
 // one warp per token.
@@ -246,17 +247,19 @@ __global__ void __launch_bounds__(256) route_topk_kernel(RouteArgs a) {
     topk_warp(a, t, lg[warp]);
 }
 
-// grid (ceil(T/32), 4), block 128: fp32 tile 32 tokens x 64 experts; thread
-// (ty, tx) accumulates tokens 4ty..4ty+3 x experts 4tx..4tx+3 (16 FMA per
-// two 16-byte shared loads).  Tiles are stored k-major; the next K chunk is
-// loaded into registers while the current one is multiplied.  The last of the
-// four expert tiles of a token tile runs the top-6 of its 32 tokens.
+// grid (ceil(T/32), 4, nks), block 128: fp32 tile 32 tokens x 64 experts over
+// k-slice blockIdx.z of nks; thread (ty, tx) accumulates tokens 4ty..4ty+3 x
+// experts 4tx..4tx+3 (16 FMA per two 16-byte shared loads).  Tiles are stored
+// k-major; the next K chunk is loaded into registers while the current one is
+// multiplied.  Partials part[z][t][e]; the last of the token tile's 4 x nks
+// CTAs adds the slices in order and runs the top-6 of its 32 tokens.
 constexpr int kRouteTiledThreads = 128;
 __global__ void __launch_bounds__(kRouteTiledThreads) route_tiled_kernel(RouteArgs a) {
     __shared__ __align__(16) float xs[2][kTileK][kTileT];
     __shared__ __align__(16) float rs[2][kTileK][kTileE];
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
     const int t0 = blockIdx.x * kTileT, e0 = blockIdx.y * kTileE;
+    const int kn = kH / a.nks, kb0 = blockIdx.z * kn;   // this CTA's k-slice
     // global -> register staging: x tile 32 x 32 (2 float4 per thread), R tile 64 x 32 (4)
     float4 xr[2], rr[4];
     auto load = [&](int k0) {
@@ -291,12 +294,12 @@ __global__ void __launch_bounds__(kRouteTiledThreads) route_tiled_kernel(RouteAr
         }
     };
     float acc[4][4] = {};
-    load(0);
+    load(kb0);
     store(0);
     __syncthreads();
     int buf = 0;
-    for (int k0 = 0; k0 < kH; k0 += kTileK) {
-        const bool more = k0 + kTileK < kH;
+    for (int k0 = kb0; k0 < kb0 + kn; k0 += kTileK) {
+        const bool more = k0 + kTileK < kb0 + kn;
         if (more) load(k0 + kTileK);
 #pragma unroll 8
         for (int kk = 0; kk < kTileK; ++kk) {
@@ -316,7 +319,7 @@ __global__ void __launch_bounds__(kRouteTiledThreads) route_tiled_kernel(RouteAr
     for (int i = 0; i < 4; ++i) {
         const int t = t0 + 4 * ty + i;
         if (t < a.T)
-            *reinterpret_cast<float4 *>(a.part + (size_t)t * kE + e0 + 4 * tx) =
+            *reinterpret_cast<float4 *>(a.part + ((size_t)blockIdx.z * a.T + t) * kE + e0 + 4 * tx) =
                 make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
     }
     __threadfence();
@@ -324,7 +327,7 @@ __global__ void __launch_bounds__(kRouteTiledThreads) route_tiled_kernel(RouteAr
     __syncthreads();
     if (tid == 0) {
         const uint32_t ticket = atomicAdd(a.cnt + blockIdx.x, 1u);
-        last = (ticket == gridDim.y - 1) ? 1u : 0u;
+        last = (ticket == gridDim.y * gridDim.z - 1) ? 1u : 0u;
     }
     __syncthreads();
     if (!last) return;
@@ -335,7 +338,11 @@ __global__ void __launch_bounds__(kRouteTiledThreads) route_tiled_kernel(RouteAr
     for (int tt = warp; tt < kTileT; tt += kW) {
         const int t = t0 + tt;
         if (t >= a.T) break;
-        for (int i = lane; i < kE; i += 32) lg[warp][i] = __ldcg(a.part + (size_t)t * kE + i);
+        for (int i = lane; i < kE; i += 32) {
+            float v = 0.f;
+            for (int z = 0; z < a.nks; ++z) v += __ldcg(a.part + ((size_t)z * a.T + t) * kE + i);
+            lg[warp][i] = v;
+        }
         __syncwarp();
         topk_warp(a, t, lg[warp]);
         __syncwarp();
@@ -347,10 +354,15 @@ __global__ void __launch_bounds__(kRouteTiledThreads) route_tiled_kernel(RouteAr
 
 using namespace ds4g;
 
+// k-slices of the tiled path: 4 up to kTiledSplitMaxT tokens (more CTAs for
+// the SMs), 1 beyond (the partials would grow to 4 KB per token)
+constexpr int kTiledSplitMaxT = 16384;
+static int tiled_nks(int T) { return T <= kTiledSplitMaxT ? 4 : 1; }
+
 static size_t route_part_bytes(int T) {
     if (T <= kRouteFusedTopK) return (size_t)kRouteKS * T * kE * 4;
     if (T <= kRouteSmallT) return (size_t)kMidKS * T * kE * 4;
-    return (size_t)T * kE * 4;
+    return (size_t)tiled_nks(T) * T * kE * 4;
 }
 
 static size_t route_mid_smem(int T) { return ((size_t)T * kMidXLd + (size_t)kMidE * kMidKC) * 4; }
@@ -403,8 +415,8 @@ extern "C" ds4g_status ds4g_moe_route(const float *hidden, int T, const float *r
         route_mid_kernel<<<dim3(kE / kMidE, kMidKS), 128, route_mid_smem(T), st>>>(a);
         route_topk_kernel<<<(T + 7) / 8, 256, 0, st>>>(a);
     } else {
-        a.nks = 1;
-        route_tiled_kernel<<<dim3((unsigned)ntile, kE / kTileE), kRouteTiledThreads, 0, st>>>(a);
+        a.nks = tiled_nks(T);
+        route_tiled_kernel<<<dim3((unsigned)ntile, kE / kTileE, (unsigned)a.nks), kRouteTiledThreads, 0, st>>>(a);
     }
     return cudaGetLastError() == cudaSuccess ? DS4G_OK : DS4G_ECUDA;
 }
