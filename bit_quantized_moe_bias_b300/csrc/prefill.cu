@@ -312,10 +312,12 @@ __device__ __forceinline__ uint32_t word_of(const BlockRegs<QT> &R, int i) {
 }
 __device__ __forceinline__ uint32_t word4(uint4 v, int k) { return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w; }
 
-// IQ2_XXS: 32 weights of record j (8 bytes of the row; qw = the 16-byte word of the row that holds it) -> 4 chunks.
+// IQ2_XXS: the 32 weights of record j (8 bytes of the row; qw = the 16-byte
+// word of the row that holds it) as 4 chunks of 8 fp16 values.  It reads only
+// the lookup tables, so the dequantisers build a stage's chunks before they
+// wait for the stage to be free, and only store them after.
 __device__ __forceinline__ void dq_iq2_record(const PFSmem &sm, const BlockRegs<DS4G_IQ2_XXS> &R, uint4 qw, int j,
-                                              uint8_t *tile,
-                                              int m, int chunk0, int rep8) {
+                                              int rep8, uint4 (&o)[4]) {
     // record j sits in the row's 16-byte word j & 3, 32-bit words 2 (j >> 2), +1;
     // qw is that 16-byte word
     const uint32_t ia = word4(qw, 2 * (j >> 2)), v = word4(qw, 2 * (j >> 2) + 1);
@@ -327,12 +329,10 @@ __device__ __forceinline__ void dq_iq2_record(const PFSmem &sm, const BlockRegs<
     for (int l = 0; l < 4; ++l) {
         const uint4 sel = sm.sel[8 * ((ia >> (8 * l)) & 255u) + rep8];
         const uint4 sg = sm.sgn[8 * ((v >> (7 * l)) & 127u) + rep8];
-        uint4 o;
-        o.x = prmt(rlo, rhi, sel.x) ^ sg.x;
-        o.y = prmt(rlo, rhi, sel.y) ^ sg.y;
-        o.z = prmt(rlo, rhi, sel.z) ^ sg.z;
-        o.w = prmt(rlo, rhi, sel.w) ^ sg.w;
-        sts128(tile, m, chunk0 + l, o);
+        o[l].x = prmt(rlo, rhi, sel.x) ^ sg.x;
+        o[l].y = prmt(rlo, rhi, sel.y) ^ sg.y;
+        o[l].z = prmt(rlo, rhi, sel.z) ^ sg.z;
+        o[l].w = prmt(rlo, rhi, sel.w) ^ sg.w;
     }
 }
 
@@ -693,6 +693,11 @@ __global__ void __launch_bounds__(kPFThreads, 1)
                     const int s = (it + ks) % kStages;
                     const uint32_t ph = ((it + ks) / kStages) & 1u;
                     if (!ok) continue;
+                    uint4 o[4];   // IQ2_XXS: this stage's chunks, built before the wait
+                    if constexpr (QT == DS4G_IQ2_XXS) {
+                        // record 2 ks + par: the row's 16-byte word 2 (ks & 1) + par, held as cur.q[ks & 1]
+                        if (!t.shared) dq_iq2_record(sm, cur, cur.q[ks & 1], 2 * ks + par, lane & 7, o);
+                    }
                     if (!pf_wait_fast(&sm.empty[s], ph ^ 1u, abort_flag)) {
                         pf_abort(a, sm.abort_flag, 0x400u);
                         ok = false;
@@ -705,8 +710,8 @@ __global__ void __launch_bounds__(kPFThreads, 1)
                             // record / sub-block 2 ks + par -> chunks 4 par .. 4 par + 3
                             const int j = 2 * ks + par;
                             if constexpr (QT == DS4G_IQ2_XXS) {
-                                // the row's 16-byte word j & 3 = 2 (ks & 1) + par is held as cur.q[ks & 1]
-                                dq_iq2_record(sm, cur, cur.q[ks & 1], j, tile, m, 4 * par, lane & 7);
+#pragma unroll
+                                for (int l = 0; l < 4; ++l) sts128(tile, m, 4 * par + l, o[l]);
                             } else if constexpr (QT == DS4G_Q4_K) {
                                 // sub-block j = row word 2 (j & 3) + (j >> 2), held as cur.q[2 (ks & 1) + (ks >> 1)]
                                 dq_q4k_sub(true, cur, j, cur.q[2 * (ks & 1) + (ks >> 1)], tile, m, 4 * par);
