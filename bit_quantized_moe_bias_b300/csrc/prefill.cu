@@ -336,10 +336,11 @@ __device__ __forceinline__ void dq_iq2_record(const PFSmem &sm, const BlockRegs<
     }
 }
 
-// Q2_K: 16 weights of one sub-block (word W, scale byte scb) -> 2 chunks in
-// the K-order (0,2,4,...,14,1,3,...,15).
+// Q2_K: 16 weights of one sub-block (word W, scale byte scb) as 2 chunks (o[0],
+// o[1]) in the K-order (0,2,4,...,14,1,3,...,15); like the IQ2_XXS records,
+// built before the stage wait and stored after it.
 __device__ __forceinline__ void dq_q2k_sub(const PFSmem &sm, uint32_t W, uint32_t scb, float d, float dmin,
-                                           uint8_t *tile, int m, int chunk0, int rep16) {
+                                           int rep16, uint4 (&o)[4]) {
     const float dsc = __fmul_rn(d, (float)(scb & 15u));
     const float dm = __fmul_rn(dmin, (float)(scb >> 4));
     uint32_t rlo, rhi;
@@ -347,10 +348,8 @@ __device__ __forceinline__ void dq_q2k_sub(const PFSmem &sm, uint32_t W, uint32_
            __fmaf_rn(dsc, 3.0f, -dm), rlo, rhi);
     const uint2 s0 = sm.q2lut[16 * (W & 255u) + rep16], s1 = sm.q2lut[16 * ((W >> 8) & 255u) + rep16];
     const uint2 s2 = sm.q2lut[16 * ((W >> 16) & 255u) + rep16], s3 = sm.q2lut[16 * (W >> 24) + rep16];
-    sts128(tile, m, chunk0,
-           make_uint4(prmt(rlo, rhi, s0.x), prmt(rlo, rhi, s0.y), prmt(rlo, rhi, s1.x), prmt(rlo, rhi, s1.y)));
-    sts128(tile, m, chunk0 + 1,
-           make_uint4(prmt(rlo, rhi, s2.x), prmt(rlo, rhi, s2.y), prmt(rlo, rhi, s3.x), prmt(rlo, rhi, s3.y)));
+    o[0] = make_uint4(prmt(rlo, rhi, s0.x), prmt(rlo, rhi, s0.y), prmt(rlo, rhi, s1.x), prmt(rlo, rhi, s1.y));
+    o[1] = make_uint4(prmt(rlo, rhi, s2.x), prmt(rlo, rhi, s2.y), prmt(rlo, rhi, s3.x), prmt(rlo, rhi, s3.y));
 }
 
 // Q4_K: weights of sub-block j, 8-column chunks cq0 .. cq0 + ncq - 1 of its 4
@@ -693,10 +692,15 @@ __global__ void __launch_bounds__(kPFThreads, 1)
                     const int s = (it + ks) % kStages;
                     const uint32_t ph = ((it + ks) / kStages) & 1u;
                     if (!ok) continue;
-                    uint4 o[4];   // IQ2_XXS: this stage's chunks, built before the wait
+                    uint4 o[4];   // IQ2_XXS / Q2_K: this stage's chunks, built before the wait
                     if constexpr (QT == DS4G_IQ2_XXS) {
                         // record 2 ks + par: the row's 16-byte word 2 (ks & 1) + par, held as cur.q[ks & 1]
                         if (!t.shared) dq_iq2_record(sm, cur, cur.q[ks & 1], 2 * ks + par, lane & 7, o);
+                    } else if constexpr (QT == DS4G_Q2_K) {
+                        // word ks of this thread's 4 (row word 4 par + ks)
+                        if (!t.shared)
+                            dq_q2k_sub(sm, word_of(cur, ks), (cur.s[0] >> (8 * ks)) & 255u, f16lo(cur.dd),
+                                       f16hi(cur.dd), lane & 15, o);
                     }
                     if (!pf_wait_fast(&sm.empty[s], ph ^ 1u, abort_flag)) {
                         pf_abort(a, sm.abort_flag, 0x400u);
@@ -718,10 +722,9 @@ __global__ void __launch_bounds__(kPFThreads, 1)
                             }
                         } else {
                             if constexpr (QT == DS4G_Q2_K) {
-                                // word ks of this thread's 4 (row word 4 par + ks) -> chunks 4 half + 2 par, + 1
-                                const float d = f16lo(cur.dd), dmin = f16hi(cur.dd);
-                                dq_q2k_sub(sm, word_of(cur, ks), (cur.s[0] >> (8 * ks)) & 255u, d, dmin, st, m,
-                                           4 * half + 2 * par, lane & 15);
+                                // -> chunks 4 half + 2 par, + 1
+                                sts128(st, m, 4 * half + 2 * par, o[0]);
+                                sts128(st, m, 4 * half + 2 * par + 1, o[1]);
                             } else if constexpr (QT == DS4G_Q4_K) {
                                 // sub-block j = 2 ks + half, chunks 2 par, 2 par + 1 of its 4
                                 const int j = 2 * ks + half;
