@@ -712,12 +712,12 @@ __global__ void __launch_bounds__(kPFThreads, 1)
                         if (a.phase == 1) {
                             uint8_t *tile = st + half * kTile;
                             // record / sub-block 2 ks + par -> chunks 4 par .. 4 par + 3
-                            const int j = 2 * ks + par;
                             if constexpr (QT == DS4G_IQ2_XXS) {
 #pragma unroll
                                 for (int l = 0; l < 4; ++l) sts128(tile, m, 4 * par + l, o[l]);
                             } else if constexpr (QT == DS4G_Q4_K) {
                                 // sub-block j = row word 2 (j & 3) + (j >> 2), held as cur.q[2 (ks & 1) + (ks >> 1)]
+                                const int j = 2 * ks + par;
                                 dq_q4k_sub(true, cur, j, cur.q[2 * (ks & 1) + (ks >> 1)], tile, m, 4 * par);
                             }
                         } else {
