@@ -54,13 +54,25 @@ extern "C" const char *ds4g_status_str(ds4g_status s) {
     return "unknown status";
 }
 
-extern "C" size_t ds4g_forward_workspace(int T) {
+// Bytes a call with exactly T tokens needs (the path T selects).
+static size_t forward_ws_need(int T) {
     if (T < 1) return 0;
     if (T >= kPrefillMinT) return prefill_workspace(T);
     const size_t dec = decode_workspace(T < kDecodeMaxT ? T : kDecodeMaxT);
     if (T <= kDecodeMaxT) return dec;
     const size_t bat = batch_workspace(T);   // IQ2_XXS/Q2_K layers; Q4_K layers take the decode path
     return bat > dec ? bat : dec;
+}
+
+// The most any call with 1..T tokens needs: each path's need grows with T,
+// so the maximum is over T and the largest T of every path below it.
+extern "C" size_t ds4g_forward_workspace(int T) {
+    if (T < 1) return 0;
+    size_t n = forward_ws_need(T);
+    const int tops[2] = {kDecodeMaxT, kPrefillMinT - 1};
+    for (int i = 0; i < 2; ++i)
+        if (tops[i] < T && forward_ws_need(tops[i]) > n) n = forward_ws_need(tops[i]);
+    return n;
 }
 
 static bool types_ok(const ds4g_layer *L) {
@@ -80,7 +92,7 @@ static ds4g_status check_forward_args(const float *hidden, int T, const ds4g_lay
                          (uintptr_t)L->down | (uintptr_t)L->sh_gate | (uintptr_t)L->sh_up |
                          (uintptr_t)L->sh_down | (uintptr_t)L->iq2_grid;
     if (al & 15) return DS4G_EALIGN;
-    if (ws_bytes < ds4g_forward_workspace(T)) return DS4G_ENOSPACE;
+    if (ws_bytes < forward_ws_need(T)) return DS4G_ENOSPACE;
     return DS4G_OK;
 }
 

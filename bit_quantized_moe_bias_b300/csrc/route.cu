@@ -372,9 +372,17 @@ static size_t route_mid_smem(int T) { return ((size_t)T * kMidXLd + (size_t)kMid
 // (zero) counters should be; partials after them.
 constexpr size_t kRouteCntBytes = ((size_t)(DS4G_ROUTE_MAX_T / kTileT + 1) * 4 + 255) / 256 * 256;
 
+static size_t route_ws_need(int T) { return kWsHeader + kRouteCntBytes + align_up(route_part_bytes(T), 256); }
+
+// The most any call with 1..T tokens needs: the partials of each path grow
+// with T, so the maximum is over T and the largest T of every path below it.
 extern "C" size_t ds4g_route_workspace(int T) {
     if (T < 1 || T > DS4G_ROUTE_MAX_T) return 0;
-    return kWsHeader + kRouteCntBytes + align_up(route_part_bytes(T), 256);
+    size_t n = route_ws_need(T);
+    const int tops[3] = {kRouteFusedTopK, kRouteSmallT, kTiledSplitMaxT};
+    for (int i = 0; i < 3; ++i)
+        if (tops[i] < T && route_ws_need(tops[i]) > n) n = route_ws_need(tops[i]);
+    return n;
 }
 
 extern "C" ds4g_status ds4g_moe_route(const float *hidden, int T, const float *router,
@@ -386,7 +394,7 @@ extern "C" ds4g_status ds4g_moe_route(const float *hidden, int T, const float *r
     if (((uintptr_t)hidden | (uintptr_t)router | (uintptr_t)bias | (uintptr_t)ids | (uintptr_t)w |
          (uintptr_t)workspace) & 15)
         return DS4G_EALIGN;
-    if (ws_bytes < ds4g_route_workspace(T)) return DS4G_ENOSPACE;
+    if (ws_bytes < route_ws_need(T)) return DS4G_ENOSPACE;
     RouteArgs a;
     a.x = hidden;
     a.T = T;

@@ -147,7 +147,9 @@ ds4g_status ds4g_dequantize(ds4g_qtype t, const void *packed, int rows, int cols
  * ds4g_route_workspace(T) bytes (the status word, ticket counters and the
  * logits), zeroed once before first use: the kernels leave the counters at
  * zero, and they sit at the same offsets for every T, so one workspace
- * serves calls with any T it is large enough for.
+ * serves calls with any T it is large enough for.  ds4g_route_workspace(T)
+ * is the most that any call with 1..T tokens needs (non-decreasing in T), so
+ * a workspace sized for the largest T serves every smaller call.
  * 1 <= T <= DS4G_ROUTE_MAX_T, else DS4G_EINVAL / DS4G_EUNSUPPORTED
  * (ds4g_route_workspace returns 0 outside that range).
  * ------------------------------------------------------------------------ */
@@ -230,6 +232,9 @@ typedef struct {
  * in one area at fixed offsets after the status word, which every kernel
  * leaves at zero and no call uses as scratch; so one workspace, large enough
  * for each call, serves any sequence of these calls and token counts.
+ * ds4g_forward_workspace(T) is the most that any call with 1..T tokens needs
+ * (non-decreasing in T, across the three paths), so a workspace sized for the
+ * largest T serves every smaller call.
  * ------------------------------------------------------------------------ */
 size_t ds4g_forward_workspace(int T);
 ds4g_status ds4g_moe_forward(const float *hidden, int T, const ds4g_layer *L,

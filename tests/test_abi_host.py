@@ -167,10 +167,18 @@ def test_decode_stack_validates_layer_types_and_workspace():
 
 
 def test_workspace_sizes_grow_with_T():
+    """A workspace sized for T tokens serves every call with 1..T tokens: both
+    size queries are non-decreasing in T, across the paths' boundaries (per-slot
+    decode / batched / prefill for the forward; small / mid / tiled router)."""
     assert B.ds4g_route_workspace(0) == 0
     assert B.ds4g_route_workspace(1) < B.ds4g_route_workspace(2048)
     assert 0 < B.ds4g_forward_workspace(1) <= B.ds4g_forward_workspace(3)
     assert B.ds4g_bucket_workspace(1) >= 256
+    L = B.lib()
+    Ts = list(range(1, 140)) + [255, 256, 1000, 2048, 4096, 16383, 16384, 16385, 20000, 65536, 65537]
+    for f in (L.ds4g_forward_workspace, L.ds4g_route_workspace):
+        sizes = [f(T) for T in Ts]
+        assert all(b >= a for a, b in zip(sizes, sizes[1:])), f
 
 
 def test_status_strings():
@@ -214,3 +222,4 @@ def test_expert_file_layout_and_header_checks(tmp_path):
     (tmp_path / "short.ds4gexp").write_bytes(raw[:4096 + stride])   # truncated
     assert L.ds4g_expert_file_open(os.fsencode(tmp_path / "short.ds4gexp"), C.byref(h)) == 1
     assert L.ds4g_expert_file_open(os.fsencode(tmp_path / "none.ds4gexp"), C.byref(h)) == 1
+
